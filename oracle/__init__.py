@@ -1,0 +1,205 @@
+"""fp64 CPU oracle for streaming log-domain Sinkhorn (squared-Euclidean entropic OT).
+
+TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the benchmark's CPU
+baseline leg may import this package. The product path (the CUDA library and its Python
+binding) never imports, links or executes anything here, and this package imports
+nothing from the product path.
+
+The arithmetic lives in ``sinkhorn_oracle.c`` (plain loops, fp64, OpenMP over output
+rows); this module compiles it with gcc on first use and wraps it with numpy. All
+inputs are promoted to fp64 before the call (fp32 -> fp64 is exact).
+
+Parity status of each function (what pins it, in tests/test_oracle_pins.py):
+  half_step_f / half_step_g  marginal identities, the attention-form (LSE-rewrite)
+                             identity, n=1 closed form, two-point closed form.
+  solve / dual_loss          two-point closed form, eps->inf closed form, eps->0
+                             brute-force assignment bound, 1-D sorted-matching bound,
+                             strong duality, monotone dual ascent, invariances.
+  grad_x                     central finite differences of the converged loss,
+                             two-point closed form.
+  transport_apply            marginals (P1 = a after F, P^T 1 = b after G), adjointness,
+                             the gradient identity grad_i = 2(a_i x_i - (P~ Y)_i).
+  hadamard_xy                h_i = <x_i, (P Y)_i> and d/dt OT(X, tY) finite difference.
+  marginals                  row sums = a after F and column sums = b after G.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sinkhorn_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LOCK = threading.Lock()
+_LIB = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i64 = ctypes.c_int64
+
+
+def lib_path() -> str:
+    return os.path.join(_BUILD_DIR, f"liboracle_{platform.machine()}.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2 -fopenmp, IEEE fp64, no fast-math)."""
+    out = lib_path()
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_half_step.argtypes = [_dp, _i64, _dp, _i64, _i64, _dp, _dp,
+                                             ctypes.c_double, _i64p, _i64, _dp]
+            lib.oracle_half_step.restype = None
+            lib.oracle_dual_loss.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64]
+            lib.oracle_dual_loss.restype = ctypes.c_double
+            lib.oracle_solve.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _dp,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         _dp, _dp, _dp]
+            lib.oracle_solve.restype = ctypes.c_int
+            lib.oracle_transport_apply.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
+                                                   _i64, ctypes.c_double, _dp, _i64,
+                                                   ctypes.c_int, _i64p, _i64, _dp]
+            lib.oracle_transport_apply.restype = None
+            lib.oracle_hadamard_xy.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
+                                               _i64, ctypes.c_double, _i64p, _i64, _dp]
+            lib.oracle_hadamard_xy.restype = None
+            lib.oracle_grad_x.argtypes = [_dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                          ctypes.c_double, _i64p, _i64, _dp]
+            lib.oracle_grad_x.restype = None
+            lib.oracle_marginals.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                             ctypes.c_double, _dp, _dp]
+            lib.oracle_marginals.restype = None
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _LIB = lib
+    return _LIB
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _p(x: np.ndarray):
+    return x.ctypes.data_as(_dp)
+
+
+def _rows(rows, count):
+    if rows is None:
+        return None, count, None
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    if r.size and (r.min() < 0 or r.max() >= count):
+        raise IndexError("row index out of range")
+    return r.ctypes.data_as(_i64p), int(r.size), r
+
+
+def num_threads() -> int:
+    return int(_lib().oracle_num_threads())
+
+
+def half_step_f(X, Y, b, g, eps, rows=None) -> np.ndarray:
+    """f_i = -eps log sum_j b_j exp((g_j - |x_i - y_j|^2)/eps) (all rows or ``rows``)."""
+    X, Y, b, g = _f64(X), _f64(Y), _f64(b), _f64(g)
+    n, d = X.shape
+    m = Y.shape[0]
+    rp, nr, keep = _rows(rows, n)
+    out = np.empty(nr, dtype=np.float64)
+    _lib().oracle_half_step(_p(X), n, _p(Y), m, d, _p(b), _p(g), float(eps), rp, nr, _p(out))
+    return out
+
+
+def half_step_g(X, Y, a, f, eps, rows=None) -> np.ndarray:
+    """g_j = -eps log sum_i a_i exp((f_i - |x_i - y_j|^2)/eps) (all columns or ``rows``)."""
+    X, Y, a, f = _f64(X), _f64(Y), _f64(a), _f64(f)
+    n, d = X.shape
+    m = Y.shape[0]
+    rp, nr, keep = _rows(rows, m)
+    out = np.empty(nr, dtype=np.float64)
+    _lib().oracle_half_step(_p(Y), m, _p(X), n, d, _p(a), _p(f), float(eps), rp, nr, _p(out))
+    return out
+
+
+def dual_loss(a, b, f, g) -> float:
+    a, b, f, g = _f64(a), _f64(b), _f64(f), _f64(g)
+    return float(_lib().oracle_dual_loss(_p(a), _p(b), _p(f), _p(g), a.size, b.size))
+
+
+def solve(X, Y, a, b, eps_schedule, iters_per_stage, g0=None):
+    """Alternating log-domain Sinkhorn. Returns (f, g, loss) in fp64."""
+    X, Y, a, b = _f64(X), _f64(Y), _f64(a), _f64(b)
+    n, d = X.shape
+    m = Y.shape[0]
+    sched = _f64(np.atleast_1d(eps_schedule))
+    f = np.zeros(n, dtype=np.float64)
+    g = np.zeros(m, dtype=np.float64) if g0 is None else _f64(g0).copy()
+    loss = ctypes.c_double(0.0)
+    _lib().oracle_solve(_p(X), _p(Y), _p(a), _p(b), n, m, d, _p(sched), int(sched.size),
+                        int(iters_per_stage), 0 if g0 is None else 1, _p(f), _p(g),
+                        ctypes.byref(loss))
+    return f, g, float(loss.value)
+
+
+def transport_apply(X, Y, a, b, f, g, eps, V, transpose=False, rows=None) -> np.ndarray:
+    """P V (n x k) or, with transpose, P^T V (m x k; V is then n x k)."""
+    X, Y, a, b, f, g, V = map(_f64, (X, Y, a, b, f, g, V))
+    n, d = X.shape
+    m = Y.shape[0]
+    k = V.shape[1]
+    rp, nr, keep = _rows(rows, m if transpose else n)
+    out = np.empty((nr, k), dtype=np.float64)
+    _lib().oracle_transport_apply(_p(X), _p(Y), _p(a), _p(b), _p(f), _p(g), n, m, d,
+                                  float(eps), _p(V), k, 1 if transpose else 0, rp, nr, _p(out))
+    return out
+
+
+def hadamard_xy(X, Y, a, b, f, g, eps, rows=None) -> np.ndarray:
+    """h_i = sum_j P_ij <x_i, y_j>."""
+    X, Y, a, b, f, g = map(_f64, (X, Y, a, b, f, g))
+    n, d = X.shape
+    m = Y.shape[0]
+    rp, nr, keep = _rows(rows, n)
+    out = np.empty(nr, dtype=np.float64)
+    _lib().oracle_hadamard_xy(_p(X), _p(Y), _p(a), _p(b), _p(f), _p(g), n, m, d, float(eps),
+                              rp, nr, _p(out))
+    return out
+
+
+def grad_x(X, Y, a, b, g, eps, rows=None) -> np.ndarray:
+    """grad_i = sum_j P~_ij 2 (x_i - y_j) with f~ = F(g)."""
+    X, Y, a, b, g = map(_f64, (X, Y, a, b, g))
+    n, d = X.shape
+    m = Y.shape[0]
+    rp, nr, keep = _rows(rows, n)
+    out = np.empty((nr, d), dtype=np.float64)
+    _lib().oracle_grad_x(_p(X), _p(Y), _p(a), _p(b), _p(g), n, m, d, float(eps), rp, nr,
+                         _p(out))
+    return out
+
+
+def marginals(X, Y, a, b, f, g, eps):
+    """Row sums P 1 and column sums P^T 1 of the plan defined by (f, g)."""
+    X, Y, a, b, f, g = map(_f64, (X, Y, a, b, f, g))
+    n, d = X.shape
+    m = Y.shape[0]
+    r = np.empty(n, dtype=np.float64)
+    c = np.empty(m, dtype=np.float64)
+    _lib().oracle_marginals(_p(X), _p(Y), _p(a), _p(b), _p(f), _p(g), n, m, d, float(eps),
+                            _p(r), _p(c))
+    return r, c

@@ -1,0 +1,48 @@
+"""Planted-mistake check for the oracle pins (CPU only).
+
+Each case copies the oracle source into a temporary directory, plants one plausible
+mistake (a dropped term, a wrong sign or factor, a transposed index, a swapped update
+order), rebuilds it there and runs the pin suite against the copy. Every mutant must
+fail at least one pin; the real oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "half_cost": ("s += t * t;", "s += 0.5 * t * t;"),
+    "drop_log_weight": ("/ eps + log(w[q]);", "/ eps;"),
+    "potential_sign": ("(h[q] - sq_cost(p, Q + q * d, d))", "(-h[q] - sq_cost(p, Q + q * d, d))"),
+    "drop_eps_scale": ("-eps * (mx + log(s))", "-(mx + log(s))"),
+    "loss_drops_g": ("s += b[j] * g[j];", "s += 0.0;"),
+    "grad_sign": ("2.0 * (xi[c] - yj[c])", "2.0 * (yj[c] - xi[c])"),
+    "apply_wrong_index": ("dst[c] += p * V[j * k + c];", "dst[c] += p * V[o * k + c];"),
+    "plan_drops_b": ("return ai * bj * exp", "return ai * exp"),
+    "hadamard_self_dot": ("dot += xi[c] * yj[c];", "dot += xi[c] * xi[c];"),
+    "g_update_first": (
+        "oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, f);\n"
+        "            oracle_half_step(Y, m, X, n, d, a, f, eps, NULL, m, g);",
+        "oracle_half_step(Y, m, X, n, d, a, f, eps, NULL, m, g);\n"
+        "            oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, f);"),
+    "row_sum_scaled": ("row_sums[i] = s;", "row_sums[i] = s * 1.0000001;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(os.path.join(ROOT, "oracle", "sinkhorn_oracle.c")).read()
+    assert old in src, f"mutation site for {name} no longer exists"
+    ign = shutil.ignore_patterns("_build", "__pycache__")
+    for sub in ("oracle", "workloads", "tests"):
+        shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub, ignore=ign)
+    shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path)
+    (tmp_path / "oracle" / "sinkhorn_oracle.c").write_text(src.replace(old, new, 1))
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-q", "-x"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 1, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
