@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the streaming log-domain Sinkhorn hot path on GB300.
+
+One step = one pass of the whole hot path over the 50k x 50k, d = 512 point-cloud workload
+(X, Y ~ N(0, I/d), uniform weights, eps = 0.1): pack + 100 alternating f/g iterations +
+dual loss, the barycentric gradient w.r.t. X, transport application P V and P^T U with
+k = 128 columns, and the Hadamard-weighted transport (P .* X Y^T) 1. The headline metric is
+Sinkhorn iterations per second (and score evaluations per second); the dominant kernel
+(the streaming LSE half-step) is also reported against the measured tensor-core peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--precision bf16|tf32]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, bounded sample, host cores
+
+Under torchrun (N > 1) every rank solves its own replica of the problem (the method has
+no data-path exchange to shard a single solve across GPUs here); the value is the sum.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Sinkhorn iters/sec & score evals/s at n=m=50k vs oracle; % of GB300 roofline"
+UNIT = "iters/s"
+WORKLOAD_IDX = 3
+K_APPLY = 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25 -> tf32 peak = bf16 x 1.1/2.25.
+TF32_OVER_BF16 = 1.1 / 2.25
+L2_FLUSH_BYTES = 256 << 20
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["flashot", "reference"], default="flashot")
+    p.add_argument("--precision", choices=["bf16", "tf32"], default="bf16")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if args.steps < 1:
+        p.error("--steps must be >= 1")
+    return args
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(prec, accumulate="f32 scores/LSE, f64 loss"):
+    return {
+        "workload": "pc50k_d512_grad: n=m=50000, d=512, X,Y~N(0,I/d) fp32, uniform weights, "
+                    "eps=0.1, 100 alternating iterations + dual loss + grad wrt X + P.V and "
+                    "P^T.U (k=128) + Hadamard (P.*XY^T)1",
+        "n": 50000, "m": 50000, "d": 512, "iters": 100, "k_apply": K_APPLY,
+        "contraction": prec, "accumulate": accumulate,
+        "l2": "flushed before every step (256 MiB write inside the timed region); "
+              "working set 2x51 MB bf16 operands",
+        "seed": 1000 + WORKLOAD_IDX,
+    }
+
+
+# ---------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs (read-only query)."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the same workload
+# ---------------------------------------------------------------------------------------
+def oracle_sample(pr, target_s=10.0):
+    """Time the oracle's f-update on a subset of rows of the full workload and extrapolate
+    to iterations per second of the whole problem (one iteration = an f-update over n rows
+    plus a g-update over m rows, each against the full other cloud)."""
+    import numpy as np
+
+    import oracle
+    g = np.zeros(pr.m)
+    eps = float(pr.eps_schedule[0])
+    r = 4 * oracle.num_threads()
+    while True:
+        rows = np.linspace(0, pr.n - 1, r).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.half_step_f(pr.X, pr.Y, pr.b, g, eps, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * target_s or r >= pr.n:
+            break
+        r = int(min(pr.n, max(2 * r, r * 0.8 * target_s / max(dt, 1e-3))))
+    per_row = dt / r
+    iter_s = per_row * pr.n + per_row * pr.m  # n = m rows of equal cost for the g-update
+    return {"value": 1.0 / iter_s, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"f-update of {r} of {pr.n} rows against all {pr.m} columns (d={pr.d}, "
+                      f"fp64), {dt:.1f} s; iteration time extrapolated as (n+m) x per-row time"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import workload
+    pr = workload(WORKLOAD_IDX)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        s = oracle_sample(pr, target_s=8.0)
+        if i >= args.warmup:
+            samples.append(s)
+    vals = [s["value"] for s in samples]
+    v = statistics.median(vals)
+    iter_s = 1.0 / v
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": iter_s * 100 * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same generator as the GPU arm)",
+        "config": workload_config("f64", "f64 (CPU oracle, dense loops, no tiling)"),
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": samples[-1]["cores"],
+                         "kind": "oracle", "sample": samples[-1]["sample"]},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "fp64 plain-loop CPU oracle timed on the host cores; one step = 100 "
+                "iterations, extrapolated from a bounded row sample per step",
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "log_domain_sinkhorn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode())
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(prec):
+    """DRAM bytes per launch of the LSE kernel from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "lse_tc_kernel_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    ent = rec.get(prec)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_full_launch")
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    from workloads import workload
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    prec = args.precision
+
+    pr = workload(WORKLOAD_IDX)
+    n, m, d = pr.n, pr.m, pr.d
+    eps = float(pr.eps_schedule[0])
+    iters = pr.iters_per_stage
+    X = torch.from_numpy(pr.X).to(dev)
+    Y = torch.from_numpy(pr.Y).to(dev)
+    V = torch.from_numpy(pr.V).to(dev)
+    U = torch.from_numpy(pr.U).to(dev)
+    ws = lds.Workspace(lds.workspace_bytes(n, m, d, K_APPLY, prec))
+    f = torch.empty(n, device=dev)
+    g = torch.empty(m, device=dev)
+    loss = torch.empty((), dtype=torch.float64, device=dev)
+    grad = torch.empty((n, d), device=dev)
+    PV = torch.empty((n, K_APPLY), device=dev)
+    PtU = torch.empty((m, K_APPLY), device=dev)
+    h = torch.empty(n, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(Xs, Ys, Vs, Us):
+        flush.zero_()
+        lds.sinkhorn_solve(Xs, Ys, None, None, eps, iters, precision=prec, f_out=f, g_out=g,
+                           loss_out=loss, workspace=ws)
+        lds.ot_grad_x(Xs, Ys, g, eps, precision=prec, out=grad, workspace=ws, reuse_pack=True)
+        lds.transport_apply(Xs, Ys, f, g, eps, Vs, precision=prec, out=PV, workspace=ws,
+                            reuse_pack=True)
+        lds.transport_apply(Xs, Ys, f, g, eps, Us, transpose=True, precision=prec, out=PtU,
+                            workspace=ws, reuse_pack=True)
+        lds.transport_hadamard_xy(Xs, Ys, f, g, eps, precision=prec, out=h, workspace=ws,
+                                  reuse_pack=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step(X, Y, V, U)
+    torch.cuda.synchronize()
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device timeout during warm-up")
+
+    # ---- timed region: inputs resident in HBM --------------------------------------------
+    timer = lds.KernelTimer(cap=args.steps * 600).start()
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = lds.launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(X, Y, V, U)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = lds.launch_count() - launches0
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    n_lse, ms_lse = timer.read(lds.KernelTimer.LSE)
+    n_ws, ms_ws = timer.read(lds.KernelTimer.WSUM)
+    n_ot, ms_ot = timer.read(lds.KernelTimer.OTHER)
+    timer.stop()
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("a kernel reported a device timeout in the timed region")
+
+    total_iters = args.steps * iters * world
+    value = total_iters / (ms / 1e3)
+    nm = float(n) * float(m)
+    scores_per_step = (2 * iters + 5) * nm  # solve + grad (2 passes) + 2 applies + Hadamard
+    score_evals = scores_per_step * args.steps * world / (ms / 1e3)
+
+    peaks, peak_src = load_peaks()
+    bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak = bf16_sus if prec == "bf16" else bf16_sus * TF32_OVER_BF16
+    lse_avg_ms = ms_lse / max(n_lse, 1)
+    flops_per_launch = 2.0 * nm * d
+    achieved = flops_per_launch / (lse_avg_ms / 1e3) / 1e12
+    traffic = profiled_traffic(prec)
+
+    # ---- end to end through the public API with host buffers -----------------------------
+    e2e = None
+    if not args.no_e2e:
+        hX = torch.from_numpy(pr.X).pin_memory()
+        hY = torch.from_numpy(pr.Y).pin_memory()
+        hV = torch.from_numpy(pr.V).pin_memory()
+        hU = torch.from_numpy(pr.U).pin_memory()
+        dX, dY, dV, dU = (torch.empty_like(t, device=dev) for t in (hX, hY, hV, hU))
+        outs_d = (f, g, loss, grad, PV, PtU, h)
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs_d]
+        h2d = sum(t.numel() * t.element_size() for t in (hX, hY, hV, hU))
+        d2h = sum(t.numel() * t.element_size() for t in outs_d)
+
+        def e2e_step():
+            for dst, src in ((dX, hX), (dY, hY), (dV, hV), (dU, hU)):
+                dst.copy_(src, non_blocking=True)
+            step(dX, dY, dV, dU)
+            for dst, src in zip(outs_h, outs_d):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = max_over_ranks(t0.elapsed_time(t1))
+        e2e = {"value": total_iters / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps,
+               "note": "pinned host -> device copy of X, Y, V, U, the step, device -> host "
+                       "copy of f, g, loss, grad, P.V, P^T.U, h; all inside the timed region"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(pr)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": prec, "data": "synthetic (seeded numpy PCG64, N(0,I/d) point clouds)",
+            "config": workload_config(prec),
+            "score_evals_per_s": score_evals,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "lse_tc_kernel (streaming LSE half-step)",
+                         "algorithmic_flops_per_launch": flops_per_launch,
+                         "avg_launch_ms": lse_avg_ms, "launches_timed": n_lse,
+                         "peak_source": f"{peak_src} bf16_tflops_sustained"
+                                        + ("" if prec == "bf16" else " x 1.1/2.25 (tf32)")},
+            "kernels_ms_per_step": {"lse": ms_lse / args.steps, "wsum": ms_ws / args.steps,
+                                    "other": ms_ot / args.steps,
+                                    "launches_per_step": {"lse": n_lse / args.steps,
+                                                          "wsum": n_ws / args.steps,
+                                                          "other": n_ot / args.steps}},
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": int(launches),
+            "cpu_baseline": cpu,
+            "replicas": "one independent problem per rank" if world > 1 else None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * flashot.h -- C ABI of the GB300 (sm_103a) streaming log-domain Sinkhorn library.
+ *
+ * Problem (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract; SAI
+ * replication review, "Summary"): entropic optimal transport between point clouds
+ * X (n x d) and Y (m x d) with weights a (n), b (m), squared Euclidean cost
+ * C_ij = |x_i - y_j|^2 and regularisation eps, solved by stabilized log-domain Sinkhorn.
+ * The dual potentials are updated as row-wise log-sum-exps of biased dot-product scores
+ * (the review's "Weaknesses" names the cost form c_ij = alpha_i + beta_j - Q_i^T K_j):
+ *
+ *   F (f-update): f_i = |x_i|^2 - eps * LSE_j[ (2<x_i,y_j> - |y_j|^2 + g_j)/eps + log b_j ]
+ *   G (g-update): g_j = |y_j|^2 - eps * LSE_i[ (2<x_i,y_j> - |x_i|^2 + f_i)/eps + log a_i ]
+ *   plan:         P_ij = a_i b_j exp((f_i + g_j - C_ij) / eps)     (never materialised)
+ *
+ * Conventions shared by every entry point below.
+ *  - Pointers named X, Y, a, b, f, g, V, out, grad, h, loss and ws are CUDA DEVICE
+ *    pointers owned by the caller, on the current CUDA device. Matrices are row-major
+ *    and contiguous (X: n*d floats, Y: m*d floats). Vectors are contiguous.
+ *  - a == NULL (b == NULL) means uniform weights 1/n (1/m). Weights are used as given:
+ *    they are not renormalised; a zero weight removes its point; negative or NaN weights
+ *    give undefined results (no device-side check, which would need a synchronisation).
+ *  - Work is enqueued asynchronously on `stream` (NULL = legacy default stream). The
+ *    library allocates no device memory: all scratch comes from the caller's workspace
+ *    `ws` of `ws_bytes` bytes, at least flashot_workspace_bytes(...) for the same
+ *    (n, m, d, k, flags), 256-byte aligned. A workspace must not be used by two calls
+ *    that may run concurrently.
+ *  - Every call returns FLASHOT_OK (0) or a negative status; no exception or abort
+ *    crosses the ABI. Argument errors are detected on the host before anything is
+ *    enqueued. FLASHOT_ERR_CUDA reports a failed launch; its cudaError_t is returned
+ *    by flashot_last_cuda_error() on the calling thread.
+ *  - Sizes: n, m >= 1, 1 <= d <= 4096, 1 <= k <= 4096, eps > 0 and finite.
+ *  - Arithmetic: scores and log-sum-exps are accumulated in fp32 (exp2 on the SFU);
+ *    the <x, y> contraction runs in the precision chosen by the FLASHOT_PREC_* flag.
+ *    Norms |x|^2, |y|^2 are taken from the fp32 inputs. The loss is reduced in fp64.
+ */
+#ifndef FLASHOT_H_
+#define FLASHOT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *flashot_stream_t;
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define FLASHOT_OK                        0
+#define FLASHOT_ERR_INVALID_ARG          -1  /* NULL pointer, size or eps out of range   */
+#define FLASHOT_ERR_ALIGNMENT            -2  /* ws not 256-byte aligned                   */
+#define FLASHOT_ERR_WORKSPACE_TOO_SMALL  -3  /* ws_bytes < flashot_workspace_bytes(...)   */
+#define FLASHOT_ERR_CUDA                 -4  /* a CUDA runtime call or launch failed      */
+#define FLASHOT_ERR_DEVICE_TIMEOUT       -5  /* a kernel gave up a bounded wait           */
+#define FLASHOT_ERR_UNSUPPORTED_DEVICE   -6  /* current device is not sm_103              */
+#define FLASHOT_ERR_NOT_IMPLEMENTED      -7  /* combination of flags not available        */
+
+/* ---- flags ------------------------------------------------------------------------- */
+/* Precision of the <x_i, y_j> contraction (low 4 bits). */
+#define FLASHOT_PREC_AUTO   0x0  /* FP32 for d < 32, TF32 tensor cores for d >= 32        */
+#define FLASHOT_PREC_FP32   0x1  /* fp32 FMA on CUDA cores (any d)                         */
+#define FLASHOT_PREC_TF32   0x2  /* tcgen05 kind::tf32, inputs rounded to tf32 (nearest)   */
+#define FLASHOT_PREC_BF16   0x3  /* tcgen05 kind::f16 with bf16 operands (nearest)         */
+#define FLASHOT_PREC_MASK   0xF
+/* solve: start from the g passed in (warm start / resume) instead of g = 0. */
+#define FLASHOT_WARM_START  0x10
+/* The workspace already holds the packed X, Y, norms and log-weights written by an
+ * earlier call with the same X, Y, a, b, n, m, d, flags and workspace; skip re-packing. */
+#define FLASHOT_REUSE_PACK  0x20
+
+/* ---- library information ------------------------------------------------------------ */
+int flashot_version(void);                       /* major*10000 + minor*100 + patch      */
+const char *flashot_status_string(int status);   /* static string, never NULL            */
+int flashot_last_cuda_error(void);               /* cudaError_t of the last ERR_CUDA      */
+
+/* Device-side status word kept in the workspace: synchronises `stream`, returns
+ * FLASHOT_ERR_DEVICE_TIMEOUT if a kernel that used this workspace gave up a bounded
+ * wait since the last call (and clears the word), else FLASHOT_OK, or ERR_CUDA. */
+int flashot_workspace_status(void *ws, flashot_stream_t stream);
+
+/* ---- diagnostics (no effect on results) ----------------------------------------------- */
+/* Number of kernels this library has launched in this process (all devices, all threads). */
+uint64_t flashot_launch_count(void);
+
+/* Kernel classes for the timer below. */
+#define FLASHOT_KERNEL_LSE    0  /* streaming log-sum-exp half-step pass (the hot kernel)  */
+#define FLASHOT_KERNEL_WSUM   1  /* streaming weighted-sum pass (apply, Hadamard, gradient) */
+#define FLASHOT_KERNEL_OTHER  2  /* packing, biases, LSE combine, loss reduction           */
+
+/* Per-launch timing on the launching stream: flashot_timer_start(cap) creates cap CUDA event
+ * pairs (host-side objects, no device memory) and from then on records one pair around each
+ * kernel launch, until cap pairs are used. flashot_timer_read(cls, &launches, &ms) waits for
+ * the recorded events and returns, for kernel class cls, the number of timed launches and
+ * their summed duration in milliseconds. flashot_timer_stop() destroys the events. Not for
+ * concurrent use from several threads. Returns a FLASHOT_* status. */
+int flashot_timer_start(int cap);
+int flashot_timer_read(int kernel_class, int64_t *launches, double *total_ms);
+int flashot_timer_stop(void);
+
+/* Bytes of workspace needed for calls with these sizes and flags. k is the column count
+ * of V for flashot_transport_apply (0 if that call is not used). Returns 0 on invalid
+ * sizes. The same workspace serves every entry point with equal (n, m, d, k, flags). */
+size_t flashot_workspace_bytes(int64_t n, int64_t m, int64_t d, int64_t k, int flags);
+
+/* ---- the hot path ------------------------------------------------------------------- */
+
+/*
+ * Full alternating solve (FlashSinkhorn abstract: stabilized log-domain Sinkhorn; the
+ * review "Summary": fused f^/g^ updates that write only the potentials back).
+ * For s = 0..n_stages-1 and it = 0..iters_per_stage-1: f = F(g), then g = G(f), at
+ * eps = eps_sched[s]. g starts at 0 unless FLASHOT_WARM_START is set (then the g passed
+ * in is read first). eps_sched is a HOST array of n_stages floats (annealing schedule).
+ * Writes f (n floats), g (m floats) and, if loss != NULL, *loss (ONE device double) =
+ * sum_i a_i f_i + sum_j b_j g_j after the final g-update.
+ */
+int flashot_sinkhorn_solve(const float *X, const float *Y, const float *a, const float *b,
+                           int64_t n, int64_t m, int64_t d, const float *eps_sched,
+                           int n_stages, int iters_per_stage, int flags, float *f, float *g,
+                           double *loss, void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/* One f-update (review "Summary": the f^ update): f = F(g). Reads g (m), writes f (n). */
+int flashot_sinkhorn_step_f(const float *X, const float *Y, const float *b, const float *g,
+                            int64_t n, int64_t m, int64_t d, float eps, int flags, float *f,
+                            void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/* One g-update (the g^ update): g = G(f). Reads f (n), writes g (m). */
+int flashot_sinkhorn_step_g(const float *X, const float *Y, const float *a, const float *f,
+                            int64_t n, int64_t m, int64_t d, float eps, int flags, float *g,
+                            void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/* Dual loss sum_i a_i f_i + sum_j b_j g_j, reduced in fp64 into ONE device double. */
+int flashot_dual_loss(const float *a, const float *b, const float *f, const float *g,
+                      int64_t n, int64_t m, double *loss, void *ws, size_t ws_bytes,
+                      flashot_stream_t stream);
+
+/*
+ * Matrix-free transport application (review "Summary" (ii): transport-vector and
+ * transport-matrix application) with P built on the fly from (f, g):
+ *   transpose == 0: out (n x k) = P V,    V is m x k row-major;
+ *   transpose != 0: out (m x k) = P^T V,  V is n x k row-major.
+ * out must not alias V.
+ */
+int flashot_transport_apply(const float *X, const float *Y, const float *a, const float *b,
+                            const float *f, const float *g, int64_t n, int64_t m, int64_t d,
+                            float eps, const float *V, int64_t k, int transpose, float *out,
+                            int flags, void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/* Hadamard-weighted transport with W = X Y^T (review "Summary" (ii)):
+ * h_i = sum_j P_ij <x_i, y_j>, h has n floats. */
+int flashot_transport_hadamard_xy(const float *X, const float *Y, const float *a,
+                                  const float *b, const float *f, const float *g, int64_t n,
+                                  int64_t m, int64_t d, float eps, float *h, int flags,
+                                  void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/*
+ * Gradient of the OT loss w.r.t. X as a barycentric projection (review "Summary" (i):
+ * the gradient as a residual "attention output"; "Weaknesses": exact for the
+ * marginal-perturbed problem at early-stopped potentials). With f~ = F(g) computed
+ * internally (softmax over j of the F-step scores):
+ *   grad_i = 2 a_i (x_i - yhat_i),  yhat_i = sum_j softmax_j(s_ij) y_j.
+ * grad has n x d floats (row-major).
+ */
+int flashot_ot_grad_x(const float *X, const float *Y, const float *a, const float *b,
+                      const float *g, int64_t n, int64_t m, int64_t d, float eps, float *grad,
+                      int flags, void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLASHOT_H_ */

@@ -1,0 +1,55 @@
+// common.cuh -- shared device helpers for the streaming log-domain Sinkhorn kernels.
+//
+// All kernels work in base 2: for an F-type pass (rows = X, columns = Y) the score is
+//   s2_ij = kappa * <x_i, y_j> + c_j,   kappa = 2 log2(e) / eps,
+//   c_j   = (g_j - |y_j|^2) log2(e) / eps + log2 b_j,
+// so that f_i = |x_i|^2 - eps ln2 * LSE2_j(s2_ij) (FlashSinkhorn: IO-Aware Entropic
+// Optimal Transport on GPU, SAI replication review, "Summary": the Sinkhorn update as a
+// row-wise log-sum-exp of biased dot-product scores). A G-type pass swaps the roles of
+// X and Y. Padded columns carry c_j = -inf and contribute exactly zero.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace flashot {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+// Finite floor for running maxima: exp2(x - kNegBig) never produces NaN from -inf - -inf.
+constexpr float kNegBig = -1.0e30f;
+
+// SFU base-2 exponential (MUFU.EX2), flush-to-zero; exp2(-inf) = +0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// What a weighted-sum pass produces: transport application P V, the barycentric gradient,
+// or the Hadamard-weighted transport (P .* X Y^T) 1.
+enum WsumMode : int { kWsumApply = 0, kWsumGrad = 1, kWsumHadamard = 2 };
+
+// Status bits written into the workspace status word by kernels that give up a wait.
+constexpr unsigned kErrTimeout = 1u;
+
+// Stream-K split of T tiles over G persistent CTAs: CTA c owns tiles [c*T/G, (c+1)*T/G).
+__host__ __device__ __forceinline__ int64_t sk_begin(int64_t c, int64_t T, int64_t G) {
+  return c * T / G;
+}
+// The CTA whose range contains tile v (largest c with sk_begin(c) <= v).
+__host__ __device__ __forceinline__ int64_t sk_owner(int64_t v, int64_t T, int64_t G) {
+  return ((v + 1) * G + T - 1) / T - 1;
+}
+
+// How the partials of one LSE pass are laid out: either n_splits fixed splits per row, or
+// (n_splits == 0) stream-K over T = row_tiles * NT tiles of 128 x 128 with G CTAs, where
+// the row tile rt has partial slots 0 .. owner((rt+1)NT-1) - owner(rt NT).
+struct SplitInfo {
+  int n_splits;
+  int64_t sk_T, sk_G, sk_NT;
+};
+
+}  // namespace flashot

@@ -1,0 +1,682 @@
+// flashot.cu -- host side of the C ABI declared in include/flashot.h.
+//
+// Argument validation, workspace layout, pass launchers and the alternating solve
+// driver for streaming log-domain Sinkhorn (FlashSinkhorn: IO-Aware Entropic Optimal
+// Transport on GPU, abstract and SAI replication review, "Summary"). Every step of the
+// computation runs in the kernels of prep_kernels.cuh, fma_kernels.cuh and
+// tc_kernels.cuh; this file only validates, carves the caller's workspace and enqueues.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "flashot.h"
+#include "common.cuh"
+#include "fma_kernels.cuh"
+#include "prep_kernels.cuh"
+#include "tc_api.h"
+#include "trace.h"
+#include <vector>
+
+namespace flashot {
+
+// ---- launch accounting (diagnostics) ----------------------------------------------------
+namespace {
+std::atomic<uint64_t> g_launches{0};
+struct EventTimer {
+  bool on = false;
+  int cap = 0, used = 0;
+  std::vector<cudaEvent_t> ev;  // 2 per launch
+  std::vector<int> cls;
+};
+EventTimer g_timer;
+}  // namespace
+
+void trace_before(int, cudaStream_t st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_timer.on && g_timer.used < g_timer.cap) cudaEventRecord(g_timer.ev[2 * g_timer.used], st);
+}
+
+void trace_after(int kernel_class, cudaStream_t st) {
+  if (g_timer.on && g_timer.used < g_timer.cap) {
+    cudaEventRecord(g_timer.ev[2 * g_timer.used + 1], st);
+    g_timer.cls[g_timer.used] = kernel_class;
+    ++g_timer.used;
+  }
+}
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int64_t kMaxRows = int64_t(1) << 28;
+constexpr int64_t kMaxD = 4096;
+constexpr int64_t kMaxK = 4096;
+constexpr int kMaxSplits = 64;
+constexpr int kRowPad = 128;
+
+inline int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
+inline int64_t ceil_div(int64_t x, int64_t q) { return (x + q - 1) / q; }
+
+// ---- device checks -------------------------------------------------------------------
+struct DeviceInfo {
+  int ok = 0;  // 0 unknown, 1 sm_103, 2 other
+  int sms = 0;
+};
+DeviceInfo g_dev[64];
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return FLASHOT_ERR_CUDA;
+}
+
+int current_device(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FLASHOT_ERR_UNSUPPORTED_DEVICE;
+  DeviceInfo& di = g_dev[dev];
+  if (di.ok == 0) {
+    int maj = 0, mnr = 0, sms_ = 0;
+    if ((e = cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&mnr, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&sms_, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    di.sms = sms_;
+    di.ok = (maj == 10 && mnr == 3) ? 1 : 2;
+  }
+  if (di.ok != 1) return FLASHOT_ERR_UNSUPPORTED_DEVICE;
+  *sms = di.sms;
+  return FLASHOT_OK;
+}
+
+// A device pointer of the current context (device or managed memory).
+bool is_device_ptr(const void* p) {
+  if (p == nullptr) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+bool opt_device_ptr(const void* p) { return p == nullptr || is_device_ptr(p); }
+
+// ---- problem geometry and workspace layout ------------------------------------------
+struct Geometry {
+  int64_t n, m, d, k;
+  int prec;          // FLASHOT_PREC_{FP32,TF32,BF16}
+  bool small;        // FP32 path with d_pad <= 32 (registers hold a whole point)
+  int64_t n_pad, m_pad;
+  int64_t dpf;       // d_pad of the fp32 packing (FP32 path)
+  int64_t dpt;       // d_pad of the tensor-core packing (TF32/BF16 path)
+  int es;            // element size of the tensor-core packing
+};
+
+int resolve_prec(int flags, int64_t d) {
+  const int p = flags & FLASHOT_PREC_MASK;
+  if (p == FLASHOT_PREC_AUTO) return d < 32 ? FLASHOT_PREC_FP32 : FLASHOT_PREC_TF32;
+  return p;
+}
+
+bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geometry* g) {
+  if (n < 1 || m < 1 || d < 1 || n > kMaxRows || m > kMaxRows || d > kMaxD || k < 0 ||
+      k > kMaxK)
+    return false;
+  const int p = resolve_prec(flags, d);
+  if (p != FLASHOT_PREC_FP32 && p != FLASHOT_PREC_TF32 && p != FLASHOT_PREC_BF16) return false;
+  g->n = n;
+  g->m = m;
+  g->d = d;
+  g->k = k;
+  g->prec = p;
+  g->n_pad = round_up(n, kRowPad);
+  g->m_pad = round_up(m, kRowPad);
+  g->small = d <= 32;
+  g->dpf = g->small ? round_up(d, 4) : round_up(d, 32);
+  g->es = (p == FLASHOT_PREC_BF16) ? 2 : 4;
+  g->dpt = round_up(d, 128 / g->es);  // one 128-byte swizzle row per k-chunk
+  return true;
+}
+
+struct Layout {
+  size_t status, xp, yp, xq, yq, vtq, alpha, beta, wa, wb, la2, lb2, biasF, biasG, ftilde,
+      lse2, partial, loss, total;
+};
+
+Layout make_layout(const Geometry& g) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = (off + bytes + 1023) / 1024 * 1024;
+    return o;
+  };
+  const size_t np = (size_t)g.n_pad, mp = (size_t)g.m_pad;
+  L.status = take(256);
+  if (g.prec == FLASHOT_PREC_FP32) {
+    L.xp = take(np * g.dpf * 4);
+    L.yp = take(mp * g.dpf * 4);
+  } else {
+    L.xq = take(np * g.dpt * g.es);
+    L.yq = take(mp * g.dpt * g.es);
+  }
+  L.alpha = take(np * 4);
+  L.beta = take(mp * 4);
+  L.wa = take(np * 4);
+  L.wb = take(mp * 4);
+  L.la2 = take(np * 4);
+  L.lb2 = take(mp * 4);
+  L.biasF = take(mp * 4);
+  L.biasG = take(np * 4);
+  L.ftilde = take(np * 4);
+  L.lse2 = take(std::max(np, mp) * 4);
+  L.partial = take((size_t)kMaxSplits * std::max(np, mp) * sizeof(float2));
+  L.loss = take(64);
+  // Last, so that every offset above is independent of k: the transposed right operand
+  // of the tensor-core weighted sums (V^T for apply, Y^T for the gradient), padded to
+  // multiples of 256 output columns.
+  if (g.prec != FLASHOT_PREC_FP32)
+    L.vtq = take((size_t)std::max(round_up(g.k, 256), round_up(g.d, 256)) * std::max(np, mp) *
+                 g.es);
+  L.total = off + 256;
+  return L;
+}
+
+// Everything a pass needs, resolved from the caller's workspace.
+struct Ctx {
+  Geometry g;
+  Layout L;
+  char* ws;
+  int sms;
+  cudaStream_t st;
+  template <typename T>
+  T* at(size_t off) const { return reinterpret_cast<T*>(ws + off); }
+};
+
+int check_ws(const Geometry& g, void* ws, size_t ws_bytes, Layout* L) {
+  if (!is_device_ptr(ws)) return FLASHOT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FLASHOT_ERR_ALIGNMENT;
+  *L = make_layout(g);
+  if (ws_bytes < L->total) return FLASHOT_ERR_WORKSPACE_TOO_SMALL;
+  return FLASHOT_OK;
+}
+
+bool eps_ok(float eps) { return std::isfinite(eps) && eps > 0.0f; }
+
+int launch_check() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FLASHOT_OK : cuda_fail(e);
+}
+
+inline unsigned grid1(int64_t total, int threads) {
+  int64_t b = ceil_div(total, threads);
+  return (unsigned)std::min<int64_t>(std::max<int64_t>(b, 1), 1 << 20);
+}
+
+// ---- packing ---------------------------------------------------------------------------
+int pack_inputs(const Ctx& c, const float* X, const float* Y, const float* a, const float* b) {
+  const Geometry& g = c.g;
+  const int T = 256;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    weights_kernel<<<grid1(g.n_pad, T), T, 0, c.st>>>(a, g.n, g.n_pad, c.at<float>(c.L.wa),
+                                                      c.at<float>(c.L.la2), c.at<unsigned>(c.L.status));
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    weights_kernel<<<grid1(g.m_pad, T), T, 0, c.st>>>(b, g.m, g.m_pad, c.at<float>(c.L.wb),
+                                                      c.at<float>(c.L.lb2), nullptr);
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    row_norms_kernel<<<grid1(g.n_pad * 32, T), T, 0, c.st>>>(X, g.n, g.d, g.n_pad,
+                                                             c.at<float>(c.L.alpha));
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    row_norms_kernel<<<grid1(g.m_pad * 32, T), T, 0, c.st>>>(Y, g.m, g.d, g.m_pad,
+                                                             c.at<float>(c.L.beta));
+  }
+  const unsigned pg = (unsigned)std::min<int64_t>(ceil_div((g.n_pad + g.m_pad) * 64, T), c.sms * 8);
+  if (g.prec == FLASHOT_PREC_FP32) {
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      pack_rows_kernel<PackKind::F32><<<pg, T, 0, c.st>>>(X, c.at<void>(c.L.xp), g.n, g.d, g.n_pad, g.dpf);
+    }
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      pack_rows_kernel<PackKind::F32><<<pg, T, 0, c.st>>>(Y, c.at<void>(c.L.yp), g.m, g.d, g.m_pad, g.dpf);
+    }
+  } else {
+    int rc = tc_pack_inputs(c.g.prec == FLASHOT_PREC_BF16, X, Y, g.n, g.m, g.d, g.n_pad, g.m_pad,
+                            g.dpt, c.at<void>(c.L.xq), c.at<void>(c.L.yq), c.sms, c.st);
+    if (rc != FLASHOT_OK) return rc;
+  }
+  return launch_check();
+}
+
+// bias = (pot - norms) log2e / eps + lw2 over one side (pot == NULL: pot = 0).
+int launch_bias(const Ctx& c, const float* pot, bool x_side, float eps) {
+  const Geometry& g = c.g;
+  const int64_t rows = x_side ? g.n : g.m, rows_pad = x_side ? g.n_pad : g.m_pad;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    bias_kernel<<<grid1(rows_pad, 256), 256, 0, c.st>>>(
+        pot, c.at<float>(x_side ? c.L.alpha : c.L.beta), c.at<float>(x_side ? c.L.la2 : c.L.lb2),
+        rows, rows_pad, kLog2e / eps, c.at<float>(x_side ? c.L.biasG : c.L.biasF));
+  }
+  return launch_check();
+}
+
+// ---- one LSE half-step -----------------------------------------------------------------
+// F-type (x_rows = true): rows X, columns Y, column bias biasF; writes out_pot (= f),
+// the next pass's bias biasG (at eps_next), and optionally the row LSE (base 2).
+// G-type: the same with X and Y exchanged.
+int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* out_pot,
+                 bool write_next_bias, float* out_lse2) {
+  const Geometry& g = c.g;
+  const int64_t n_rows = x_rows ? g.n : g.m;
+  const int64_t rows_pad = x_rows ? g.n_pad : g.m_pad;
+  const int64_t cols_pad = x_rows ? g.m_pad : g.n_pad;
+  const float* colBias = c.at<float>(x_rows ? c.L.biasF : c.L.biasG);
+  float2* partial = c.at<float2>(c.L.partial);
+  const float kappa = 2.0f * kLog2e / eps;
+  SplitInfo split{1, 0, 0, 0};
+  int n_splits = 1;
+  if (g.prec == FLASHOT_PREC_FP32) {
+    const float* rowP = c.at<float>(x_rows ? c.L.xp : c.L.yp);
+    const float* colP = c.at<float>(x_rows ? c.L.yp : c.L.xp);
+    const int R = (g.dpf <= 16) ? 4 : 2;
+    const int64_t rows_per_block = g.small ? (int64_t)kFmaThreads * R : kFmaThreads;
+    const int64_t row_blocks = ceil_div(n_rows, rows_per_block);
+    const int n_tiles = (int)(cols_pad / (g.small ? kFmaBN : 32));
+    const int64_t target = (int64_t)c.sms * 8;
+    n_splits = (int)std::min<int64_t>({ceil_div(target, row_blocks), (int64_t)n_tiles,
+                                        (int64_t)kMaxSplits});
+    n_splits = std::max(n_splits, 1);
+    const int tps = (int)ceil_div(n_tiles, n_splits);
+    n_splits = (int)ceil_div(n_tiles, tps);
+    split.n_splits = n_splits;
+    dim3 grid((unsigned)row_blocks, (unsigned)n_splits);
+    if (g.small) {
+      TraceScope ts_(FLASHOT_KERNEL_LSE, c.st);
+#define FLASHOT_LSE_SMALL(DPV, RV)                                                        \
+  lse_fma_small_kernel<DPV, RV><<<grid, kFmaThreads, 0, c.st>>>(rowP, colP, colBias, n_rows, \
+                                                                n_tiles, tps, kappa, partial, \
+                                                                rows_pad)
+      switch (g.dpf) {
+        case 4: FLASHOT_LSE_SMALL(4, 4); break;
+        case 8: FLASHOT_LSE_SMALL(8, 4); break;
+        case 12: FLASHOT_LSE_SMALL(12, 4); break;
+        case 16: FLASHOT_LSE_SMALL(16, 4); break;
+        case 20: FLASHOT_LSE_SMALL(20, 2); break;
+        case 24: FLASHOT_LSE_SMALL(24, 2); break;
+        case 28: FLASHOT_LSE_SMALL(28, 2); break;
+        case 32: FLASHOT_LSE_SMALL(32, 2); break;
+        default: return FLASHOT_ERR_INVALID_ARG;
+      }
+#undef FLASHOT_LSE_SMALL
+    } else {
+      {
+        TraceScope ts_(FLASHOT_KERNEL_LSE, c.st);
+        lse_fma_generic_kernel<<<grid, kFmaThreads, 0, c.st>>>(rowP, colP, colBias, n_rows, g.dpf,
+                                                               n_tiles, tps, kappa, partial,
+                                                               rows_pad);
+      }
+    }
+  } else {
+    int rc = tc_lse_pass(g.prec == FLASHOT_PREC_BF16, c.at<void>(x_rows ? c.L.xq : c.L.yq),
+                         c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, n_rows, rows_pad,
+                         cols_pad, g.dpt, kappa, partial, kMaxSplits, c.sms,
+                         c.at<unsigned>(c.L.status), &split, c.st);
+    if (rc != FLASHOT_OK) return rc;
+  }
+  int rc = launch_check();
+  if (rc != FLASHOT_OK) return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    lse_combine_kernel<<<grid1(rows_pad, 256), 256, 0, c.st>>>(
+        partial, split, rows_pad, n_rows, rows_pad, c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
+        c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
+        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr, out_lse2);
+  }
+  return launch_check();
+}
+
+// ---- weighted-sum passes (apply, grad, Hadamard) -----------------------------------------
+// rows on the X side unless `transpose`; rowBias / colBias as prepared by the caller.
+int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float* V, int64_t ldv,
+                  int64_t k, const float* X, const float* Y, float* out, int64_t ldo) {
+  const Geometry& g = c.g;
+  const bool x_rows = !transpose;
+  const int64_t n_rows = x_rows ? g.n : g.m;
+  const int64_t n_cols = x_rows ? g.m : g.n;
+  const int64_t cols_pad = x_rows ? g.m_pad : g.n_pad;
+  const float* colBias = c.at<float>(x_rows ? c.L.biasF : c.L.biasG);
+  const float* rowBias = c.at<float>(x_rows ? c.L.biasG : c.L.biasF);
+  const float* rowW = c.at<float>(x_rows ? c.L.wa : c.L.wb);
+  const float kappa = 2.0f * kLog2e / eps;
+  if (g.prec != FLASHOT_PREC_FP32) {
+    if (mode == kWsumGrad) {  // right operand of the second contraction: the column points
+      V = x_rows ? Y : X;
+      ldv = g.d;
+      k = g.d;
+    }
+    return tc_wsum_pass(g.prec == FLASHOT_PREC_BF16, mode, c.at<void>(x_rows ? c.L.xq : c.L.yq),
+                        c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows, n_cols,
+                        x_rows ? g.n_pad : g.m_pad, cols_pad, g.d, g.dpt, kappa, V, ldv, k,
+                        c.at<void>(c.L.vtq), rowW, X, out, ldo, c.sms,
+                        c.at<unsigned>(c.L.status), c.st);
+  }
+  const float* rowP = c.at<float>(x_rows ? c.L.xp : c.L.yp);
+  const float* colP = c.at<float>(x_rows ? c.L.yp : c.L.xp);
+  if (mode == kWsumGrad) {
+    V = colP;
+    ldv = g.dpf;
+    k = g.d;
+  }
+  const int64_t kk = (mode == kWsumHadamard) ? 1 : k;
+  dim3 grid((unsigned)ceil_div(n_rows, kFmaThreads), (unsigned)ceil_div(kk, 32));
+  const int n_tiles = (int)(cols_pad / 32);
+  TraceScope ts_(FLASHOT_KERNEL_WSUM, c.st);
+  if (g.small) {
+#define FLASHOT_WSUM_SMALL(DPV, MODEV)                                                     \
+  wsum_fma_small_kernel<DPV, MODEV><<<grid, kFmaThreads, 0, c.st>>>(                       \
+      rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
+      out, ldo)
+#define FLASHOT_WSUM_MODES(DPV)                                    \
+  case DPV:                                                        \
+    if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply);   \
+    else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad); \
+    else FLASHOT_WSUM_SMALL(DPV, kWsumHadamard);                   \
+    break;
+    switch (g.dpf) {
+      FLASHOT_WSUM_MODES(4)
+      FLASHOT_WSUM_MODES(8)
+      FLASHOT_WSUM_MODES(12)
+      FLASHOT_WSUM_MODES(16)
+      FLASHOT_WSUM_MODES(20)
+      FLASHOT_WSUM_MODES(24)
+      FLASHOT_WSUM_MODES(28)
+      FLASHOT_WSUM_MODES(32)
+      default: return FLASHOT_ERR_INVALID_ARG;
+    }
+#undef FLASHOT_WSUM_MODES
+#undef FLASHOT_WSUM_SMALL
+  } else {
+#define FLASHOT_WSUM_GENERIC(MODEV)                                                           \
+  wsum_fma_generic_kernel<MODEV><<<grid, kFmaThreads, 0, c.st>>>(                             \
+      rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, g.dpf, kappa, V, ldv, k, rowW, X, \
+      g.d, out, ldo)
+    if (mode == kWsumApply) FLASHOT_WSUM_GENERIC(kWsumApply);
+    else if (mode == kWsumGrad) FLASHOT_WSUM_GENERIC(kWsumGrad);
+    else FLASHOT_WSUM_GENERIC(kWsumHadamard);
+#undef FLASHOT_WSUM_GENERIC
+  }
+  return launch_check();
+}
+
+// Common prologue of every hot-path entry point.
+int begin(int64_t n, int64_t m, int64_t d, int64_t k, int flags, void* ws, size_t ws_bytes,
+          flashot_stream_t stream, Ctx* c) {
+  if (!make_geometry(n, m, d, k, flags, &c->g)) return FLASHOT_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = current_device(&sms);
+  if (rc != FLASHOT_OK) return rc;
+  rc = check_ws(c->g, ws, ws_bytes, &c->L);
+  if (rc != FLASHOT_OK) return rc;
+  c->ws = static_cast<char*>(ws);
+  c->sms = sms;
+  c->st = reinterpret_cast<cudaStream_t>(stream);
+  return FLASHOT_OK;
+}
+
+}  // namespace
+}  // namespace flashot
+
+using namespace flashot;
+
+extern "C" {
+
+int flashot_version(void) { return kVersion; }
+
+const char* flashot_status_string(int s) {
+  switch (s) {
+    case FLASHOT_OK: return "ok";
+    case FLASHOT_ERR_INVALID_ARG: return "invalid argument";
+    case FLASHOT_ERR_ALIGNMENT: return "workspace pointer is not 256-byte aligned";
+    case FLASHOT_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FLASHOT_ERR_CUDA: return "CUDA runtime error (see flashot_last_cuda_error)";
+    case FLASHOT_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case FLASHOT_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+    case FLASHOT_ERR_NOT_IMPLEMENTED: return "not implemented for these flags";
+    default: return "unknown status";
+  }
+}
+
+int flashot_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t flashot_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int flashot_timer_stop(void) {
+  for (cudaEvent_t e : g_timer.ev) cudaEventDestroy(e);
+  g_timer = EventTimer{};
+  return FLASHOT_OK;
+}
+
+int flashot_timer_start(int cap) {
+  if (cap < 1 || cap > (1 << 20)) return FLASHOT_ERR_INVALID_ARG;
+  flashot_timer_stop();
+  g_timer.ev.resize(2 * (size_t)cap, nullptr);
+  g_timer.cls.assign((size_t)cap, -1);
+  for (auto& e : g_timer.ev) {
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) {
+      flashot_timer_stop();
+      return cuda_fail(err);
+    }
+  }
+  g_timer.cap = cap;
+  g_timer.on = true;
+  return FLASHOT_OK;
+}
+
+int flashot_timer_read(int kernel_class, int64_t* launches, double* total_ms) {
+  if (!launches || !total_ms) return FLASHOT_ERR_INVALID_ARG;
+  int64_t cnt = 0;
+  double ms = 0.0;
+  for (int i = 0; i < g_timer.used; ++i) {
+    if (g_timer.cls[i] != kernel_class) continue;
+    cudaError_t err = cudaEventSynchronize(g_timer.ev[2 * i + 1]);
+    float t = 0.0f;
+    if (err == cudaSuccess) err = cudaEventElapsedTime(&t, g_timer.ev[2 * i], g_timer.ev[2 * i + 1]);
+    if (err != cudaSuccess) return cuda_fail(err);
+    ++cnt;
+    ms += t;
+  }
+  *launches = cnt;
+  *total_ms = ms;
+  return FLASHOT_OK;
+}
+
+size_t flashot_workspace_bytes(int64_t n, int64_t m, int64_t d, int64_t k, int flags) {
+  Geometry g;
+  if (!make_geometry(n, m, d, k, flags, &g)) return 0;
+  return make_layout(g).total;
+}
+
+int flashot_workspace_status(void* ws, flashot_stream_t stream) {
+  if (!is_device_ptr(ws)) return FLASHOT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FLASHOT_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    e = cudaMemsetAsync(ws, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FLASHOT_ERR_DEVICE_TIMEOUT;
+  }
+  return FLASHOT_OK;
+}
+
+int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const float* b,
+                           int64_t n, int64_t m, int64_t d, const float* eps_sched, int n_stages,
+                           int iters_per_stage, int flags, float* f, float* g, double* loss,
+                           void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_sched || n_stages < 1 || iters_per_stage < 1) return FLASHOT_ERR_INVALID_ARG;
+  for (int s = 0; s < n_stages; ++s)
+    if (!eps_ok(eps_sched[s])) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !opt_device_ptr(loss))
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  // Initial F-step bias from g (warm start) or g = 0.
+  if ((rc = launch_bias(c, (flags & FLASHOT_WARM_START) ? g : nullptr, false, eps_sched[0])) !=
+      FLASHOT_OK)
+    return rc;
+  for (int s = 0; s < n_stages; ++s) {
+    const float eps = eps_sched[s];
+    for (int it = 0; it < iters_per_stage; ++it) {
+      const bool last_of_stage = (it == iters_per_stage - 1);
+      const float eps_next = (last_of_stage && s + 1 < n_stages) ? eps_sched[s + 1] : eps;
+      if ((rc = run_lse_pass(c, true, eps, eps, f, true, nullptr)) != FLASHOT_OK) return rc;
+      if ((rc = run_lse_pass(c, false, eps, eps_next, g, true, nullptr)) != FLASHOT_OK) return rc;
+    }
+  }
+  if (loss) {
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      dual_loss_kernel<<<1, 1024, 0, c.st>>>(c.at<float>(c.L.wa), f, n, c.at<float>(c.L.wb), g, m,
+                                             loss);
+    }
+    if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  }
+  return FLASHOT_OK;
+}
+
+int flashot_sinkhorn_step_f(const float* X, const float* Y, const float* b, const float* g,
+                            int64_t n, int64_t m, int64_t d, float eps, int flags, float* f,
+                            void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_ok(eps)) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(b) || !is_device_ptr(g) ||
+      !is_device_ptr(f))
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, nullptr, b)) != FLASHOT_OK)
+    return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  return run_lse_pass(c, true, eps, eps, f, false, nullptr);
+}
+
+int flashot_sinkhorn_step_g(const float* X, const float* Y, const float* a, const float* f,
+                            int64_t n, int64_t m, int64_t d, float eps, int flags, float* g,
+                            void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_ok(eps)) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !is_device_ptr(f) ||
+      !is_device_ptr(g))
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, nullptr)) != FLASHOT_OK)
+    return rc;
+  if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+  return run_lse_pass(c, false, eps, eps, g, false, nullptr);
+}
+
+int flashot_dual_loss(const float* a, const float* b, const float* f, const float* g, int64_t n,
+                      int64_t m, double* loss, void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  Ctx c;
+  int rc = begin(n, m, 1, 0, FLASHOT_PREC_FP32, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!opt_device_ptr(a) || !opt_device_ptr(b) || !is_device_ptr(f) || !is_device_ptr(g) ||
+      !is_device_ptr(loss))
+    return FLASHOT_ERR_INVALID_ARG;
+  const int T = 256;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    weights_kernel<<<grid1(c.g.n_pad, T), T, 0, c.st>>>(a, n, c.g.n_pad, c.at<float>(c.L.wa),
+                                                        c.at<float>(c.L.la2), nullptr);
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    weights_kernel<<<grid1(c.g.m_pad, T), T, 0, c.st>>>(b, m, c.g.m_pad, c.at<float>(c.L.wb),
+                                                        c.at<float>(c.L.lb2), nullptr);
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    dual_loss_kernel<<<1, 1024, 0, c.st>>>(c.at<float>(c.L.wa), f, n, c.at<float>(c.L.wb), g, m,
+                                           loss);
+  }
+  return launch_check();
+}
+
+int flashot_transport_apply(const float* X, const float* Y, const float* a, const float* b,
+                            const float* f, const float* g, int64_t n, int64_t m, int64_t d,
+                            float eps, const float* V, int64_t k, int transpose, float* out,
+                            int flags, void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_ok(eps) || k < 1) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, k, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(V) || !is_device_ptr(out) ||
+      (const void*)out == (const void*)V)
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+  return run_wsum_pass(c, kWsumApply, transpose != 0, eps, V, k, k, X, Y, out, k);
+}
+
+int flashot_transport_hadamard_xy(const float* X, const float* Y, const float* a, const float* b,
+                                  const float* f, const float* g, int64_t n, int64_t m, int64_t d,
+                                  float eps, float* h, int flags, void* ws, size_t ws_bytes,
+                                  flashot_stream_t stream) {
+  if (!eps_ok(eps)) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(h))
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+  return run_wsum_pass(c, kWsumHadamard, false, eps, nullptr, 0, 1, X, Y, h, 1);
+}
+
+int flashot_ot_grad_x(const float* X, const float* Y, const float* a, const float* b,
+                      const float* g, int64_t n, int64_t m, int64_t d, float eps, float* grad,
+                      int flags, void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_ok(eps)) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(g) || !is_device_ptr(grad))
+    return FLASHOT_ERR_INVALID_ARG;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  // f~ = F(g); its combine writes biasG = log2 a_i - L_i, so the weighted pass below uses
+  // w_ij = a_i softmax_j(s_ij); the gradient kernel renormalises by sum_j w_ij.
+  if ((rc = run_lse_pass(c, true, eps, eps, c.at<float>(c.L.ftilde), true, nullptr)) != FLASHOT_OK)
+    return rc;
+  return run_wsum_pass(c, kWsumGrad, false, eps, nullptr, 0, d, X, Y, grad, d);
+}
+
+}  // extern "C"

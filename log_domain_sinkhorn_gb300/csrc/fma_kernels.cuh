@@ -1,0 +1,332 @@
+// fma_kernels.cuh -- CUDA-core (fp32 FMA) streaming passes.
+//
+// Used for small d (d < 32, where a tensor-core tile would be mostly padding and the
+// epilogue dominates anyway) and for the FP32 precision option at any d. Like the
+// tensor-core kernels they never form the n x m score matrix: each CTA keeps its rows'
+// online (max, sum) state in registers and streams column tiles through shared memory
+// (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract: tiles streamed
+// through on-chip SRAM, potentials updated in a single pass).
+//
+// Two families:
+//  * lse_*   : one half-step's row-wise base-2 log-sum-exp, split over column ranges;
+//              each split writes a (max, sum) partial, lse_combine_kernel merges them.
+//  * wsum_*  : weighted sums with weights w_ij = exp2(kappa <p_i, q_j> + c_j + r_i):
+//              transport application (P V), the barycentric gradient (softmax-weighted
+//              Y) and the Hadamard-weighted transport (sum_j P_ij <x_i, y_j>).
+#pragma once
+
+#include "common.cuh"
+
+namespace flashot {
+
+constexpr int kFmaThreads = 128;
+constexpr int kFmaBN = 128;  // columns per shared-memory tile, small-d LSE kernel
+constexpr int kFmaJ = 8;     // columns per online-LSE chunk
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b, float acc) {
+  acc = fmaf(a.x, b.x, acc);
+  acc = fmaf(a.y, b.y, acc);
+  acc = fmaf(a.z, b.z, acc);
+  return fmaf(a.w, b.w, acc);
+}
+
+// Online base-2 LSE update of (M, S) with a chunk of J scores.
+template <int J>
+__device__ __forceinline__ void lse_chunk(const float (&s)[J], float& M, float& S) {
+  float mx = s[0];
+#pragma unroll
+  for (int j = 1; j < J; ++j) mx = fmaxf(mx, s[j]);
+  if (mx > M) {
+    S *= ex2(M - mx);
+    M = mx;
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < J; ++j) acc += ex2(s[j] - M);
+  S += acc;
+}
+
+// ---------------------------------------------------------------------------------------
+// LSE pass, d_pad = DP <= 32 (multiple of 4): each thread owns R rows, x in registers.
+// rowP: n_rows x DP, colP: (n_col_tiles*kFmaBN) x DP, packed fp32 (zero padded).
+// Grid: (row blocks, splits). Split s covers column tiles [s*tps, (s+1)*tps).
+// ---------------------------------------------------------------------------------------
+template <int DP, int R>
+__global__ void __launch_bounds__(kFmaThreads)
+lse_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
+                     const float* __restrict__ colBias, int64_t n_rows, int n_col_tiles,
+                     int tiles_per_split, float kappa, float2* __restrict__ partial,
+                     int64_t ld) {
+  static_assert(DP % 4 == 0 && DP <= 32, "DP must be a multiple of 4, at most 32");
+  static_assert(kFmaBN == kFmaThreads, "one bias entry per thread");
+  constexpr int Q = DP / 4;
+  __shared__ float4 ys[kFmaBN * Q];
+  __shared__ float cs[kFmaBN];
+  const int tid = threadIdx.x;
+  const int64_t row0 = (int64_t)blockIdx.x * (kFmaThreads * R) + tid;
+
+  float4 x[R][Q];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t row = row0 + (int64_t)r * kFmaThreads;
+    const float4* src = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * DP);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) x[r][q] = src[q];
+  }
+  float M[R], S[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    M[r] = kNegBig;
+    S[r] = 0.0f;
+  }
+
+  const int t0 = blockIdx.y * tiles_per_split;
+  const int t1 = min(t0 + tiles_per_split, n_col_tiles);
+  for (int t = t0; t < t1; ++t) {
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(colP + (int64_t)t * kFmaBN * DP);
+    for (int e = tid; e < kFmaBN * Q; e += kFmaThreads) ys[e] = src[e];
+    cs[tid] = colBias[(int64_t)t * kFmaBN + tid];
+    __syncthreads();
+#pragma unroll 1
+    for (int jc = 0; jc < kFmaBN; jc += kFmaJ) {
+      float s[R][kFmaJ];
+#pragma unroll
+      for (int jj = 0; jj < kFmaJ; ++jj) {
+        float acc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+          const float4 y = ys[(jc + jj) * Q + q];
+#pragma unroll
+          for (int r = 0; r < R; ++r) acc[r] = dot4(x[r][q], y, acc[r]);
+        }
+        const float c = cs[jc + jj];
+#pragma unroll
+        for (int r = 0; r < R; ++r) s[r][jj] = fmaf(kappa, acc[r], c);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) lse_chunk<kFmaJ>(s[r], M[r], S[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t row = row0 + (int64_t)r * kFmaThreads;
+    if (row < n_rows) partial[blockIdx.y * ld + row] = make_float2(M[r], S[r]);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// LSE pass, any d_pad (multiple of 32): one row per thread; dots for 32 columns are
+// accumulated over 32-wide k-chunks staged in shared memory.
+// colP has n_col_tiles*32 rows.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFmaThreads)
+lse_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
+                       const float* __restrict__ colBias, int64_t n_rows, int64_t d_pad,
+                       int n_col_tiles, int tiles_per_split, float kappa,
+                       float2* __restrict__ partial, int64_t ld) {
+  __shared__ float4 ys[32 * 8];
+  __shared__ float cs[32];
+  const int tid = threadIdx.x;
+  const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
+  const float4* xr = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * d_pad);
+  const int nkc = (int)(d_pad / 32);
+  float M = kNegBig, S = 0.0f;
+  const int t0 = blockIdx.y * tiles_per_split;
+  const int t1 = min(t0 + tiles_per_split, n_col_tiles);
+  for (int t = t0; t < t1; ++t) {
+    float acc[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+    for (int kc = 0; kc < nkc; ++kc) {
+      __syncthreads();
+      for (int e = tid; e < 256; e += kFmaThreads) {
+        const int c = e >> 3, q = e & 7;
+        ys[e] = reinterpret_cast<const float4*>(colP + ((int64_t)t * 32 + c) * d_pad +
+                                                (int64_t)kc * 32)[q];
+      }
+      if (kc == 0 && tid < 32) cs[tid] = colBias[(int64_t)t * 32 + tid];
+      __syncthreads();
+      float4 xv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xv[q] = xr[kc * 8 + q];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[c] = dot4(xv[q], ys[c * 8 + q], acc[c]);
+      }
+    }
+#pragma unroll
+    for (int c0 = 0; c0 < 32; c0 += kFmaJ) {
+      float s[kFmaJ];
+#pragma unroll
+      for (int j = 0; j < kFmaJ; ++j) s[j] = fmaf(kappa, acc[c0 + j], cs[c0 + j]);
+      lse_chunk<kFmaJ>(s, M, S);
+    }
+  }
+  if (row < n_rows) partial[blockIdx.y * ld + row] = make_float2(M, S);
+}
+
+// Final write of a weighted-sum row (shared by the two wsum kernels).
+template <int MODE>
+__device__ __forceinline__ void wsum_store(const float (&acc)[32], float sumw, float had,
+                                           int64_t row, int64_t o0, int64_t k,
+                                           const float* __restrict__ rowW,
+                                           const float* __restrict__ Xrow, int64_t d,
+                                           float* __restrict__ out, int64_t ldo) {
+  if constexpr (MODE == kWsumHadamard) {
+    out[row] = had;
+  } else if constexpr (MODE == kWsumGrad) {
+    // grad_i = 2 a_i (x_i - yhat_i), yhat_i = sum_j w_ij y_j / sum_j w_ij
+    const float a = rowW[row];
+    const float inv = sumw > 0.0f ? 1.0f / sumw : 0.0f;
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+      const int64_t oo = o0 + o;
+      if (oo < d) out[row * ldo + oo] = a > 0.0f ? 2.0f * a * (Xrow[row * d + oo] - acc[o] * inv)
+                                                 : 0.0f;
+    }
+  } else {
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+      const int64_t oo = o0 + o;
+      if (oo < k) out[row * ldo + oo] = acc[o];
+    }
+  }
+}
+
+// Stage a 32-column x 32-output tile of V (rows of V are the pass's columns j), zero
+// padded in both directions.
+__device__ __forceinline__ void stage_v_tile(float (*vs)[33], const float* __restrict__ V,
+                                             int64_t ldv, int64_t n_cols, int64_t k,
+                                             int64_t j0, int64_t o0, int tid) {
+  for (int e = tid; e < 32 * 32; e += kFmaThreads) {
+    const int c = e >> 5, o = e & 31;
+    const int64_t j = j0 + c, oo = o0 + o;
+    vs[c][o] = (j < n_cols && oo < k) ? V[j * ldv + oo] : 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Weighted sums, d_pad = DP <= 32. One row per thread; output columns [o0, o0+32) per
+// blockIdx.y. w_ij = exp2(kappa <p_i, q_j> + c_j + r_i).
+//  Apply:    out_i[o] = sum_j w_ij V_j[o]
+//  Grad:     V = packed column points; out_i = 2 a_i (x_i - sum_j w_ij q_j / sum_j w_ij)
+//  Hadamard: out_i = sum_j w_ij <p_i, q_j>
+// ---------------------------------------------------------------------------------------
+template <int DP, int MODE>
+__global__ void __launch_bounds__(kFmaThreads)
+wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
+                      const float* __restrict__ colBias, const float* __restrict__ rowBias,
+                      int64_t n_rows, int64_t n_cols, int n_col_tiles, float kappa,
+                      const float* __restrict__ V, int64_t ldv, int64_t k,
+                      const float* __restrict__ rowW, const float* __restrict__ Xrow,
+                      int64_t d, float* __restrict__ out, int64_t ldo) {
+  constexpr int Q = DP / 4;
+  __shared__ float4 ys[32 * Q];
+  __shared__ float cs[32];
+  __shared__ float vs[32][33];
+  const int tid = threadIdx.x;
+  const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
+  const int64_t o0 = (int64_t)blockIdx.y * 32;
+  float4 x[Q];
+  const float4* xr = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * DP);
+#pragma unroll
+  for (int q = 0; q < Q; ++q) x[q] = xr[q];
+  const float rb = row < n_rows ? rowBias[row] : neg_inf();
+  float acc[32];
+#pragma unroll
+  for (int o = 0; o < 32; ++o) acc[o] = 0.0f;
+  float sumw = 0.0f, had = 0.0f;
+  for (int t = 0; t < n_col_tiles; ++t) {
+    __syncthreads();
+    const float4* src = reinterpret_cast<const float4*>(colP + (int64_t)t * 32 * DP);
+    for (int e = tid; e < 32 * Q; e += kFmaThreads) ys[e] = src[e];
+    if (tid < 32) cs[tid] = colBias[(int64_t)t * 32 + tid];
+    if constexpr (MODE != kWsumHadamard) stage_v_tile(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
+    __syncthreads();
+#pragma unroll 4
+    for (int c = 0; c < 32; ++c) {
+      float dot = 0.0f;
+#pragma unroll
+      for (int q = 0; q < Q; ++q) dot = dot4(x[q], ys[c * Q + q], dot);
+      const float w = ex2(fmaf(kappa, dot, cs[c]) + rb);
+      if constexpr (MODE == kWsumHadamard) {
+        had = fmaf(w, dot, had);
+      } else {
+#pragma unroll
+        for (int o = 0; o < 32; ++o) acc[o] = fmaf(w, vs[c][o], acc[o]);
+        if constexpr (MODE == kWsumGrad) sumw += w;
+      }
+    }
+  }
+  if (row < n_rows) wsum_store<MODE>(acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+}
+
+// Weighted sums, any d_pad (multiple of 32): dots for 32 columns accumulated over 32-wide
+// k-chunks, then the same epilogue as the small-d kernel.
+template <int MODE>
+__global__ void __launch_bounds__(kFmaThreads)
+wsum_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
+                        const float* __restrict__ colBias, const float* __restrict__ rowBias,
+                        int64_t n_rows, int64_t n_cols, int n_col_tiles, int64_t d_pad,
+                        float kappa, const float* __restrict__ V, int64_t ldv, int64_t k,
+                        const float* __restrict__ rowW, const float* __restrict__ Xrow,
+                        int64_t d, float* __restrict__ out, int64_t ldo) {
+  __shared__ float4 ys[32 * 8];
+  __shared__ float cs[32];
+  __shared__ float vs[32][33];
+  const int tid = threadIdx.x;
+  const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
+  const int64_t o0 = (int64_t)blockIdx.y * 32;
+  const float4* xr = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * d_pad);
+  const int nkc = (int)(d_pad / 32);
+  const float rb = row < n_rows ? rowBias[row] : neg_inf();
+  float out_acc[32];
+#pragma unroll
+  for (int o = 0; o < 32; ++o) out_acc[o] = 0.0f;
+  float sumw = 0.0f, had = 0.0f;
+  for (int t = 0; t < n_col_tiles; ++t) {
+    float acc[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+    for (int kc = 0; kc < nkc; ++kc) {
+      __syncthreads();
+      for (int e = tid; e < 256; e += kFmaThreads) {
+        const int c = e >> 3, q = e & 7;
+        ys[e] = reinterpret_cast<const float4*>(colP + ((int64_t)t * 32 + c) * d_pad +
+                                                (int64_t)kc * 32)[q];
+      }
+      if (kc == 0) {
+        if (tid < 32) cs[tid] = colBias[(int64_t)t * 32 + tid];
+        if constexpr (MODE != kWsumHadamard)
+          stage_v_tile(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
+      }
+      __syncthreads();
+      float4 xv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xv[q] = xr[kc * 8 + q];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[c] = dot4(xv[q], ys[c * 8 + q], acc[c]);
+      }
+    }
+#pragma unroll 4
+    for (int c = 0; c < 32; ++c) {
+      const float w = ex2(fmaf(kappa, acc[c], cs[c]) + rb);
+      if constexpr (MODE == kWsumHadamard) {
+        had = fmaf(w, acc[c], had);
+      } else {
+#pragma unroll
+        for (int o = 0; o < 32; ++o) out_acc[o] = fmaf(w, vs[c][o], out_acc[o]);
+        if constexpr (MODE == kWsumGrad) sumw += w;
+      }
+    }
+  }
+  if (row < n_rows) wsum_store<MODE>(out_acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+}
+
+}  // namespace flashot

@@ -1,0 +1,120 @@
+// prep_kernels.cuh -- packing, norms, log-weights, score biases, LSE combine and loss.
+//
+// These are the O((n + m) d) steps around the streaming passes: they fold the norms
+// |x|^2, |y|^2 and the log-weights into per-row / per-column biases (FlashSinkhorn, SAI
+// replication review, "Weaknesses": cost of the form c_ij = alpha_i + beta_j - Q_i^T K_j).
+#pragma once
+
+#include "common.cuh"
+#include "pack_kernels.cuh"
+
+namespace flashot {
+
+// norms[r] = |src_r|^2 from the fp32 input (one warp per row); 0 for padding rows.
+__global__ void row_norms_kernel(const float* __restrict__ src, int64_t rows, int64_t d,
+                                 int64_t rows_pad, float* __restrict__ norms) {
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows_pad) return;
+  float s = 0.0f;
+  if (warp < rows) {
+    const float* p = src + warp * d;
+    for (int64_t c = lane; c < d; c += 32) s = fmaf(p[c], p[c], s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) norms[warp] = s;
+}
+
+// w_out[i] = w[i] (or 1/rows if w == NULL), lw2[i] = log2 w_out[i]; padding: 0 and -inf.
+// The first thread also clears the workspace status word.
+__global__ void weights_kernel(const float* __restrict__ w, int64_t rows, int64_t rows_pad,
+                               float* __restrict__ w_out, float* __restrict__ lw2,
+                               unsigned* __restrict__ status) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i == 0 && status != nullptr) *status = 0u;
+  if (i >= rows_pad) return;
+  if (i < rows) {
+    const float v = w ? w[i] : (float)(1.0 / (double)rows);
+    w_out[i] = v;
+    lw2[i] = v > 0.0f ? log2f(v) : neg_inf();
+  } else {
+    w_out[i] = 0.0f;
+    lw2[i] = neg_inf();
+  }
+}
+
+// Column (or row) bias of a pass whose "other side" has potential pot:
+//   bias_i = (pot_i - norm_i) log2(e) / eps + lw2_i ;  pot == NULL means pot = 0.
+// Padding entries get -inf so they never contribute.
+__global__ void bias_kernel(const float* __restrict__ pot, const float* __restrict__ norms,
+                            const float* __restrict__ lw2, int64_t rows, int64_t rows_pad,
+                            float inv_eps_log2e, float* __restrict__ bias) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= rows_pad) return;
+  if (i < rows) {
+    const float p = pot ? pot[i] : 0.0f;
+    bias[i] = (p - norms[i]) * inv_eps_log2e + lw2[i];
+  } else {
+    bias[i] = neg_inf();
+  }
+}
+
+// Merge per-split (max, sum) partials of the base-2 LSE and finish the half-step:
+//   L_i  = M + log2 S,   pot_i = norm_i - eps ln2 L_i,
+//   next_bias_i = lw2_i - L_i * (eps / eps_next)   (= (pot_i - norm_i) log2e/eps_next + lw2_i)
+// next_bias is the bias the following pass (the other side's update at eps_next) needs;
+// its padding entries [rows, rows_pad) are set to -inf so padded points carry no mass.
+__global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo split,
+                                   int64_t ld, int64_t rows, int64_t rows_pad,
+                                   const float* __restrict__ norms, float eps,
+                                   const float* __restrict__ lw2, float eps_ratio,
+                                   float* __restrict__ out_pot, float* __restrict__ next_bias,
+                                   float* __restrict__ out_lse2) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= rows) {
+    if (i < rows_pad && next_bias) next_bias[i] = neg_inf();
+    return;
+  }
+  int n_splits = split.n_splits;
+  if (n_splits == 0) {
+    const int64_t rt = i / 128;
+    n_splits = (int)(sk_owner((rt + 1) * split.sk_NT - 1, split.sk_T, split.sk_G) -
+                     sk_owner(rt * split.sk_NT, split.sk_T, split.sk_G) + 1);
+  }
+  float M = kNegBig;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, partial[s * ld + i].x);
+  float S = 0.0f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float2 p = partial[s * ld + i];
+    S += p.y * ex2(p.x - M);
+  }
+  const float L = M + log2f(S);  // S == 0 (no mass) gives -inf, so pot = +inf
+  const float pot = norms[i] - eps * kLn2 * L;
+  if (out_pot) out_pot[i] = pot;
+  if (next_bias) next_bias[i] = lw2[i] - L * eps_ratio;
+  if (out_lse2) out_lse2[i] = L;
+}
+
+// loss = sum_i wa_i f_i + sum_j wb_j g_j in fp64; one block, deterministic order.
+__global__ void __launch_bounds__(1024)
+dual_loss_kernel(const float* __restrict__ wa, const float* __restrict__ f, int64_t n,
+                 const float* __restrict__ wb, const float* __restrict__ g, int64_t m,
+                 double* __restrict__ loss) {
+  __shared__ double red[32];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += (double)wa[i] * (double)f[i];
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) s += (double)wb[j] * (double)g[j];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    s = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) *loss = s;
+  }
+}
+
+}  // namespace flashot

@@ -1,0 +1,820 @@
+// tc_kernels.cu -- tcgen05 (5th-generation tensor core) streaming passes for sm_103a.
+//
+// The half-step of stabilized log-domain Sinkhorn is a row-wise log-sum-exp of biased
+// dot-product scores (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract;
+// SAI replication review, "Summary": tiles of Q and K streamed through on-chip memory,
+// scores formed on the fly, running row-wise LSE statistics, only potentials written
+// back). On sm_103a the score tile S = P_rows * Q_cols^T is a dense contraction, so it
+// runs on tcgen05.mma with the 128 x 128 fp32 accumulator in Tensor Memory:
+//
+//   warp 0      TMA producer: row tile (resident when it fits) + column-tile K-chunks
+//               into a ring of shared-memory stages (128-byte swizzle);
+//   warp 1      MMA issuer: one elected thread issues tcgen05.mma into one of two TMEM
+//               accumulators and tcgen05.commit's stage / accumulator barriers;
+//   warps 2..5  epilogue: tcgen05.ld the S tile (one row per thread), add the column
+//               bias, online base-2 max / sum-exp (MUFU ex2), while the MMA fills the
+//               other accumulator.
+//
+// Work split: the (row tile, column tile) pairs are linearised row-tile-major and cut
+// into gridDim.x contiguous ranges, one per persistent CTA ("stream-K"), so every SM
+// gets the same number of tiles to within one. A CTA emits one (max, sum) partial per
+// row tile it touches; lse_combine_kernel merges them (at most kMaxSplits per row).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "flashot.h"
+#include "common.cuh"
+#include "pack_kernels.cuh"
+#include "ptx.cuh"
+#include "tc_api.h"
+#include "trace.h"
+
+namespace flashot {
+namespace tc {
+
+constexpr int kBM = 128;                 // rows per tile (MMA M)
+constexpr int kBN = 128;                 // columns per tile (MMA N)
+constexpr int kChunk = 128 * 128;        // bytes of one 128-row x 128-byte K-chunk box
+constexpr int kThreads = 192;            // 6 warps
+constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 256;      // two 128-column fp32 accumulators
+constexpr int kSmemLimit = 232448;       // 227 KB per block (opt-in maximum)
+
+struct __align__(128) Ctrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t a_full;
+  uint64_t a_empty;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  float bias[4][2][kBN];                 // per epilogue warp, double-buffered column bias
+};
+
+__device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
+  atomicOr(status, kErrTimeout);
+  ctl.abort_flag = 1;
+}
+
+// ---------------------------------------------------------------------------------------
+// LSE pass: partial[slot * ld + row] = (max_j s2_ij, sum_j 2^(s2_ij - max)) over the
+// column tiles of this CTA's range, s2_ij = kappa <p_i, q_j> + colBias_j.
+// kARes: the row tile (all K-chunks) stays in shared memory for a whole segment.
+// ---------------------------------------------------------------------------------------
+template <bool kBF16, bool kARes>
+__global__ void __launch_bounds__(kThreads, 1)
+lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
+              int kc_count, int stages, float kappa, float2* __restrict__ partial, int64_t ld,
+              unsigned* __restrict__ status) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Ctrl ctl;
+  constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = ptx::smem_u32(dyn_smem);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = dyn_smem + (base - raw);
+  const uint32_t a_bytes = kARes ? (uint32_t)kc_count * kChunk : 0u;
+  const uint32_t stage_bytes = kARes ? (uint32_t)kChunk : 2u * kChunk;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
+  const int64_t t_begin = sk_begin(cta, T, G), t_end = sk_begin(cta + 1, T, G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(&ctl.full[s], 1);
+      ptx::mbar_init(&ctl.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl.acc_full[b], 1);
+      ptx::mbar_init(&ctl.acc_empty[b], 128);
+    }
+    ptx::mbar_init(&ctl.a_full, 1);
+    ptx::mbar_init(&ctl.a_empty, 1);
+    ptx::mbar_init(&ctl.mma_done, 1);
+    ctl.abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&mapA);
+    ptx::tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------- TMA producer -------------------------------------
+      uint32_t stage = 0, ph = 0, a_ph = 0;
+      int64_t issued = 0, a_issued = 0;
+      bool ok = true;
+      for (int64_t t = t_begin; ok && t < t_end;) {
+        const int64_t rt = t / NT;
+        const int64_t seg_end = min(t_end, (rt + 1) * NT);
+        if constexpr (kARes) {
+          if (!ptx::mbar_wait(&ctl.a_empty, a_ph ^ 1u)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.a_full, a_bytes);
+          for (int kc = 0; kc < kc_count; ++kc)
+            ptx::tma_load_2d(&mapA, &ctl.a_full, smem + (size_t)kc * kChunk, kc * kElems,
+                             (int)(rt * kBM));
+          a_ph ^= 1u;
+          ++a_issued;
+        }
+        for (int64_t tt = t; ok && tt < seg_end; ++tt) {
+          const int jt = (int)(tt - rt * NT);
+          for (int kc = 0; kc < kc_count; ++kc) {
+            if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
+            uint8_t* st = smem + a_bytes + (size_t)stage * stage_bytes;
+            if constexpr (kARes) {
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage], kChunk);
+              ptx::tma_load_2d(&mapB, &ctl.full[stage], st, kc * kElems, jt * kBN);
+            } else {
+              ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * kChunk);
+              ptx::tma_load_2d(&mapA, &ctl.full[stage], st, kc * kElems, (int)(rt * kBM));
+              ptx::tma_load_2d(&mapB, &ctl.full[stage], st + kChunk, kc * kElems, jt * kBN);
+            }
+            ++issued;
+            if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
+          }
+        }
+        t = seg_end;
+      }
+      if (!ok) flag_error(ctl, status);
+      // Drain: every copy issued must have landed before the CTA may exit.
+      for (int s = 0; s < stages; ++s) {
+        const int64_t arms = issued / stages + (s < issued % stages ? 1 : 0);
+        if (arms > 0) ptx::mbar_wait(&ctl.full[s], (uint32_t)((arms - 1) & 1));
+      }
+      if (a_issued > 0) ptx::mbar_wait(&ctl.a_full, (uint32_t)((a_issued - 1) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------- MMA issuer ----------------------------------------
+      constexpr uint32_t idesc = ptx::make_idesc<kBF16>(kBM, kBN);
+      uint32_t stage = 0, ph = 0, a_ph = 0, ab = 0, acc_ph = 0;
+      bool ok = true;
+      for (int64_t t = t_begin; ok && t < t_end;) {
+        const int64_t rt = t / NT;
+        const int64_t seg_end = min(t_end, (rt + 1) * NT);
+        if constexpr (kARes) {
+          if (!ptx::mbar_wait(&ctl.a_full, a_ph)) { ok = false; break; }
+          a_ph ^= 1u;
+          ptx::tc_fence_after();
+        }
+        for (int64_t tt = t; ok && tt < seg_end; ++tt) {
+          if (!ptx::mbar_wait(&ctl.acc_empty[ab], acc_ph ^ 1u)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem + ab * kBN;
+          for (int kc = 0; kc < kc_count; ++kc) {
+            if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + a_bytes + stage * stage_bytes;
+            const uint32_t a_addr = kARes ? base + (uint32_t)kc * kChunk : st;
+            const uint32_t b_addr = kARes ? st : st + kChunk;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::umma<kBF16>(d_tmem, ptx::sdesc_k128(a_addr + kk * 32),
+                               ptx::sdesc_k128(b_addr + kk * 32), idesc,
+                               (kc | kk) != 0 ? 1u : 0u);
+            ptx::umma_commit(&ctl.empty[stage]);
+            if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          ptx::umma_commit(&ctl.acc_full[ab]);
+          if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+        }
+        if constexpr (kARes) ptx::umma_commit(&ctl.a_empty);
+        t = seg_end;
+      }
+      if (!ok) flag_error(ctl, status);
+      // Every MMA issued must have retired before Tensor Memory is released.
+      ptx::umma_commit(&ctl.mma_done);
+      ptx::mbar_wait(&ctl.mma_done, 0);
+    }
+  } else {
+    // --------------------------------- epilogue ------------------------------------------
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int ew = warp - 2;           // private bias buffer
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t ab = 0, acc_ph = 0, bb = 0;
+    bool ok = true;
+    float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t_begin < t_end)
+      bnext = __ldg(reinterpret_cast<const float4*>(colBias + (t_begin % NT) * kBN) + lane);
+    for (int64_t t = t_begin; ok && t < t_end;) {
+      const int64_t rt = t / NT;
+      const int64_t seg_end = min(t_end, (rt + 1) * NT);
+      float M = kNegBig, S = 0.0f;
+      for (int64_t tt = t; tt < seg_end; ++tt) {
+        reinterpret_cast<float4*>(ctl.bias[ew][bb])[lane] = bnext;
+        if (tt + 1 < t_end)
+          bnext = __ldg(reinterpret_cast<const float4*>(colBias + ((tt + 1) % NT) * kBN) + lane);
+        __syncwarp();
+        if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        float v[kBN];
+        ptx::tmem_ld_x128_sync(tmem + lane_base + ab * kBN, v);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl.acc_empty[ab]);
+        if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+        const float4* cb = reinterpret_cast<const float4*>(ctl.bias[ew][bb]);
+        float mx = kNegBig;
+#pragma unroll
+        for (int j = 0; j < kBN; j += 4) {
+          const float4 b4 = cb[j / 4];
+          v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
+          v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
+          v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
+          v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
+          mx = fmaxf(mx, fmaxf(fmaxf(v[j], v[j + 1]), fmaxf(v[j + 2], v[j + 3])));
+        }
+        if (mx > M) {
+          S *= ex2(M - mx);
+          M = mx;
+        }
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < kBN; j += 4) {
+          s0 += ex2(v[j + 0] - M);
+          s1 += ex2(v[j + 1] - M);
+          s2 += ex2(v[j + 2] - M);
+          s3 += ex2(v[j + 3] - M);
+        }
+        S += (s0 + s1) + (s2 + s3);
+        bb ^= 1u;
+      }
+      if (!ok) break;
+      const int64_t row = rt * kBM + q * 32 + lane;
+      const int64_t slot = cta - sk_owner(rt * NT, T, G);
+      if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
+      t = seg_end;
+    }
+    if (!ok) flag_error(ctl, status);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Weighted-sum pass: transport application, barycentric gradient, Hadamard-weighted
+// transport (FlashSinkhorn, SAI replication review, "Summary" (i)-(ii)). Per CTA = (row
+// tile, group of kKV output columns):
+//   S   = rows * cols^T                      tcgen05.mma, double-buffered in TMEM
+//   w_ij = exp2(kappa S_ij + colBias_j + rowBias_i)         epilogue, fp32 + MUFU ex2
+//   O   += W * V^T-tile                      second tcgen05.mma, W written to shared memory
+//                                            by the epilogue in the swizzled K-major layout
+// The weights are bounded (plan entries, or a_i times softmax weights), so no running max
+// is needed. The S MMA of tile j+1 overlaps the epilogue of tile j. kKV == 0: Hadamard
+// only (h_i = sum_j w_ij S_ij, no second MMA).
+// ---------------------------------------------------------------------------------------
+constexpr int kWsMaxStages = 4;
+
+struct __align__(128) WCtrl {
+  uint64_t full[kWsMaxStages];
+  uint64_t empty[kWsMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t w_full[2];
+  uint64_t w_empty[2];
+  uint64_t v_full[2];
+  uint64_t v_empty[2];
+  uint64_t o_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  float bias[4][2][kBN];
+};
+
+__device__ __forceinline__ void flag_error_w(WCtrl& ctl, unsigned* status) {
+  atomicOr(status, kErrTimeout);
+  ctl.abort_flag = 1;
+}
+
+template <bool kBF16, int kMode, int kKV>
+__global__ void __launch_bounds__(kThreads, 1)
+wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+               const __grid_constant__ CUtensorMap mapV, const float* __restrict__ colBias,
+               const float* __restrict__ rowBias, int64_t n_rows, int NT, int kc_count, int n_st,
+               int n_w, int n_v, float kappa, const float* __restrict__ rowW,
+               const float* __restrict__ Xrow, int64_t d, int64_t k, float* __restrict__ out,
+               int64_t ldo, unsigned* __restrict__ status) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ WCtrl ctl;
+  constexpr bool kHad = (kKV == 0);
+  constexpr int es = kBF16 ? 2 : 4;
+  constexpr int kElems = 128 / es;                       // elements per 128-byte K-chunk row
+  constexpr int kWChunks = kBN * es / 128;               // K-chunks over the 128 columns j
+  constexpr uint32_t kWBytes = (uint32_t)kWChunks * kChunk;
+  constexpr uint32_t kVChunkBytes = (uint32_t)(kKV > 0 ? kKV : 1) * 128;
+  constexpr uint32_t kVBytes = kHad ? 0u : (uint32_t)kWChunks * kVChunkBytes;
+  constexpr int kVBoxRows = kKV > 128 ? 128 : (kKV > 0 ? kKV : 1);
+  constexpr uint32_t kTmemCols = kHad ? 256u : 512u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = ptx::smem_u32(dyn_smem);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = dyn_smem + (base - raw);
+  const uint32_t st_base = 0;
+  const uint32_t w_base = (uint32_t)n_st * 2u * kChunk;
+  const uint32_t v_base = w_base + (uint32_t)n_w * kWBytes;
+  const int64_t rt = blockIdx.x;
+  const int64_t o0 = (int64_t)blockIdx.y * kKV;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < n_st; ++s) {
+      ptx::mbar_init(&ctl.full[s], 1);
+      ptx::mbar_init(&ctl.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl.acc_full[b], 1);
+      ptx::mbar_init(&ctl.acc_empty[b], 128);
+      ptx::mbar_init(&ctl.w_full[b], 128);
+      ptx::mbar_init(&ctl.w_empty[b], 1);
+      ptx::mbar_init(&ctl.v_full[b], 1);
+      ptx::mbar_init(&ctl.v_empty[b], 1);
+    }
+    ptx::mbar_init(&ctl.o_full, 1);
+    ptx::mbar_init(&ctl.mma_done, 1);
+    ctl.abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&mapA);
+    ptx::tma_prefetch_desc(&mapB);
+    if constexpr (!kHad) ptx::tma_prefetch_desc(&mapV);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------- TMA producer -------------------------------------
+      uint32_t stage = 0, ph = 0;
+      int64_t issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int jt = 0; ok && jt < NT; ++jt) {
+        for (int kc = 0; kc < kc_count; ++kc) {
+          if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
+          uint8_t* st = smem + st_base + (size_t)stage * 2 * kChunk;
+          ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * kChunk);
+          ptx::tma_load_2d(&mapA, &ctl.full[stage], st, kc * kElems, (int)(rt * kBM));
+          ptx::tma_load_2d(&mapB, &ctl.full[stage], st + kChunk, kc * kElems, jt * kBN);
+          ++issued;
+          if (++stage == (uint32_t)n_st) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        if constexpr (!kHad) {
+          const int vs = jt % n_v;
+          if (!ptx::mbar_wait(&ctl.v_empty[vs], (uint32_t)((jt / n_v) & 1) ^ 1u)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.v_full[vs], kVBytes);
+          uint8_t* vt = smem + v_base + (size_t)vs * kVBytes;
+          for (int vc = 0; vc < kWChunks; ++vc)
+            for (int ob = 0; ob < kKV / kVBoxRows; ++ob)
+              ptx::tma_load_2d(&mapV, &ctl.v_full[vs], vt + (size_t)vc * kVChunkBytes + ob * kVBoxRows * 128,
+                               jt * kBN + vc * kElems, (int)(o0 + ob * kVBoxRows));
+          ++v_issued;
+        }
+      }
+      if (!ok) flag_error_w(ctl, status);
+      for (int s = 0; s < n_st; ++s) {
+        const int64_t arms = issued / n_st + (s < issued % n_st ? 1 : 0);
+        if (arms > 0) ptx::mbar_wait(&ctl.full[s], (uint32_t)((arms - 1) & 1));
+      }
+      for (int s = 0; s < n_v; ++s) {
+        const int64_t arms = v_issued / n_v + (s < v_issued % n_v ? 1 : 0);
+        if (arms > 0) ptx::mbar_wait(&ctl.v_full[s], (uint32_t)((arms - 1) & 1));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------- MMA issuer ----------------------------------------
+      constexpr uint32_t idesc_s = ptx::make_idesc<kBF16>(kBM, kBN);
+      constexpr uint32_t idesc_o = ptx::make_idesc<kBF16>(kBM, kKV > 0 ? kKV : 128);
+      uint32_t stage = 0, ph = 0;
+      bool ok = true;
+      for (int t = 0; ok && t <= NT; ++t) {
+        if (t < NT) {
+          const uint32_t ab = (uint32_t)(t & 1);
+          if (!ptx::mbar_wait(&ctl.acc_empty[ab], (uint32_t)((t >> 1) & 1) ^ 1u)) { ok = false; break; }
+          ptx::tc_fence_after();
+          for (int kc = 0; kc < kc_count; ++kc) {
+            if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + st_base + stage * 2u * kChunk;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::umma<kBF16>(tmem + ab * kBN, ptx::sdesc_k128(st + kk * 32),
+                               ptx::sdesc_k128(st + kChunk + kk * 32), idesc_s,
+                               (kc | kk) != 0 ? 1u : 0u);
+            ptx::umma_commit(&ctl.empty[stage]);
+            if (++stage == (uint32_t)n_st) { stage = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          ptx::umma_commit(&ctl.acc_full[ab]);
+        }
+        if constexpr (!kHad) {
+          if (t >= 1) {
+            const int u = t - 1;
+            const int wb = u % n_w, vs = u % n_v;
+            if (!ptx::mbar_wait(&ctl.w_full[wb], (uint32_t)((u / n_w) & 1))) { ok = false; break; }
+            if (!ptx::mbar_wait(&ctl.v_full[vs], (uint32_t)((u / n_v) & 1))) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t wa = base + w_base + (uint32_t)wb * kWBytes;
+            const uint32_t va = base + v_base + (uint32_t)vs * kVBytes;
+#pragma unroll
+            for (int vc = 0; vc < kWChunks; ++vc) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::umma<kBF16>(tmem + 256, ptx::sdesc_k128(wa + vc * kChunk + kk * 32),
+                                 ptx::sdesc_k128(va + vc * kVChunkBytes + kk * 32), idesc_o,
+                                 (u | vc | kk) != 0 ? 1u : 0u);
+            }
+            ptx::umma_commit(&ctl.w_empty[wb]);
+            ptx::umma_commit(&ctl.v_empty[vs]);
+          }
+        }
+      }
+      if constexpr (!kHad) ptx::umma_commit(&ctl.o_full);
+      if (!ok) flag_error_w(ctl, status);
+      ptx::umma_commit(&ctl.mma_done);
+      ptx::mbar_wait(&ctl.mma_done, 0);
+    }
+  } else {
+    // --------------------------------- epilogue ------------------------------------------
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    const int rloc = q * 32 + lane;            // row within the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int64_t row = rt * kBM + rloc;
+    const float rb = row < n_rows ? rowBias[row] : neg_inf();
+    float sumw = 0.0f, had = 0.0f;
+    bool ok = true;
+    float4 bnext = __ldg(reinterpret_cast<const float4*>(colBias) + lane);
+    for (int jt = 0; jt < NT; ++jt) {
+      const int bb = jt & 1;
+      reinterpret_cast<float4*>(ctl.bias[ew][bb])[lane] = bnext;
+      if (jt + 1 < NT)
+        bnext = __ldg(reinterpret_cast<const float4*>(colBias + (int64_t)(jt + 1) * kBN) + lane);
+      __syncwarp();
+      const uint32_t ab = (uint32_t)(jt & 1);
+      if (!ptx::mbar_wait(&ctl.acc_full[ab], (uint32_t)((jt >> 1) & 1))) { ok = false; break; }
+      ptx::tc_fence_after();
+      float v[kBN];
+      ptx::tmem_ld_x128_sync(tmem + lane_base + ab * kBN, v);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&ctl.acc_empty[ab]);
+      const float4* cb = reinterpret_cast<const float4*>(ctl.bias[ew][bb]);
+#pragma unroll
+      for (int j = 0; j < kBN; j += 4) {
+        const float4 b4 = cb[j / 4];
+        const float w0 = ex2(fmaf(kappa, v[j + 0], b4.x) + rb);
+        const float w1 = ex2(fmaf(kappa, v[j + 1], b4.y) + rb);
+        const float w2 = ex2(fmaf(kappa, v[j + 2], b4.z) + rb);
+        const float w3 = ex2(fmaf(kappa, v[j + 3], b4.w) + rb);
+        if constexpr (kHad) {
+          had = fmaf(w0, v[j + 0], had);
+          had = fmaf(w1, v[j + 1], had);
+          had = fmaf(w2, v[j + 2], had);
+          had = fmaf(w3, v[j + 3], had);
+        }
+        sumw += (w0 + w1) + (w2 + w3);
+        v[j + 0] = w0;
+        v[j + 1] = w1;
+        v[j + 2] = w2;
+        v[j + 3] = w3;
+      }
+      if constexpr (!kHad) {
+        const int wb = jt % n_w;
+        if (!ptx::mbar_wait(&ctl.w_empty[wb], (uint32_t)((jt / n_w) & 1) ^ 1u)) { ok = false; break; }
+        const uint32_t wrow = base + w_base + (uint32_t)wb * kWBytes + (uint32_t)rloc * 128u;
+#pragma unroll
+        for (int c = 0; c < kWChunks; ++c) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint32_t p0, p1, p2, p3;
+            if constexpr (kBF16) {
+              const int j = c * 64 + u * 8;
+              __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j + 0], v[j + 1]);
+              __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
+              __nv_bfloat162 h3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
+              p0 = *reinterpret_cast<uint32_t*>(&h0);
+              p1 = *reinterpret_cast<uint32_t*>(&h1);
+              p2 = *reinterpret_cast<uint32_t*>(&h2);
+              p3 = *reinterpret_cast<uint32_t*>(&h3);
+            } else {
+              const int j = c * 32 + u * 4;
+              asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(p0) : "f"(v[j + 0]));
+              asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(p1) : "f"(v[j + 1]));
+              asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(p2) : "f"(v[j + 2]));
+              asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(p3) : "f"(v[j + 3]));
+            }
+            ptx::st_shared_v4(wrow + (uint32_t)c * kChunk + (uint32_t)((u ^ (rloc & 7)) << 4),
+                              p0, p1, p2, p3);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(&ctl.w_full[wb]);
+      }
+    }
+    if constexpr (kHad) {
+      if (ok && row < n_rows) out[row] = had;
+    } else {
+      if (ok && !ptx::mbar_wait(&ctl.o_full, 0)) ok = false;
+      if (ok) {
+        ptx::tc_fence_after();
+        const float a = (kMode == kWsumGrad && row < n_rows) ? rowW[row] : 0.0f;
+        const float inv = sumw > 0.0f ? 1.0f / sumw : 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < kKV / 32; ++c) {
+          float o[32];
+          ptx::tmem_ld_x32_sync(tmem + lane_base + 256 + c * 32, o);
+          if (row < n_rows) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int64_t oo = o0 + c * 32 + t;
+              if constexpr (kMode == kWsumGrad) {
+                if (oo < d)
+                  out[row * ldo + oo] = a > 0.0f ? 2.0f * a * (Xrow[row * d + oo] - o[t] * inv) : 0.0f;
+              } else {
+                if (oo < k) out[row * ldo + oo] = o[t];
+              }
+            }
+          }
+        }
+      }
+    }
+    if (!ok) flag_error_w(ctl, status);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host helpers -------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D map over a packed operand (rows x cols elements, row-major), box = 128 rows x 128 B,
+// 128-byte swizzle (the layout the UMMA K-major SW128 descriptor expects).
+int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return FLASHOT_ERR_CUDA;
+  const int es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kBM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
+}
+
+template <typename K>
+int set_smem(K kernel, int bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+// Number of persistent CTAs: at most one per SM, at most one per tile, and few enough
+// that no row tile is split over more than max_splits CTAs.
+int64_t choose_grid(int64_t row_tiles, int64_t NT, int sms, int max_splits) {
+  const int64_t T = row_tiles * NT;
+  int64_t G = std::min<int64_t>(sms, T);
+  while (G > 1) {
+    int64_t worst = 0;
+    for (int64_t rt = 0; rt < row_tiles; ++rt) {
+      const int64_t s = sk_owner((rt + 1) * NT - 1, T, G) - sk_owner(rt * NT, T, G) + 1;
+      worst = std::max(worst, s);
+    }
+    if (worst <= max_splits) break;
+    --G;
+  }
+  return std::max<int64_t>(G, 1);
+}
+
+}  // namespace tc
+
+using namespace tc;
+
+int tc_pack_inputs(bool bf16, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,
+                   int64_t n_pad, int64_t m_pad, int64_t dpt, void* xq, void* yq, int sms,
+                   cudaStream_t st) {
+  const int T = 256;
+  const unsigned g1 = (unsigned)std::min<int64_t>((n_pad * dpt + T - 1) / T, (int64_t)sms * 16);
+  const unsigned g2 = (unsigned)std::min<int64_t>((m_pad * dpt + T - 1) / T, (int64_t)sms * 16);
+  if (bf16) {
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_kernel<PackKind::BF16><<<g1, T, 0, st>>>(X, xq, n, d, n_pad, dpt); }
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_kernel<PackKind::BF16><<<g2, T, 0, st>>>(Y, yq, m, d, m_pad, dpt); }
+  } else {
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_kernel<PackKind::TF32><<<g1, T, 0, st>>>(X, xq, n, d, n_pad, dpt); }
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_kernel<PackKind::TF32><<<g2, T, 0, st>>>(Y, yq, m, d, m_pad, dpt); }
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+template <bool kBF16, bool kARes>
+static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float* colBias,
+                      int64_t n_rows, int64_t NT, int64_t T, int kc, int64_t G, float kappa,
+                      float2* partial, int64_t ld, unsigned* status, cudaStream_t st) {
+  const int ctrl = (int)sizeof(Ctrl);
+  const int a_bytes = kARes ? kc * kChunk : 0;
+  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
+  const int budget = kSmemLimit - ctrl - 1024 - a_bytes;
+  const int stages = std::min(kMaxStages, budget / stage_bytes);
+  if (stages < 2) return FLASHOT_ERR_INVALID_ARG;
+  const int dyn = a_bytes + stages * stage_bytes + 1024;
+  auto kern = lse_tc_kernel<kBF16, kARes>;
+  int rc = set_smem(kern, dyn);
+  if (rc != FLASHOT_OK) return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_LSE, st);
+    kern<<<(unsigned)G, kThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages, kappa,
+                                             partial, ld, status);
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colBias,
+                int64_t n_rows, int64_t rows_pad, int64_t cols_pad, int64_t dpt, float kappa,
+                float2* partial, int max_splits, int sms, unsigned* status, SplitInfo* info,
+                cudaStream_t st) {
+  const int es = bf16 ? 2 : 4;
+  const int kc = (int)(dpt * es / 128);
+  const int64_t row_tiles = rows_pad / kBM, NT = cols_pad / kBN;
+  const int64_t T = row_tiles * NT;
+  const int64_t G = choose_grid(row_tiles, NT, sms, max_splits);
+  CUtensorMap mA, mB;
+  int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
+  if (rc == FLASHOT_OK) rc = make_map(&mB, colQ, cols_pad, dpt, bf16);
+  if (rc != FLASHOT_OK) return rc;
+  info->n_splits = 0;
+  info->sk_T = T;
+  info->sk_G = G;
+  info->sk_NT = NT;
+  const bool ares = kc * kChunk <= 128 * 1024;
+  if (bf16) {
+    return ares ? launch_lse<true, true>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
+                                         rows_pad, status, st)
+                : launch_lse<true, false>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
+                                          rows_pad, status, st);
+  }
+  return ares ? launch_lse<false, true>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
+                                        rows_pad, status, st)
+              : launch_lse<false, false>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
+                                         rows_pad, status, st);
+}
+
+template <bool kBF16, int kMode, int kKV>
+static int launch_wsum(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mV,
+                       const float* colBias, const float* rowBias, int64_t n_rows,
+                       int64_t row_tiles, int groups, int NT, int kc, float kappa,
+                       const float* rowW, const float* X, int64_t d, int64_t k, float* out,
+                       int64_t ldo, unsigned* status, cudaStream_t st) {
+  constexpr int es = kBF16 ? 2 : 4;
+  const int w_bytes = (kKV == 0) ? 0 : kBN * es * 128;             // 128 rows x 128 columns
+  const int v_bytes = (kKV == 0) ? 0 : kKV * 128 * (kBN * es / 128);
+  const int budget = kSmemLimit - (int)sizeof(WCtrl) - 1024;
+  // At least 2 operand stages, one W and one V buffer; then double W, double V, more stages.
+  int n_st = 2, n_w = (kKV == 0) ? 0 : 1, n_v = (kKV == 0) ? 0 : 1;
+  auto total = [&]() { return n_st * 2 * kChunk + n_w * w_bytes + n_v * v_bytes; };
+  if (total() > budget) return FLASHOT_ERR_INVALID_ARG;
+  if (kKV != 0 && total() + w_bytes <= budget) ++n_w;
+  if (kKV != 0 && total() + v_bytes <= budget) ++n_v;
+  while (n_st < kWsMaxStages && total() + 2 * kChunk <= budget) ++n_st;
+  const int dyn = total() + 1024;
+  auto kern = wsum_tc_kernel<kBF16, kMode, kKV>;
+  int rc = set_smem(kern, dyn);
+  if (rc != FLASHOT_OK) return rc;
+  dim3 grid((unsigned)row_tiles, (unsigned)groups);
+  {
+    TraceScope ts_(FLASHOT_KERNEL_WSUM, st);
+    kern<<<grid, kThreads, dyn, st>>>(mA, mB, mV, colBias, rowBias, n_rows, NT, kc, n_st,
+                                      std::max(n_w, 1), std::max(n_v, 1), kappa, rowW, X, d, k,
+                                      out, ldo, status);
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+// 2-D map over the transposed right operand (out_rows x cols_pad), box = box_rows x 128 B.
+int make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16,
+                  int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return FLASHOT_ERR_CUDA;
+  const int es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
+}
+
+int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const float* colBias,
+                 const float* rowBias, int64_t n_rows, int64_t n_cols, int64_t rows_pad,
+                 int64_t cols_pad, int64_t d, int64_t dpt, float kappa, const float* V,
+                 int64_t ldv, int64_t k, void* vtq, const float* rowW, const float* X,
+                 float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st) {
+  (void)sms;
+  const int es = bf16 ? 2 : 4;
+  const int kc = (int)(dpt * es / 128);
+  const int64_t row_tiles = rows_pad / kBM;
+  const int NT = (int)(cols_pad / kBN);
+  CUtensorMap mA, mB, mV;
+  int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
+  if (rc == FLASHOT_OK) rc = make_map(&mB, colQ, cols_pad, dpt, bf16);
+  if (rc != FLASHOT_OK) return rc;
+  if (mode == kWsumHadamard) {
+    mV = mB;  // unused
+    return bf16 ? launch_wsum<true, kWsumHadamard, 0>(mA, mB, mV, colBias, rowBias, n_rows,
+                                                      row_tiles, 1, NT, kc, kappa, rowW, X, d, 1,
+                                                      out, ldo, status, st)
+                : launch_wsum<false, kWsumHadamard, 0>(mA, mB, mV, colBias, rowBias, n_rows,
+                                                       row_tiles, 1, NT, kc, kappa, rowW, X, d,
+                                                       1, out, ldo, status, st);
+  }
+  // Output-column group width: 64, 128, or 256 (bf16 only; tf32 W/V tiles are twice as big).
+  const int kv = (k <= 64) ? 64 : (k <= 128 || !bf16) ? 128 : 256;
+  const int groups = (int)((k + kv - 1) / kv);
+  const int64_t out_rows_pad = (int64_t)groups * kv;
+  if (ldv != k) return FLASHOT_ERR_INVALID_ARG;
+  {
+    dim3 blk(32, 8), grd((unsigned)(cols_pad / 32), (unsigned)(out_rows_pad / 32));
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+    if (bf16)
+      pack_transpose_kernel<PackKind::BF16><<<grd, blk, 0, st>>>(V, vtq, n_cols, k, cols_pad,
+                                                                 out_rows_pad);
+    else
+      pack_transpose_kernel<PackKind::TF32><<<grd, blk, 0, st>>>(V, vtq, n_cols, k, cols_pad,
+                                                                 out_rows_pad);
+  }
+  if (cudaGetLastError() != cudaSuccess) return FLASHOT_ERR_CUDA;
+  rc = make_map_rows(&mV, vtq, out_rows_pad, cols_pad, bf16, kv > 128 ? 128 : kv);
+  if (rc != FLASHOT_OK) return rc;
+#define FLASHOT_WSUM_TC(B, M, KV)                                                             \
+  launch_wsum<B, M, KV>(mA, mB, mV, colBias, rowBias, n_rows, row_tiles, groups, NT, kc, kappa, \
+                        rowW, X, d, k, out, ldo, status, st)
+  if (mode == kWsumGrad) {
+    if (bf16) {
+      if (kv == 64) return FLASHOT_WSUM_TC(true, kWsumGrad, 64);
+      if (kv == 128) return FLASHOT_WSUM_TC(true, kWsumGrad, 128);
+      return FLASHOT_WSUM_TC(true, kWsumGrad, 256);
+    }
+    if (kv == 64) return FLASHOT_WSUM_TC(false, kWsumGrad, 64);
+    return FLASHOT_WSUM_TC(false, kWsumGrad, 128);
+  }
+  if (bf16) {
+    if (kv == 64) return FLASHOT_WSUM_TC(true, kWsumApply, 64);
+    if (kv == 128) return FLASHOT_WSUM_TC(true, kWsumApply, 128);
+    return FLASHOT_WSUM_TC(true, kWsumApply, 256);
+  }
+  if (kv == 64) return FLASHOT_WSUM_TC(false, kWsumApply, 64);
+  return FLASHOT_WSUM_TC(false, kWsumApply, 128);
+#undef FLASHOT_WSUM_TC
+}
+
+}  // namespace flashot

@@ -1,0 +1,63 @@
+"""Helpers shared by the GPU parity tests: tensors from the seeded problems and the
+error measures the tolerances are stated in."""
+import numpy as np
+import torch
+
+# Tolerances (stated for the method's floating-point paths):
+#   potentials: relative L-inf error scaled by max|f|, <= 1e-4 for fp32/tf32 scores;
+#   loss:       relative error <= 1e-4 (fp32/tf32), <= 2e-3 for bf16 scores.
+# Only a loss bar is stated for bf16 scores; the potentials of that path are held to the
+# same relative 2e-3 (the loss <a,f> + <b,g> inherits their relative error).
+# The same bounds are used for transport application, Hadamard and gradient outputs
+# (scaled by the largest magnitude of the oracle's output).
+POT_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
+LOSS_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
+OUT_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
+
+
+def to_dev(arr):
+    return None if arr is None else torch.from_numpy(np.ascontiguousarray(arr)).cuda()
+
+
+def problem_tensors(pr, uniform_as_none=True):
+    X = to_dev(pr.X)
+    Y = to_dev(pr.Y)
+    a = None if (uniform_as_none and pr.uniform_weights) else to_dev(pr.a)
+    b = None if (uniform_as_none and pr.uniform_weights) else to_dev(pr.b)
+    return X, Y, a, b
+
+
+def scaled_linf(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = max(np.abs(ref).max(), 1e-30)
+    return float(np.abs(got - ref).max() / scale)
+
+
+def rel_err(got, ref):
+    return abs(float(got) - float(ref)) / max(abs(float(ref)), 1e-30)
+
+
+def pot_err(f, g, f_ref, g_ref):
+    """Relative L-inf error of the potential pair, scaled by the largest potential
+    magnitude of the reference: max(|f - f_ref|, |g - g_ref|) / max(|f_ref|, |g_ref|).
+    (f, g) are defined jointly, so one scale serves both."""
+    f, g, f_ref, g_ref = (np.asarray(x, np.float64) for x in (f, g, f_ref, g_ref))
+    scale = max(np.abs(f_ref).max(), np.abs(g_ref).max(), 1e-30)
+    return float(max(np.abs(f - f_ref).max(), np.abs(g - g_ref).max()) / scale)
+
+
+# Unit roundoff of the contraction's operands (round to nearest): fp32 2^-24, tf32 2^-11,
+# bf16 2^-9 (relative error of one rounded operand).
+OPERAND_U = {"fp32": 2.0 ** -24, "tf32": 2.0 ** -11, "bf16": 2.0 ** -9}
+
+
+def half_step_bound(precision, P, Q, eps, ref):
+    """Rigorous worst case of one half-step's error from rounding the operands of <p, q>:
+    each dot moves by at most 2u sum_k |p_k q_k|, each score by 2/eps times that, and the
+    soft-min f = -eps log sum ... by at most eps times the largest score error, so
+    |df_i| <= 4u max_j sum_k |p_ik||q_jk|. Plus the fp32 epilogue (1e-6 relative)."""
+    P = np.abs(np.asarray(P, np.float64))
+    Q = np.abs(np.asarray(Q, np.float64))
+    worst = (P @ Q.T).max(axis=1)
+    return 4.0 * OPERAND_U[precision] * worst + 1e-6 * np.abs(ref).max()
