@@ -51,6 +51,10 @@ def parse_args():
     p.add_argument("--precision", choices=["bf16", "tf32"], default="bf16")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-passes", type=int, default=0, metavar="P",
+                   help="profiling driver: pack once, run P f-updates and P g-updates of the "
+                        "workload (no timing, no JSON line) and exit; for ncu captures")
+    p.add_argument("--n", type=int, default=None, help="override n = m (profiling driver)")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -409,8 +413,42 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_profile_driver(args):
+    """A short, self-contained sequence of the hot kernel for profilers: one pack, then
+    alternating f- and g-updates of the workload (optionally with n = m overridden)."""
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    from workloads import make_problem, WORKLOADS
+    spec = dict(WORKLOADS[WORKLOAD_IDX])
+    if args.n:
+        spec["n"] = spec["m"] = args.n
+    spec.pop("k", None)
+    pr = make_problem(seed=1000 + WORKLOAD_IDX, **spec)
+    X = torch.from_numpy(pr.X).cuda()
+    Y = torch.from_numpy(pr.Y).cuda()
+    eps = float(pr.eps_schedule[0])
+    ws = lds.Workspace(lds.workspace_bytes(pr.n, pr.m, pr.d, 0, args.precision))
+    g = torch.zeros(pr.m, device="cuda")
+    f = torch.empty(pr.n, device="cuda")
+    lds.sinkhorn_step_f(X, Y, g, eps, precision=args.precision, out=f, workspace=ws)
+    for _ in range(args.profile_passes):
+        lds.sinkhorn_step_g(X, Y, f, eps, precision=args.precision, out=g, workspace=ws,
+                            reuse_pack=True)
+        lds.sinkhorn_step_f(X, Y, g, eps, precision=args.precision, out=f, workspace=ws,
+                            reuse_pack=True)
+    torch.cuda.synchronize()
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("device timeout reported")
+    print(f"profile driver: n=m={pr.n} d={pr.d} {args.precision}: "
+          f"{2 * args.profile_passes + 1} LSE passes, f[0]={float(f[0]):.6f}")
+
+
 def main():
     args = parse_args()
+    if args.profile_passes > 0:
+        run_profile_driver(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -52,6 +52,7 @@ SIGNATURES = {
     "flashot_timer_read": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(_c_i64),
                                           ctypes.POINTER(ctypes.c_double)]),
     "flashot_timer_stop": (ctypes.c_int, []),
+    "flashot_selftest_bounded_wait": (ctypes.c_int, [_vp, _c_i64, _vp]),
     "flashot_sinkhorn_solve": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.POINTER(ctypes.c_float),
         ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),

@@ -528,6 +528,18 @@ int flashot_workspace_status(void* ws, flashot_stream_t stream) {
   return FLASHOT_OK;
 }
 
+int flashot_selftest_bounded_wait(void* ws, int64_t limit_ns, flashot_stream_t stream) {
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return FLASHOT_ERR_INVALID_ARG;
+  int sms = 0;
+  int rc = current_device(&sms);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(ws)) return FLASHOT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FLASHOT_ERR_ALIGNMENT;
+  rc = tc_selftest_bounded_wait(static_cast<unsigned*>(ws), limit_ns,
+                                reinterpret_cast<cudaStream_t>(stream));
+  return rc == FLASHOT_OK ? launch_check() : rc;
+}
+
 int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const float* b,
                            int64_t n, int64_t m, int64_t d, const float* eps_sched, int n_stages,
                            int iters_per_stage, int flags, float* f, float* g, double* loss,

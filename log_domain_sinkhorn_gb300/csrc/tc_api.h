@@ -10,6 +10,9 @@
 
 namespace flashot {
 
+// Launch the bounded-wait self-test kernel (see flashot_selftest_bounded_wait).
+int tc_selftest_bounded_wait(unsigned* status, int64_t limit_ns, cudaStream_t st);
+
 // Pack X (n x d) and Y (m x d) fp32 into row-padded, K-padded operand copies for the
 // tensor cores: bf16 (round to nearest even) or tf32-rounded fp32.
 int tc_pack_inputs(bool bf16, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,

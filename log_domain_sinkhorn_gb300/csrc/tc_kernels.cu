@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdint>
 
 #include "flashot.h"
@@ -53,8 +54,10 @@ struct __align__(128) Ctrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  float bias[4][2][kBN];                 // per epilogue warp, double-buffered column bias
+  alignas(16) float bias[4][2][kBN];     // per epilogue warp, double-buffered column bias (float4 access)
 };
+
+static_assert(offsetof(Ctrl, bias) % 16 == 0, "bias is read with 16-byte vector loads");
 
 __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
   atomicOr(status, kErrTimeout);
@@ -297,8 +300,9 @@ struct __align__(128) WCtrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  float bias[4][2][kBN];
+  alignas(16) float bias[4][2][kBN];     // read as float4
 };
+static_assert(offsetof(WCtrl, bias) % 16 == 0, "bias is read with 16-byte vector loads");
 
 __device__ __forceinline__ void flag_error_w(WCtrl& ctl, unsigned* status) {
   atomicOr(status, kErrTimeout);
@@ -575,6 +579,16 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   }
 }
 
+// Waits on a barrier that never completes; the bounded wait gives up and reports.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, unsigned* __restrict__ status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_barrier_init();
+    if (!ptx::mbar_wait(&bar, 0, limit_ns)) atomicOr(status, kErrTimeout);
+  }
+}
+
 // ---- host helpers -------------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -633,6 +647,14 @@ int64_t choose_grid(int64_t row_tiles, int64_t NT, int sms, int max_splits) {
 }  // namespace tc
 
 using namespace tc;
+
+int tc_selftest_bounded_wait(unsigned* status, int64_t limit_ns, cudaStream_t st) {
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+    bounded_wait_selftest_kernel<<<1, 32, 0, st>>>((uint64_t)limit_ns, status);
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
 
 int tc_pack_inputs(bool bf16, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,
                    int64_t n_pad, int64_t m_pad, int64_t dpt, void* xq, void* yq, int sms,

@@ -12,7 +12,14 @@ import torch
 # (scaled by the largest magnitude of the oracle's output).
 POT_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
 LOSS_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
-OUT_TOL = {"fp32": 1e-4, "tf32": 1e-4, "bf16": 2e-3}
+# Transport application, Hadamard and gradient outputs (no bound is stated for them):
+# with operands rounded to the MMA type (unit roundoff u), every dot product carries an
+# error of RMS u sqrt(2/(3d)) |x||y|, i.e. a relative error of 2/eps times that in each
+# plan entry, plus u/sqrt(3) from rounding the weights for the second contraction; against
+# a random-sign V these do not average out. For the d = 1024, eps = 0.1 workload this
+# predicts a max error of ~4e-4 (tf32) and ~1.6e-3 (bf16) relative to max|P V|; the
+# bounds below are 2.5x that. The fp32 path keeps 1e-4.
+OUT_TOL = {"fp32": 1e-4, "tf32": 1e-3, "bf16": 4e-3}
 
 
 def to_dev(arr):
