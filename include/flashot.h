@@ -172,6 +172,32 @@ int flashot_ot_grad_x(const float *X, const float *Y, const float *a, const floa
                       const float *g, int64_t n, int64_t m, int64_t d, float eps, float *grad,
                       int flags, void *ws, size_t ws_bytes, flashot_stream_t stream);
 
+/* ---- allocation-free variant -------------------------------------------------------- */
+/*
+ * The paper has no counterpart to this entry point; it exists for callers that cannot give
+ * the library a workspace: a host framework that owns all device memory through its own
+ * fixed arena and forbids its plugins to call cudaMalloc, or a latency-critical loop where
+ * a cudaMalloc / cudaFree (which may synchronise the device) is not acceptable.
+ *
+ * flashot_sinkhorn_step_f_noalloc computes the same f = F(g) as flashot_sinkhorn_step_f
+ * (same arguments, minus ws / ws_bytes) and allocates nothing: its scratch is one array of
+ * FLASHOT_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library as device memory, which
+ * every GPU that loads the library keeps reserved until the process exits. X, Y, b, g and
+ * f are still the caller's device buffers.
+ *  - Sizes whose workspace (flashot_workspace_bytes(n, m, d, 0, flags)) exceeds 64 MiB are
+ *    rejected with FLASHOT_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *  - Only the precision bits of flags are used; the inputs are always re-packed, because
+ *    the array keeps whatever the previous call left in it.
+ *  - The first call on a device looks up the array's device address with that device
+ *    current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls on a device share the one array: calls whose GPU work may overlap (other
+ *    streams, other host threads) race on it and give undefined results. Serialise them.
+ */
+#define FLASHOT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int flashot_sinkhorn_step_f_noalloc(const float *X, const float *Y, const float *b,
+                                    const float *g, int64_t n, int64_t m, int64_t d, float eps,
+                                    int flags, float *f, flashot_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
