@@ -55,7 +55,7 @@ constexpr int64_t kMaxRows = int64_t(1) << 28;
 constexpr int64_t kMaxD = 4096;
 constexpr int64_t kMaxK = 4096;
 constexpr int kMaxSplits = 64;
-constexpr int kRowPad = 128;
+constexpr int kRowPad = 256;  // the tensor-core LSE pass tiles columns by 256
 
 inline int64_t round_up(int64_t x, int64_t q) { return (x + q - 1) / q * q; }
 inline int64_t ceil_div(int64_t x, int64_t q) { return (x + q - 1) / q; }

@@ -37,11 +37,12 @@ namespace flashot {
 namespace tc {
 
 constexpr int kBM = 128;                 // rows per tile (MMA M)
-constexpr int kBN = 128;                 // columns per tile (MMA N)
+constexpr int kBN = 128;                 // columns per tile of the weighted-sum pass (MMA N)
+constexpr int kLseBN = 256;              // columns per tile of the LSE pass (MMA N)
 constexpr int kChunk = 128 * 128;        // bytes of one 128-row x 128-byte K-chunk box
 constexpr int kThreads = 192;            // 6 warps
 constexpr int kMaxStages = 8;
-constexpr uint32_t kTmemCols = 256;      // two 128-column fp32 accumulators
+constexpr uint32_t kLseTmemCols = 512;   // two 256-column fp32 accumulators
 constexpr int kSmemLimit = 232448;       // 227 KB per block (opt-in maximum)
 
 struct __align__(128) Ctrl {
@@ -54,20 +55,56 @@ struct __align__(128) Ctrl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  alignas(16) float bias[4][2][kBN];     // per epilogue warp, double-buffered column bias (float4 access)
 };
-
-static_assert(offsetof(Ctrl, bias) % 16 == 0, "bias is read with 16-byte vector loads");
 
 __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
   atomicOr(status, kErrTimeout);
   ctl.abort_flag = 1;
 }
 
+// One 128-column half of an S tile row: scores s2 = kappa * dot + bias, then the online
+// base-2 (max, sum) update. Packed fp32x2 FMAs/adds and a 3-input max halve the FP32 issue
+// count; the 128 exponentials go to the SFU.
+__device__ __forceinline__ void lse_half(float (&v)[128], const float4* __restrict__ cb,
+                                         uint64_t kappa2, float& M, float& S) {
+  float mx = kNegBig;
+#pragma unroll
+  for (int j = 0; j < 128; j += 4) {
+    const float4 b4 = __ldg(cb + j / 4);
+    uint64_t p0 = ptx::fma2(ptx::pack2(v[j], v[j + 1]), kappa2, ptx::pack2(b4.x, b4.y));
+    uint64_t p1 = ptx::fma2(ptx::pack2(v[j + 2], v[j + 3]), kappa2, ptx::pack2(b4.z, b4.w));
+    ptx::unpack2(p0, v[j], v[j + 1]);
+    ptx::unpack2(p1, v[j + 2], v[j + 3]);
+    mx = ptx::max3(mx, v[j], v[j + 1]);
+    mx = ptx::max3(mx, v[j + 2], v[j + 3]);
+  }
+  if (mx > M) {
+    S *= ex2(M - mx);
+    M = mx;
+  }
+  const uint64_t negM = ptx::pack2(-M, -M);
+  uint64_t acc0 = 0, acc1 = 0;  // bit pattern 0 = (+0.0f, +0.0f)
+#pragma unroll
+  for (int j = 0; j < 128; j += 4) {
+    float e0, e1, e2, e3;
+    ptx::unpack2(ptx::add2(ptx::pack2(v[j], v[j + 1]), negM), e0, e1);
+    ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2], v[j + 3]), negM), e2, e3);
+    acc0 = ptx::add2(acc0, ptx::pack2(ex2(e0), ex2(e1)));
+    acc1 = ptx::add2(acc1, ptx::pack2(ex2(e2), ex2(e3)));
+  }
+  float a0, a1, a2, a3;
+  ptx::unpack2(acc0, a0, a1);
+  ptx::unpack2(acc1, a2, a3);
+  S += (a0 + a1) + (a2 + a3);
+}
+
 // ---------------------------------------------------------------------------------------
 // LSE pass: partial[slot * ld + row] = (max_j s2_ij, sum_j 2^(s2_ij - max)) over the
 // column tiles of this CTA's range, s2_ij = kappa <p_i, q_j> + colBias_j.
-// kARes: the row tile (all K-chunks) stays in shared memory for a whole segment.
+// Tiles are 128 rows x 256 columns (tcgen05.mma M = 128, N = 256).
+// kARes: the row tile (all K-chunks) stays in shared memory for a whole segment, and each
+// stage holds one 256-row x 128-byte K-chunk of the column cloud; otherwise each stage
+// holds a K-chunk of both.
 // ---------------------------------------------------------------------------------------
 template <bool kBF16, bool kARes>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -78,12 +115,14 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
   constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
+  constexpr uint32_t kBChunk = 2u * kChunk;  // 256 rows x 128 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = ptx::smem_u32(dyn_smem);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = dyn_smem + (base - raw);
   const uint32_t a_bytes = kARes ? (uint32_t)kc_count * kChunk : 0u;
-  const uint32_t stage_bytes = kARes ? (uint32_t)kChunk : 2u * kChunk;
+  const uint32_t stage_bytes = kARes ? kBChunk : kChunk + kBChunk;
+  const uint32_t b_off = kARes ? 0u : (uint32_t)kChunk;  // B chunk offset within a stage
   const int64_t G = gridDim.x, cta = blockIdx.x;
   const int64_t t_begin = sk_begin(cta, T, G), t_end = sk_begin(cta + 1, T, G);
 
@@ -107,7 +146,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     ptx::tma_prefetch_desc(&mapB);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl.tmem_base, kTmemCols);
+    ptx::tmem_alloc(&ctl.tmem_base, kLseTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -138,14 +177,10 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           for (int kc = 0; kc < kc_count; ++kc) {
             if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
             uint8_t* st = smem + a_bytes + (size_t)stage * stage_bytes;
-            if constexpr (kARes) {
-              ptx::mbar_arrive_expect_tx(&ctl.full[stage], kChunk);
-              ptx::tma_load_2d(&mapB, &ctl.full[stage], st, kc * kElems, jt * kBN);
-            } else {
-              ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * kChunk);
+            ptx::mbar_arrive_expect_tx(&ctl.full[stage], stage_bytes);
+            if constexpr (!kARes)
               ptx::tma_load_2d(&mapA, &ctl.full[stage], st, kc * kElems, (int)(rt * kBM));
-              ptx::tma_load_2d(&mapB, &ctl.full[stage], st + kChunk, kc * kElems, jt * kBN);
-            }
+            ptx::tma_load_2d(&mapB, &ctl.full[stage], st + b_off, kc * kElems, jt * kLseBN);
             ++issued;
             if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
           }
@@ -163,7 +198,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------- MMA issuer ----------------------------------------
-      constexpr uint32_t idesc = ptx::make_idesc<kBF16>(kBM, kBN);
+      constexpr uint32_t idesc = ptx::make_idesc<kBF16>(kBM, kLseBN);
       uint32_t stage = 0, ph = 0, a_ph = 0, ab = 0, acc_ph = 0;
       bool ok = true;
       for (int64_t t = t_begin; ok && t < t_end;) {
@@ -177,17 +212,17 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         for (int64_t tt = t; ok && tt < seg_end; ++tt) {
           if (!ptx::mbar_wait(&ctl.acc_empty[ab], acc_ph ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t d_tmem = tmem + ab * kBN;
+          const uint32_t d_tmem = tmem + ab * kLseBN;
           for (int kc = 0; kc < kc_count; ++kc) {
             if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t st = base + a_bytes + stage * stage_bytes;
             const uint32_t a_addr = kARes ? base + (uint32_t)kc * kChunk : st;
-            const uint32_t b_addr = kARes ? st : st + kChunk;
+            const uint64_t a_desc = ptx::sdesc_k128(a_addr);
+            const uint64_t b_desc = ptx::sdesc_k128(st + b_off);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::umma<kBF16>(d_tmem, ptx::sdesc_k128(a_addr + kk * 32),
-                               ptx::sdesc_k128(b_addr + kk * 32), idesc,
+            for (int kk = 0; kk < 4; ++kk)  // K advance: 32 bytes = 2 in the address field
+              ptx::umma<kBF16>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
                                (kc | kk) != 0 ? 1u : 0u);
             ptx::umma_commit(&ctl.empty[stage]);
             if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
@@ -207,54 +242,31 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   } else {
     // --------------------------------- epilogue ------------------------------------------
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int ew = warp - 2;           // private bias buffer
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t ab = 0, acc_ph = 0, bb = 0;
+    const uint64_t kappa2 = ptx::pack2(kappa, kappa);
+    uint32_t ab = 0, acc_ph = 0;
     bool ok = true;
-    float4 bnext = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t_begin < t_end)
-      bnext = __ldg(reinterpret_cast<const float4*>(colBias + (t_begin % NT) * kBN) + lane);
+    if (t_begin < t_end && lane < 8)   // 1 KB of bias per tile: one 128-byte line per lane
+      ptx::prefetch_l1(colBias + (t_begin % NT) * kLseBN + lane * 32);
     for (int64_t t = t_begin; ok && t < t_end;) {
       const int64_t rt = t / NT;
       const int64_t seg_end = min(t_end, (rt + 1) * NT);
       float M = kNegBig, S = 0.0f;
       for (int64_t tt = t; tt < seg_end; ++tt) {
-        reinterpret_cast<float4*>(ctl.bias[ew][bb])[lane] = bnext;
-        if (tt + 1 < t_end)
-          bnext = __ldg(reinterpret_cast<const float4*>(colBias + ((tt + 1) % NT) * kBN) + lane);
-        __syncwarp();
+        const float4* cb = reinterpret_cast<const float4*>(colBias + (tt % NT) * kLseBN);
+        if (tt + 1 < t_end && lane < 8)
+          ptx::prefetch_l1(colBias + ((tt + 1) % NT) * kLseBN + lane * 32);
         if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
         ptx::tc_fence_after();
-        float v[kBN];
-        ptx::tmem_ld_x128_sync(tmem + lane_base + ab * kBN, v);
+        const uint32_t taddr = tmem + lane_base + ab * kLseBN;
+        float v[128];
+        ptx::tmem_ld_x128_sync(taddr, v);
+        lse_half(v, cb, kappa2, M, S);
+        ptx::tmem_ld_x128_sync(taddr + 128, v);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.acc_empty[ab]);
+        ptx::mbar_arrive(&ctl.acc_empty[ab]);   // both halves are in registers now
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        const float4* cb = reinterpret_cast<const float4*>(ctl.bias[ew][bb]);
-        float mx = kNegBig;
-#pragma unroll
-        for (int j = 0; j < kBN; j += 4) {
-          const float4 b4 = cb[j / 4];
-          v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
-          v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
-          v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
-          v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
-          mx = fmaxf(mx, fmaxf(fmaxf(v[j], v[j + 1]), fmaxf(v[j + 2], v[j + 3])));
-        }
-        if (mx > M) {
-          S *= ex2(M - mx);
-          M = mx;
-        }
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < kBN; j += 4) {
-          s0 += ex2(v[j + 0] - M);
-          s1 += ex2(v[j + 1] - M);
-          s2 += ex2(v[j + 2] - M);
-          s3 += ex2(v[j + 3] - M);
-        }
-        S += (s0 + s1) + (s2 + s3);
-        bb ^= 1u;
+        lse_half(v, cb + 32, kappa2, M, S);
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
@@ -269,7 +281,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, kLseTmemCols);
   }
 }
 
@@ -621,6 +633,25 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool 
   return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
 }
 
+// 2-D map over a packed operand (rows x cols elements), box = box_rows x 128 B, 128-byte
+// swizzle: the column cloud of the LSE pass (256-row boxes) and the transposed right operand
+// of the weighted sums.
+int make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16,
+                  int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return FLASHOT_ERR_CUDA;
+  const int es = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
+}
+
 template <typename K>
 int set_smem(K kernel, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -682,7 +713,7 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
                       float2* partial, int64_t ld, unsigned* status, cudaStream_t st) {
   const int ctrl = (int)sizeof(Ctrl);
   const int a_bytes = kARes ? kc * kChunk : 0;
-  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
+  const int stage_bytes = kARes ? 2 * kChunk : 3 * kChunk;
   const int budget = kSmemLimit - ctrl - 1024 - a_bytes;
   const int stages = std::min(kMaxStages, budget / stage_bytes);
   if (stages < 2) return FLASHOT_ERR_INVALID_ARG;
@@ -704,12 +735,13 @@ int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colB
                 cudaStream_t st) {
   const int es = bf16 ? 2 : 4;
   const int kc = (int)(dpt * es / 128);
-  const int64_t row_tiles = rows_pad / kBM, NT = cols_pad / kBN;
+  if (rows_pad % kBM != 0 || cols_pad % kLseBN != 0) return FLASHOT_ERR_INVALID_ARG;
+  const int64_t row_tiles = rows_pad / kBM, NT = cols_pad / kLseBN;
   const int64_t T = row_tiles * NT;
   const int64_t G = choose_grid(row_tiles, NT, sms, max_splits);
   CUtensorMap mA, mB;
   int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
-  if (rc == FLASHOT_OK) rc = make_map(&mB, colQ, cols_pad, dpt, bf16);
+  if (rc == FLASHOT_OK) rc = make_map_rows(&mB, colQ, cols_pad, dpt, bf16, kLseBN);
   if (rc != FLASHOT_OK) return rc;
   info->n_splits = 0;
   info->sk_T = T;
@@ -757,23 +789,6 @@ static int launch_wsum(const CUtensorMap& mA, const CUtensorMap& mB, const CUten
                                       out, ldo, status);
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
-}
-
-// 2-D map over the transposed right operand (out_rows x cols_pad), box = box_rows x 128 B.
-int make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16,
-                  int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return FLASHOT_ERR_CUDA;
-  const int es = bf16 ? 2 : 4;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
 }
 
 int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const float* colBias,
