@@ -45,10 +45,11 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t v, int64_t T, int64
 }
 
 // How the partials of one LSE pass are laid out: either n_splits fixed splits per row, or
-// (n_splits == 0) stream-K over T = row_tiles * NT tiles of 128 x 128 with G CTAs, where
-// the row tile rt has partial slots 0 .. owner((rt+1)NT-1) - owner(rt NT).
+// (n_splits == 0) stream-K over T = row_tiles * NT tiles (128-row tiles) with G CTAs, where
+// the row tile rt has slots_per_owner * (owner((rt+1)NT-1) - owner(rt NT) + 1) slots.
 struct SplitInfo {
   int n_splits;
+  int slots_per_owner;  // stream-K: partial slots each owning CTA writes per row tile
   int64_t sk_T, sk_G, sk_NT;
 };
 

@@ -40,7 +40,9 @@ constexpr int kBM = 128;                 // rows per tile (MMA M)
 constexpr int kBN = 128;                 // columns per tile of the weighted-sum pass (MMA N)
 constexpr int kLseBN = 256;              // columns per tile of the LSE pass (MMA N)
 constexpr int kChunk = 128 * 128;        // bytes of one 128-row x 128-byte K-chunk box
-constexpr int kThreads = 192;            // 6 warps
+constexpr int kThreads = 192;            // weighted-sum pass: 6 warps
+constexpr int kLseThreads = 320;         // LSE pass: TMA warp, MMA warp, 8 epilogue warps
+constexpr int kLseEpiThreads = 256;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kLseTmemCols = 512;   // two 256-column fp32 accumulators
 constexpr int kSmemLimit = 232448;       // 227 KB per block (opt-in maximum)
@@ -62,40 +64,42 @@ __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
   ctl.abort_flag = 1;
 }
 
-// One 128-column half of an S tile row: scores s2 = kappa * dot + bias, then the online
-// base-2 (max, sum) update. Packed fp32x2 FMAs/adds and a 3-input max halve the FP32 issue
-// count; the 128 exponentials go to the SFU.
-__device__ __forceinline__ void lse_half(float (&v)[128], const float4* __restrict__ cb,
-                                         uint64_t kappa2, float& M, float& S) {
-  float mx = kNegBig;
+// 64 columns of one S-tile row: scores s2 = kappa * dot + bias, then the online base-2
+// (max, sum) update (rescaled only when the chunk raises the running max). One FFMA, half a
+// 3-input max, one FADD, one SFU ex2 and one FADD per score.
+__device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __restrict__ cb,
+                                            float kappa, float& M, float& S) {
+  // Four independent running maxima / eight sums keep the dependency chains short.
+  float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
 #pragma unroll
-  for (int j = 0; j < 128; j += 4) {
+  for (int j = 0; j < 64; j += 8) {
     const float4 b4 = __ldg(cb + j / 4);
-    uint64_t p0 = ptx::fma2(ptx::pack2(v[j], v[j + 1]), kappa2, ptx::pack2(b4.x, b4.y));
-    uint64_t p1 = ptx::fma2(ptx::pack2(v[j + 2], v[j + 3]), kappa2, ptx::pack2(b4.z, b4.w));
-    ptx::unpack2(p0, v[j], v[j + 1]);
-    ptx::unpack2(p1, v[j + 2], v[j + 3]);
-    mx = ptx::max3(mx, v[j], v[j + 1]);
-    mx = ptx::max3(mx, v[j + 2], v[j + 3]);
+    const float4 b5 = __ldg(cb + j / 4 + 1);
+    v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
+    v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
+    v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
+    v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
+    v[j + 4] = fmaf(kappa, v[j + 4], b5.x);
+    v[j + 5] = fmaf(kappa, v[j + 5], b5.y);
+    v[j + 6] = fmaf(kappa, v[j + 6], b5.z);
+    v[j + 7] = fmaf(kappa, v[j + 7], b5.w);
+    m0 = ptx::max3(m0, v[j + 0], v[j + 1]);
+    m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
+    m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
+    m3 = ptx::max3(m3, v[j + 6], v[j + 7]);
   }
+  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
   if (mx > M) {
     S *= ex2(M - mx);
     M = mx;
   }
-  const uint64_t negM = ptx::pack2(-M, -M);
-  uint64_t acc0 = 0, acc1 = 0;  // bit pattern 0 = (+0.0f, +0.0f)
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < 128; j += 4) {
-    float e0, e1, e2, e3;
-    ptx::unpack2(ptx::add2(ptx::pack2(v[j], v[j + 1]), negM), e0, e1);
-    ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2], v[j + 3]), negM), e2, e3);
-    acc0 = ptx::add2(acc0, ptx::pack2(ex2(e0), ex2(e1)));
-    acc1 = ptx::add2(acc1, ptx::pack2(ex2(e2), ex2(e3)));
+  for (int j = 0; j < 64; j += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s[u] += ex2(v[j + u] - M);
   }
-  float a0, a1, a2, a3;
-  ptx::unpack2(acc0, a0, a1);
-  ptx::unpack2(acc1, a2, a3);
-  S += (a0 + a1) + (a2 + a3);
+  S += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -107,7 +111,7 @@ __device__ __forceinline__ void lse_half(float (&v)[128], const float4* __restri
 // holds a K-chunk of both.
 // ---------------------------------------------------------------------------------------
 template <bool kBF16, bool kARes>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kLseThreads, 1)
 lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
               int kc_count, int stages, float kappa, float2* __restrict__ partial, int64_t ld,
@@ -133,7 +137,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.acc_full[b], 1);
-      ptx::mbar_init(&ctl.acc_empty[b], 128);
+      ptx::mbar_init(&ctl.acc_empty[b], kLseEpiThreads);
     }
     ptx::mbar_init(&ctl.a_full, 1);
     ptx::mbar_init(&ctl.a_empty, 1);
@@ -241,36 +245,40 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
   } else {
     // --------------------------------- epilogue ------------------------------------------
-    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    // Warps 2..9: warp w reads TMEM lane quarter (w % 4) (rows 32q .. 32q+31) and column
+    // half h = (w - 2) / 4 of every 256-column tile; each (row, half) keeps its own online
+    // (max, sum) and becomes its own partial slot, merged later by the combine kernel.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const uint64_t kappa2 = ptx::pack2(kappa, kappa);
     uint32_t ab = 0, acc_ph = 0;
     bool ok = true;
-    if (t_begin < t_end && lane < 8)   // 1 KB of bias per tile: one 128-byte line per lane
-      ptx::prefetch_l1(colBias + (t_begin % NT) * kLseBN + lane * 32);
+    if (t_begin < t_end && lane < 4)   // 512 B of bias per half-tile: one line per lane
+      ptx::prefetch_l1(colBias + (t_begin % NT) * kLseBN + h * 128 + lane * 32);
     for (int64_t t = t_begin; ok && t < t_end;) {
       const int64_t rt = t / NT;
       const int64_t seg_end = min(t_end, (rt + 1) * NT);
       float M = kNegBig, S = 0.0f;
       for (int64_t tt = t; tt < seg_end; ++tt) {
-        const float4* cb = reinterpret_cast<const float4*>(colBias + (tt % NT) * kLseBN);
-        if (tt + 1 < t_end && lane < 8)
-          ptx::prefetch_l1(colBias + ((tt + 1) % NT) * kLseBN + lane * 32);
+        const float4* cb =
+            reinterpret_cast<const float4*>(colBias + (tt % NT) * kLseBN + h * 128);
+        if (tt + 1 < t_end && lane < 4)
+          ptx::prefetch_l1(colBias + ((tt + 1) % NT) * kLseBN + h * 128 + lane * 32);
         if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + ab * kLseBN;
-        float v[128];
-        ptx::tmem_ld_x128_sync(taddr, v);
-        lse_half(v, cb, kappa2, M, S);
-        ptx::tmem_ld_x128_sync(taddr + 128, v);
+        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
+        float v[64];
+        ptx::tmem_ld_x64_sync(taddr, v);
+        lse_chunk64(v, cb, kappa, M, S);
+        ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.acc_empty[ab]);   // both halves are in registers now
+        ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_half(v, cb + 32, kappa2, M, S);
+        lse_chunk64(v, cb + 16, kappa, M, S);
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
-      const int64_t slot = cta - sk_owner(rt * NT, T, G);
+      const int64_t slot = 2 * (cta - sk_owner(rt * NT, T, G)) + h;
       if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
       t = seg_end;
     }
@@ -723,8 +731,8 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
   if (rc != FLASHOT_OK) return rc;
   {
     TraceScope ts_(FLASHOT_KERNEL_LSE, st);
-    kern<<<(unsigned)G, kThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages, kappa,
-                                             partial, ld, status);
+    kern<<<(unsigned)G, kLseThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages,
+                                                kappa, partial, ld, status);
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
@@ -738,12 +746,14 @@ int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colB
   if (rows_pad % kBM != 0 || cols_pad % kLseBN != 0) return FLASHOT_ERR_INVALID_ARG;
   const int64_t row_tiles = rows_pad / kBM, NT = cols_pad / kLseBN;
   const int64_t T = row_tiles * NT;
-  const int64_t G = choose_grid(row_tiles, NT, sms, max_splits);
+  // Two partial slots (column halves) per CTA and row tile.
+  const int64_t G = choose_grid(row_tiles, NT, sms, max_splits / 2);
   CUtensorMap mA, mB;
   int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
   if (rc == FLASHOT_OK) rc = make_map_rows(&mB, colQ, cols_pad, dpt, bf16, kLseBN);
   if (rc != FLASHOT_OK) return rc;
   info->n_splits = 0;
+  info->slots_per_owner = 2;
   info->sk_T = T;
   info->sk_G = G;
   info->sk_NT = NT;
