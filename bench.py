@@ -48,13 +48,17 @@ def parse_args():
     p.add_argument("--steps", type=int, default=5)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["flashot", "reference"], default="flashot")
-    p.add_argument("--precision", choices=["bf16", "tf32"], default="bf16")
+    p.add_argument("--precision", choices=["bf16", "tf32", "tf32x3", "fp32"], default=None,
+                   help="contraction precision (default: bf16; fp32 for the d < 32 workloads)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-passes", type=int, default=0, metavar="P",
                    help="profiling driver: pack once, run P f-updates and P g-updates of the "
                         "workload (no timing, no JSON line) and exit; for ncu captures")
     p.add_argument("--n", type=int, default=None, help="override n = m (profiling driver)")
+    p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
+                   help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
+                        "lines for the other point-cloud workloads")
     args = p.parse_args()
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -234,6 +238,112 @@ def profiled_traffic(prec):
     if not ent or ent.get("source_hash") != kernel_source_hash():
         return None
     return ent.get("dram_bytes_per_full_launch")
+
+
+# Peak fp32 FMA throughput used for the CUDA-core path: 152 SMs x 128 FP32 lanes x 2 flops
+# per FMA x the maximum SM clock. The SFU peak for ex2 is taken as 32 per clock per SM.
+FP32_LANES_PER_SM = 128
+SFU_EX2_PER_SM_CLK = 32
+N_SMS = 152
+
+
+def run_other_workload(args):
+    """Supplementary measurement of workloads 1, 2, 4 (solves) and 5 (transport application
+    at converged potentials): one JSON line each, in that workload's own unit."""
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    from workloads import workload
+    idx = args.workload
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pr = workload(idx)
+    prec = args.precision or ("fp32" if pr.d < 32 else "bf16")
+    n, m, d = pr.n, pr.m, pr.d
+    X = torch.from_numpy(pr.X).to(dev)
+    Y = torch.from_numpy(pr.Y).to(dev)
+    a = None if pr.uniform_weights else torch.from_numpy(pr.a).to(dev)
+    b = None if pr.uniform_weights else torch.from_numpy(pr.b).to(dev)
+    sched = [float(e) for e in pr.eps_schedule]
+    k = pr.V.shape[1] if pr.V is not None else 0
+    ws = lds.Workspace(lds.workspace_bytes(n, m, d, k, prec))
+    f = torch.empty(n, device=dev)
+    g = torch.empty(m, device=dev)
+    loss = torch.empty((), dtype=torch.float64, device=dev)
+    nm = float(n) * float(m)
+    if idx == 5:
+        lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
+                           g_out=g, loss_out=loss, workspace=ws)
+        V = torch.from_numpy(pr.V).to(dev)
+        U = torch.from_numpy(pr.U).to(dev)
+        PV = torch.empty((n, k), device=dev)
+        PtU = torch.empty((m, k), device=dev)
+        h = torch.empty(n, device=dev)
+        eps = sched[0]
+
+        def step():
+            lds.transport_apply(X, Y, f, g, eps, V, a, b, precision=prec, out=PV, workspace=ws,
+                                reuse_pack=True)
+            lds.transport_apply(X, Y, f, g, eps, U, a, b, transpose=True, precision=prec,
+                                out=PtU, workspace=ws, reuse_pack=True)
+            lds.transport_hadamard_xy(X, Y, f, g, eps, a, b, precision=prec, out=h,
+                                      workspace=ws, reuse_pack=True)
+        units_per_step, unit, scores_per_step = 3, "transport applications/s", 3 * nm
+        hot = lds.KernelTimer.WSUM
+    else:
+        def step():
+            lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
+                               g_out=g, loss_out=loss, workspace=ws)
+        units_per_step, unit = pr.total_iters, "iters/s"
+        scores_per_step = 2 * nm * pr.total_iters
+        hot = lds.KernelTimer.LSE
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    timer = lds.KernelTimer(cap=args.steps * 2200).start()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    launches0 = lds.launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    launches = lds.launch_count() - launches0
+    n_hot, ms_hot = timer.read(hot)
+    timer.stop()
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("device timeout reported")
+    peaks, _ = load_peaks()
+    clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    avg = ms_hot / max(n_hot, 1) / 1e3
+    per_launch_scores = nm
+    if prec == "fp32":
+        roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
+                "peak": N_SMS * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)"}
+    else:
+        bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        # Algorithmic flops (2d per score); split tf32 runs three tf32 contractions, so its
+        # ceiling for the algorithmic rate is a third of the tf32 peak.
+        tf32 = bf16_sus * TF32_OVER_BF16
+        roof = {"bound": "tensor", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
+                "peak": bf16_sus if prec == "bf16" else (tf32 / 3 if prec == "tf32x3" else tf32),
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["sfu_frac"] = (per_launch_scores / avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk)
+    roof["avg_launch_ms"] = avg * 1e3
+    roof["launches_timed"] = n_hot
+    line = {"metric": f"workload {idx} ({pr.name}) throughput", "supplementary": True,
+            "value": units_per_step * args.steps / (ms / 1e3), "unit": unit,
+            "score_evals_per_s": scores_per_step * args.steps / (ms / 1e3),
+            "ms_per_step": ms / args.steps, "steps": args.steps, "warmup": args.warmup,
+            "dtype": prec, "config": {"workload": pr.name, "n": n, "m": m, "d": d,
+                                      "eps": sched if len(sched) > 1 else sched[0],
+                                      "iters_per_stage": pr.iters_per_stage},
+            "roofline": roof, "gpu_launches": int(launches)}
+    print(json.dumps(line), flush=True)
 
 
 def run_gpu(args):
@@ -447,11 +557,16 @@ def run_profile_driver(args):
 def main():
     args = parse_args()
     if args.profile_passes > 0:
+        args.precision = args.precision or "bf16"
         run_profile_driver(args)
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != WORKLOAD_IDX:
+        run_other_workload(args)
     else:
+        if args.precision is None:
+            args.precision = "bf16"
         run_gpu(args)
 
 

@@ -62,6 +62,11 @@ typedef struct CUstream_st *flashot_stream_t;
 #define FLASHOT_PREC_FP32   0x1  /* fp32 FMA on CUDA cores (any d)                         */
 #define FLASHOT_PREC_TF32   0x2  /* tcgen05 kind::tf32, inputs rounded to tf32 (nearest)   */
 #define FLASHOT_PREC_BF16   0x3  /* tcgen05 kind::f16 with bf16 operands (nearest)         */
+/* tcgen05 kind::tf32 on split operands: x = hi + lo (hi = tf32(x), lo = tf32(x - hi)), packed
+ * along K as X = [hi | hi | lo], Y = [hi | lo | hi], so one contraction over 3x the K
+ * returns hi.hi + hi.lo + lo.hi (about fp32 accuracy for the scores; 3x the MMA work). The
+ * second contraction of transport application / gradient stays single tf32. */
+#define FLASHOT_PREC_TF32X3 0x4
 #define FLASHOT_PREC_MASK   0xF
 /* solve: start from the g passed in (warm start / resume) instead of g = 0. */
 #define FLASHOT_WARM_START  0x10

@@ -31,6 +31,7 @@ PREC_AUTO = 0x0
 PREC_FP32 = 0x1
 PREC_TF32 = 0x2
 PREC_BF16 = 0x3
+PREC_TF32X3 = 0x4
 WARM_START = 0x10
 REUSE_PACK = 0x20
 
@@ -38,7 +39,8 @@ KERNEL_LSE = 0
 KERNEL_WSUM = 1
 KERNEL_OTHER = 2
 
-PRECISIONS = {"auto": PREC_AUTO, "fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16}
+PRECISIONS = {"auto": PREC_AUTO, "fp32": PREC_FP32, "tf32": PREC_TF32, "bf16": PREC_BF16,
+              "tf32x3": PREC_TF32X3}
 
 # Exported symbol -> (restype, argtypes). The header declares exactly these.
 SIGNATURES = {

@@ -129,7 +129,9 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
       k > kMaxK)
     return false;
   const int p = resolve_prec(flags, d);
-  if (p != FLASHOT_PREC_FP32 && p != FLASHOT_PREC_TF32 && p != FLASHOT_PREC_BF16) return false;
+  if (p != FLASHOT_PREC_FP32 && p != FLASHOT_PREC_TF32 && p != FLASHOT_PREC_BF16 &&
+      p != FLASHOT_PREC_TF32X3)
+    return false;
   g->n = n;
   g->m = m;
   g->d = d;
@@ -141,6 +143,7 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
   g->dpf = g->small ? round_up(d, 4) : round_up(d, 32);
   g->es = (p == FLASHOT_PREC_BF16) ? 2 : 4;
   g->dpt = round_up(d, 128 / g->es);  // one 128-byte swizzle row per k-chunk
+  if (p == FLASHOT_PREC_TF32X3) g->dpt *= 3;  // [hi | hi | lo] against [hi | lo | hi]
   return true;
 }
 
@@ -254,8 +257,9 @@ int pack_inputs(const Ctx& c, const float* X, const float* Y, const float* a, co
       pack_rows_kernel<PackKind::F32><<<pg, T, 0, c.st>>>(Y, c.at<void>(c.L.yp), g.m, g.d, g.m_pad, g.dpf);
     }
   } else {
-    int rc = tc_pack_inputs(c.g.prec == FLASHOT_PREC_BF16, X, Y, g.n, g.m, g.d, g.n_pad, g.m_pad,
-                            g.dpt, c.at<void>(c.L.xq), c.at<void>(c.L.yq), c.sms, c.st);
+    const int mode = g.prec == FLASHOT_PREC_BF16 ? 1 : (g.prec == FLASHOT_PREC_TF32X3 ? 2 : 0);
+    int rc = tc_pack_inputs(mode, X, Y, g.n, g.m, g.d, g.n_pad, g.m_pad, g.dpt,
+                            c.at<void>(c.L.xq), c.at<void>(c.L.yq), c.sms, c.st);
     if (rc != FLASHOT_OK) return rc;
   }
   return launch_check();

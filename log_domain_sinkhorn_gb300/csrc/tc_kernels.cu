@@ -695,13 +695,22 @@ int tc_selftest_bounded_wait(unsigned* status, int64_t limit_ns, cudaStream_t st
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
 
-int tc_pack_inputs(bool bf16, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,
+int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,
                    int64_t n_pad, int64_t m_pad, int64_t dpt, void* xq, void* yq, int sms,
                    cudaStream_t st) {
   const int T = 256;
   const unsigned g1 = (unsigned)std::min<int64_t>((n_pad * dpt + T - 1) / T, (int64_t)sms * 16);
   const unsigned g2 = (unsigned)std::min<int64_t>((m_pad * dpt + T - 1) / T, (int64_t)sms * 16);
-  if (bf16) {
+  const bool bf16 = (mode == 1);
+  if (mode == 2) {
+    const int64_t seg = dpt / 3;
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_tf32x3_kernel<<<g1, T, 0, st>>>(X, static_cast<uint32_t*>(xq), n, d, n_pad, seg,
+                                                0b100); }
+    { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+      pack_rows_tf32x3_kernel<<<g2, T, 0, st>>>(Y, static_cast<uint32_t*>(yq), m, d, m_pad, seg,
+                                                0b010); }
+  } else if (bf16) {
     { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
       pack_rows_kernel<PackKind::BF16><<<g1, T, 0, st>>>(X, xq, n, d, n_pad, dpt); }
     { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);

@@ -16,7 +16,7 @@ from workloads import make_problem, scaled_workload, workload
 
 pytestmark = pytest.mark.gpu
 
-TC_PRECS = ["tf32", "bf16"]
+TC_PRECS = ["tf32", "bf16", "tf32x3"]
 
 
 @pytest.mark.parametrize("precision", TC_PRECS)
@@ -62,7 +62,7 @@ def test_half_steps_random(cuda_lib, precision, n, m, d):
     assert np.all(np.abs(f_gpu - f_ref) <= half_step_bound(precision, pr.X, pr.Y, eps, f_ref))
     assert np.all(np.abs(g_gpu - g_ref) <= half_step_bound(precision, pr.Y, pr.X, eps, g_ref))
     # ... and, once each soft-min averages over enough terms, within the stated tolerance.
-    if min(n, m) >= 256:
+    if min(n, m) >= 256 or precision == "tf32x3":
         assert scaled_linf(f_gpu, f_ref) <= POT_TOL[precision]
         assert scaled_linf(g_gpu, g_ref) <= POT_TOL[precision]
 
@@ -165,7 +165,7 @@ def test_apply_exact_operands_within_rounding_bound(cuda_lib, precision, n, m, d
     """With exact scores, P V differs from the oracle only by the rounding of the weights
     and of V to the MMA operand type: |err| <= 2u (P |V|) + fp32 epilogue. A data-layout
     mistake in the second contraction would be O(P |V|)."""
-    from gpu_helpers import OPERAND_U
+    from gpu_helpers import SECOND_U
     lds = cuda_lib
     X, Y, V, U, a, b, f, g, eps = _exact_problem(n, m, d, k, seed=n + d + k)
     args = (to_dev(X), to_dev(Y), to_dev(f), to_dev(g), eps)
@@ -173,7 +173,7 @@ def test_apply_exact_operands_within_rounding_bound(cuda_lib, precision, n, m, d
                              precision=precision).cpu().numpy()
     PtU = lds.transport_apply(*args, to_dev(U), to_dev(a), to_dev(b), transpose=True,
                               precision=precision).cpu().numpy()
-    u = OPERAND_U[precision]
+    u = SECOND_U[precision]
     for got, W, tr in ((PV, V, False), (PtU, U, True)):
         ref = oracle.transport_apply(X, Y, a, b, f, g, eps, W, transpose=tr)
         mag = oracle.transport_apply(X, Y, a, b, f, g, eps, np.abs(W), transpose=tr)
@@ -187,7 +187,7 @@ def test_apply_exact_operands_within_rounding_bound(cuda_lib, precision, n, m, d
 def test_grad_exact_operands_within_rounding_bound(cuda_lib, precision, n, m, d):
     """grad_i = 2 a_i (x_i - sum_j w_ij y_j / sum_j w_ij): with exact points only the
     weights are rounded, so |err_io| <= 2 a_i 2u (P~ |Y|)_io / a_i = 4u (P~ |Y|)_io."""
-    from gpu_helpers import OPERAND_U
+    from gpu_helpers import SECOND_U
     lds = cuda_lib
     X, Y, _, _, a, b, _, g, eps = _exact_problem(n, m, d, 1, seed=7 * n + d)
     grad = lds.ot_grad_x(to_dev(X), to_dev(Y), to_dev(g), eps, to_dev(a), to_dev(b),
@@ -195,7 +195,7 @@ def test_grad_exact_operands_within_rounding_bound(cuda_lib, precision, n, m, d)
     ref = oracle.grad_x(X, Y, a, b, g, eps)
     ft = oracle.half_step_f(X, Y, b, g, eps)
     mag = oracle.transport_apply(X, Y, a, b, ft, g, eps, np.abs(Y))
-    bound = 4 * OPERAND_U[precision] * mag + 8e-6 * (mag + np.abs(a)[:, None] * np.abs(X)) \
+    bound = 4 * SECOND_U[precision] * mag + 8e-6 * (mag + np.abs(a)[:, None] * np.abs(X)) \
         + 1e-7 * np.abs(ref).max()
     assert np.all(np.abs(grad - ref) <= bound), np.abs(grad - ref).max()
 
@@ -237,3 +237,36 @@ def test_apply_grad_hadamard_workload5_scaled(cuda_lib, precision):
                                                    transpose=True)) <= tol
     assert scaled_linf(h, oracle.hadamard_xy(pr.X, pr.Y, pr.a, pr.b, f32, g32, eps)) <= tol
     assert scaled_linf(grad, oracle.grad_x(pr.X, pr.Y, pr.a, pr.b, g32, eps)) <= tol
+
+
+def test_split_tf32_anneal_rect_d16_scaled(cuda_lib):
+    """The split-tf32 mode on the low-eps rectangular d = 16 workload (Dirichlet weights,
+    eps 1.0 -> 0.01 over 10 stages; scaled to n = 600, m = 2400, 20 iterations per stage),
+    where plain tf32 scores are too coarse: potentials and loss at the fp32 tolerance."""
+    pr = scaled_workload(4, n=600, m=2400, iters=20)
+    X, Y, a, b = problem_tensors(pr)
+    f, g, loss = cuda_lib.sinkhorn_solve(X, Y, a, b, list(pr.eps_schedule), pr.iters_per_stage,
+                                         precision="tf32x3")
+    f_ref, g_ref, loss_ref = oracle.solve(pr.X, pr.Y, pr.a, pr.b, pr.eps_schedule,
+                                          pr.iters_per_stage)
+    assert pot_err(f.cpu().numpy(), g.cpu().numpy(), f_ref, g_ref) <= POT_TOL["tf32x3"]
+    assert rel_err(float(loss.cpu()), loss_ref) <= LOSS_TOL["tf32x3"]
+
+
+def test_split_tf32_full_rect_d16_anneal_sampled(cuda_lib):
+    """Full-size rectangular workload (20k x 80k, d = 16, 10 stages x 50 iterations) with
+    split tf32: one-step parity on sampled rows / columns at the final potentials."""
+    lds = cuda_lib
+    pr = workload(4)
+    X, Y, a, b = problem_tensors(pr)
+    f, g, loss = lds.sinkhorn_solve(X, Y, a, b, list(pr.eps_schedule), pr.iters_per_stage,
+                                    precision="tf32x3")
+    eps = float(pr.eps_schedule[-1])
+    f2 = lds.sinkhorn_step_f(X, Y, g, eps, b, precision="tf32x3").cpu().numpy()
+    f_np, g_np = f.cpu().numpy(), g.cpu().numpy()
+    rows, cols = _sample(pr.n, 21), _sample(pr.m, 22)
+    f_ref = oracle.half_step_f(pr.X, pr.Y, pr.b, g_np, eps, rows=rows)
+    g_ref = oracle.half_step_g(pr.X, pr.Y, pr.a, f_np, eps, rows=cols)
+    scale = max(np.abs(f_ref).max(), np.abs(g_ref).max())
+    assert np.abs(f2[rows] - f_ref).max() / scale <= POT_TOL["tf32x3"]
+    assert np.abs(g_np[cols] - g_ref).max() / scale <= POT_TOL["tf32x3"]
