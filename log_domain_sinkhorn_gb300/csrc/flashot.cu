@@ -148,7 +148,7 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
 }
 
 struct Layout {
-  size_t status, xp, yp, xq, yq, vtq, alpha, beta, wa, wb, la2, lb2, biasF, biasG, ftilde,
+  size_t status, xp, yp, xq, yq, vtq, wsp, alpha, beta, wa, wb, la2, lb2, biasF, biasG, ftilde,
       lse2, partial, loss, total;
 };
 
@@ -187,6 +187,9 @@ Layout make_layout(const Geometry& g) {
   if (g.prec != FLASHOT_PREC_FP32)
     L.vtq = take((size_t)std::max(round_up(g.k, 256), round_up(g.d, 256)) * std::max(np, mp) *
                  g.es);
+  // Partial sums of the bf16 weighted-sum pass (stream-K over 128 x 256 tiles).
+  if (g.prec == FLASHOT_PREC_BF16)
+    L.wsp = take(tc_wsum2_scratch_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)));
   L.total = off + 256;
   return L;
 }
@@ -372,6 +375,12 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
       ldv = g.d;
       k = g.d;
     }
+    if (g.prec == FLASHOT_PREC_BF16)
+      return tc_wsum2_pass(mode, c.at<void>(x_rows ? c.L.xq : c.L.yq),
+                           c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows, n_cols,
+                           x_rows ? g.n_pad : g.m_pad, cols_pad, g.d, g.dpt, kappa, V, ldv, k,
+                           c.at<void>(c.L.vtq), c.at<void>(c.L.wsp), rowW, X, out, ldo, c.sms,
+                           c.at<unsigned>(c.L.status), c.st);
     return tc_wsum_pass(g.prec == FLASHOT_PREC_BF16, mode, c.at<void>(x_rows ? c.L.xq : c.L.yq),
                         c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows, n_cols,
                         x_rows ? g.n_pad : g.m_pad, cols_pad, g.d, g.dpt, kappa, V, ldv, k,

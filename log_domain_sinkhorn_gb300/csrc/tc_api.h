@@ -38,4 +38,14 @@ int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const 
                  int64_t ldv, int64_t k, void* vtq, const float* rowW, const float* X,
                  float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st);
 
+// bf16 weighted-sum pass on 128 x 256 tiles with stream-K partials (tc_wsum2.cu). scratch
+// holds tc_wsum2_scratch_bytes(rows_pad, max(k, d)) bytes for the partial sums.
+size_t tc_wsum2_scratch_bytes(int64_t rows_pad, int64_t k_or_d);
+int tc_wsum2_pass(int mode, const void* rowQ, const void* colQ, const float* colBias,
+                  const float* rowBias, int64_t n_rows, int64_t n_cols, int64_t rows_pad,
+                  int64_t cols_pad, int64_t d, int64_t dpt, float kappa, const float* V,
+                  int64_t ldv, int64_t k, void* vtq, void* scratch, const float* rowW,
+                  const float* X, float* out, int64_t ldo, int sms, unsigned* status,
+                  cudaStream_t st);
+
 }  // namespace flashot

@@ -31,6 +31,7 @@
 #include "pack_kernels.cuh"
 #include "ptx.cuh"
 #include "tc_api.h"
+#include "tc_host.h"
 #include "trace.h"
 
 namespace flashot {
@@ -607,80 +608,6 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, unsigned* __rest
     ptx::fence_barrier_init();
     if (!ptx::mbar_wait(&bar, 0, limit_ns)) atomicOr(status, kErrTimeout);
   }
-}
-
-// ---- host helpers -------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2-D map over a packed operand (rows x cols elements, row-major), box = 128 rows x 128 B,
-// 128-byte swizzle (the layout the UMMA K-major SW128 descriptor expects).
-int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return FLASHOT_ERR_CUDA;
-  const int es = bf16 ? 2 : 4;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kBM};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
-}
-
-// 2-D map over a packed operand (rows x cols elements), box = box_rows x 128 B, 128-byte
-// swizzle: the column cloud of the LSE pass (256-row boxes) and the transposed right operand
-// of the weighted sums.
-int make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, bool bf16,
-                  int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return FLASHOT_ERR_CUDA;
-  const int es = bf16 ? 2 : 4;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FLASHOT_OK : FLASHOT_ERR_INVALID_ARG;
-}
-
-template <typename K>
-int set_smem(K kernel, int bytes) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  return e == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
-}
-
-// Number of persistent CTAs: at most one per SM, at most one per tile, and few enough
-// that no row tile is split over more than max_splits CTAs.
-int64_t choose_grid(int64_t row_tiles, int64_t NT, int sms, int max_splits) {
-  const int64_t T = row_tiles * NT;
-  int64_t G = std::min<int64_t>(sms, T);
-  while (G > 1) {
-    int64_t worst = 0;
-    for (int64_t rt = 0; rt < row_tiles; ++rt) {
-      const int64_t s = sk_owner((rt + 1) * NT - 1, T, G) - sk_owner(rt * NT, T, G) + 1;
-      worst = std::max(worst, s);
-    }
-    if (worst <= max_splits) break;
-    --G;
-  }
-  return std::max<int64_t>(G, 1);
 }
 
 }  // namespace tc
