@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "fma_kernels.cuh"
 #include "prep_kernels.cuh"
+#include "small_solve.h"
 #include "tc_api.h"
 #include "trace.h"
 #include <vector>
@@ -566,6 +567,11 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
       !is_device_ptr(f) || !is_device_ptr(g) || !opt_device_ptr(loss))
     return FLASHOT_ERR_INVALID_ARG;
+  // Small fp32 problems: every iteration in one launch of one thread-block cluster.
+  if (c.g.prec == FLASHOT_PREC_FP32 && c.g.small &&
+      small_solve_eligible(n, m, c.g.dpf, n_stages))
+    return small_solve(X, Y, a, b, n, m, d, c.g.dpf, eps_sched, n_stages, iters_per_stage,
+                       (flags & FLASHOT_WARM_START) != 0, f, g, loss, c.st);
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   // Initial F-step bias from g (warm start) or g = 0.
   if ((rc = launch_bias(c, (flags & FLASHOT_WARM_START) ? g : nullptr, false, eps_sched[0])) !=
