@@ -56,6 +56,10 @@ def parse_args():
                    help="profiling driver: pack once, run P f-updates and P g-updates of the "
                         "workload (no timing, no JSON line) and exit; for ncu captures")
     p.add_argument("--n", type=int, default=None, help="override n = m (profiling driver)")
+    p.add_argument("--schedule", choices=["alternating", "symmetric"], default="alternating",
+                   help="supplementary lines: iteration schedule of the solves")
+    p.add_argument("--divergence", action="store_true",
+                   help="supplementary line: debiased Sinkhorn divergence (three solves)")
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -290,10 +294,22 @@ def run_other_workload(args):
                                       workspace=ws, reuse_pack=True)
         units_per_step, unit, scores_per_step = 3, "transport applications/s", 3 * nm
         hot = lds.KernelTimer.WSUM
+    elif args.divergence:
+        res = torch.empty(4, dtype=torch.float64, device=dev)
+        dws = lds.Workspace(int(lds.library().flashot_divergence_workspace_bytes(
+            n, m, d, lds._flags(prec, schedule=args.schedule))))
+
+        def step():
+            lds.sinkhorn_divergence(X, Y, a, b, sched, pr.iters_per_stage, precision=prec,
+                                    schedule=args.schedule, out=res, workspace=dws)
+        units_per_step, unit = 1, "divergences/s"
+        scores_per_step = 2 * (n * m + n * n + m * m) * pr.total_iters
+        hot = lds.KernelTimer.LSE
+        per_launch_override = (n * m + n * n + m * m) / 3.0
     else:
         def step():
             lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
-                               g_out=g, loss_out=loss, workspace=ws)
+                               g_out=g, loss_out=loss, workspace=ws, schedule=args.schedule)
         units_per_step, unit = pr.total_iters, "iters/s"
         scores_per_step = 2 * nm * pr.total_iters
         hot = lds.KernelTimer.LSE
@@ -319,7 +335,7 @@ def run_other_workload(args):
     peaks, _ = load_peaks()
     clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
     avg = ms_hot / max(n_hot, 1) / 1e3
-    per_launch_scores = nm
+    per_launch_scores = locals().get("per_launch_override", nm)
     if prec == "fp32":
         roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
                 "peak": N_SMS * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)"}
@@ -335,7 +351,10 @@ def run_other_workload(args):
     roof["sfu_frac"] = (per_launch_scores / avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk)
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
-    line = {"metric": f"workload {idx} ({pr.name}) throughput", "supplementary": True,
+    line = {"metric": f"workload {idx} ({pr.name}) throughput"
+                      + (" [debiased divergence]" if args.divergence else "")
+                      + (" [symmetric schedule]" if args.schedule == "symmetric" else ""),
+            "supplementary": True,
             "value": units_per_step * args.steps / (ms / 1e3), "unit": unit,
             "score_evals_per_s": scores_per_step * args.steps / (ms / 1e3),
             "ms_per_step": ms / args.steps, "steps": args.steps, "warmup": args.warmup,
@@ -562,7 +581,7 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload != WORKLOAD_IDX:
+    elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":
         run_other_workload(args)
     else:
         if args.precision is None:

@@ -73,6 +73,10 @@ typedef struct CUstream_st *flashot_stream_t;
 /* The workspace already holds the packed X, Y, norms and log-weights written by an
  * earlier call with the same X, Y, a, b, n, m, d, flags and workspace; skip re-packing. */
 #define FLASHOT_REUSE_PACK  0x20
+/* solve: symmetric (averaged) schedule, f' = (f + F(g))/2 and g' = (g + G(f))/2 from the
+ * same previous iterate (the review's "Strengths": symmetric-vs-alternating comparison).
+ * Starts from f = g = 0, or with FLASHOT_WARM_START from the f and g passed in. */
+#define FLASHOT_SYMMETRIC   0x40
 
 /* ---- library information ------------------------------------------------------------ */
 int flashot_version(void);                       /* major*10000 + minor*100 + patch      */
@@ -140,6 +144,20 @@ int flashot_sinkhorn_step_f(const float *X, const float *Y, const float *b, cons
 int flashot_sinkhorn_step_g(const float *X, const float *Y, const float *a, const float *f,
                             int64_t n, int64_t m, int64_t d, float eps, int flags, float *g,
                             void *ws, size_t ws_bytes, flashot_stream_t stream);
+
+/*
+ * Debiased Sinkhorn divergence S(a, b) = OT(a, b) - OT(a, a)/2 - OT(b, b)/2 (the review's
+ * "Reproducibility & code": the debiased-Sinkhorn sweep of the OTDD pipeline), each OT
+ * term the dual loss of a solve of X against Y, X against X and Y against Y with the same
+ * eps schedule, iteration count and flags (FLASHOT_SYMMETRIC selects the schedule).
+ * out: FOUR device doubles {S, OT(a,b), OT(a,a), OT(b,b)}. ws must hold at least
+ * flashot_divergence_workspace_bytes(n, m, d, flags) bytes.
+ */
+size_t flashot_divergence_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags);
+int flashot_sinkhorn_divergence(const float *X, const float *Y, const float *a, const float *b,
+                                int64_t n, int64_t m, int64_t d, const float *eps_sched,
+                                int n_stages, int iters_per_stage, int flags, double *out,
+                                void *ws, size_t ws_bytes, flashot_stream_t stream);
 
 /* Dual loss sum_i a_i f_i + sum_j b_j g_j, reduced in fp64 into ONE device double. */
 int flashot_dual_loss(const float *a, const float *b, const float *f, const float *g,

@@ -24,6 +24,7 @@ __all__ = [
     "Workspace", "workspace_bytes", "sinkhorn_solve", "sinkhorn_step_f", "sinkhorn_step_g",
     "dual_loss", "transport_apply", "transport_hadamard_xy", "ot_grad_x", "workspace_status",
     "FlashotError", "library", "version", "launch_count", "KernelTimer",
+    "sinkhorn_divergence",
 ]
 
 
@@ -36,7 +37,8 @@ def version() -> int:
     return int(library().flashot_version())
 
 
-def _flags(precision: str, warm: bool = False, reuse: bool = False) -> int:
+def _flags(precision: str, warm: bool = False, reuse: bool = False,
+           schedule: str = "alternating") -> int:
     try:
         fl = PRECISIONS[precision]
     except KeyError:
@@ -45,6 +47,10 @@ def _flags(precision: str, warm: bool = False, reuse: bool = False) -> int:
         fl |= _binding.WARM_START
     if reuse:
         fl |= _binding.REUSE_PACK
+    if schedule == "symmetric":
+        fl |= _binding.SYMMETRIC
+    elif schedule != "alternating":
+        raise ValueError("schedule must be 'alternating' or 'symmetric'")
     return fl
 
 
@@ -119,13 +125,18 @@ def sinkhorn_solve(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] =
                    precision: str = "auto", g0: Optional[torch.Tensor] = None,
                    f_out: Optional[torch.Tensor] = None, g_out: Optional[torch.Tensor] = None,
                    loss_out: Optional[torch.Tensor] = None,
-                   workspace: Optional[Workspace] = None, reuse_pack: bool = False):
-    """Alternating solve; ``eps`` is a float or an annealing schedule (one eps per stage).
-    Returns (f, g, loss) with loss a 0-d float64 CUDA tensor. ``g0`` warm-starts."""
+                   workspace: Optional[Workspace] = None, reuse_pack: bool = False,
+                   schedule: str = "alternating", f0: Optional[torch.Tensor] = None):
+    """Solve; ``eps`` is a float or an annealing schedule (one eps per stage). Returns
+    (f, g, loss) with loss a 0-d float64 CUDA tensor. ``schedule`` is "alternating"
+    (f = F(g), then g = G(f)) or "symmetric" (both averaged with the previous iterate).
+    ``g0`` warm-starts the alternating schedule; ``f0`` and ``g0`` the symmetric one."""
     n, m, d = _sizes(X, Y)
     sched = [float(eps)] if isinstance(eps, (int, float)) else [float(e) for e in eps]
     lib = library()
     f = f_out if f_out is not None else torch.empty(n, dtype=torch.float32, device=X.device)
+    if f0 is not None and f.data_ptr() != f0.data_ptr():
+        f.copy_(f0)
     if g0 is not None:
         g = g_out if g_out is not None else torch.empty(m, dtype=torch.float32, device=X.device)
         if g.data_ptr() != g0.data_ptr():
@@ -134,7 +145,8 @@ def sinkhorn_solve(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] =
         g = g_out if g_out is not None else torch.empty(m, dtype=torch.float32, device=X.device)
     loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float64,
                                                              device=X.device)
-    flags = _flags(precision, warm=g0 is not None, reuse=reuse_pack)
+    warm = g0 is not None and (schedule == "alternating" or f0 is not None)
+    flags = _flags(precision, warm=warm, reuse=reuse_pack, schedule=schedule)
     ws = _ws(workspace, workspace_bytes(n, m, d, 0, precision))
     arr = (ctypes.c_float * len(sched))(*sched)
     st = lib.flashot_sinkhorn_solve(
@@ -279,3 +291,27 @@ class KernelTimer:
 
     def stop(self):
         library().flashot_timer_stop()
+
+
+def sinkhorn_divergence(X, Y, a=None, b=None, eps: Union[float, Sequence[float]] = 0.1,
+                        iters_per_stage: int = 100, *, precision: str = "auto",
+                        schedule: str = "symmetric", out=None, workspace=None):
+    """Debiased Sinkhorn divergence S = OT(a,b) - OT(a,a)/2 - OT(b,b)/2. Returns a float64
+    CUDA tensor [S, OT(a,b), OT(a,a), OT(b,b)]."""
+    n, m, d = _sizes(X, Y)
+    sched = [float(eps)] if isinstance(eps, (int, float)) else [float(e) for e in eps]
+    lib = library()
+    flags = _flags(precision, schedule=schedule)
+    nb = int(lib.flashot_divergence_workspace_bytes(n, m, d, flags))
+    if nb == 0:
+        raise ValueError("invalid sizes")
+    ws = _ws(workspace, nb)
+    res = out if out is not None else torch.empty(4, dtype=torch.float64, device=X.device)
+    arr = (ctypes.c_float * len(sched))(*sched)
+    st = lib.flashot_sinkhorn_divergence(
+        _dev_ptr(X, "X", (n, d)), _dev_ptr(Y, "Y", (m, d)),
+        _dev_ptr(a, "a", (n,), optional=True), _dev_ptr(b, "b", (m,), optional=True),
+        n, m, d, arr, len(sched), int(iters_per_stage), flags,
+        _dev_ptr(res, "out", (4,), dtype=torch.float64), ws.ptr, ws.nbytes, _stream())
+    _binding.check(st, "flashot_sinkhorn_divergence")
+    return res

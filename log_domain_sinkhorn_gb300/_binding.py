@@ -34,6 +34,7 @@ PREC_BF16 = 0x3
 PREC_TF32X3 = 0x4
 WARM_START = 0x10
 REUSE_PACK = 0x20
+SYMMETRIC = 0x40
 
 KERNEL_LSE = 0
 KERNEL_WSUM = 1
@@ -64,6 +65,11 @@ SIGNATURES = {
     "flashot_sinkhorn_step_g": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int, _vp, _vp,
         ctypes.c_size_t, _vp]),
+    "flashot_divergence_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64,
+                                                             ctypes.c_int]),
+    "flashot_sinkhorn_divergence": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.POINTER(ctypes.c_float),
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, ctypes.c_size_t, _vp]),
     "flashot_dual_loss": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _vp, _vp, ctypes.c_size_t, _vp]),
     "flashot_transport_apply": (ctypes.c_int, [

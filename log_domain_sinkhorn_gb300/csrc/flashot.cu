@@ -287,7 +287,7 @@ int launch_bias(const Ctx& c, const float* pot, bool x_side, float eps) {
 // the next pass's bias biasG (at eps_next), and optionally the row LSE (base 2).
 // G-type: the same with X and Y exchanged.
 int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* out_pot,
-                 bool write_next_bias, float* out_lse2) {
+                 bool write_next_bias, float* out_lse2, bool average = false) {
   const Geometry& g = c.g;
   const int64_t n_rows = x_rows ? g.n : g.m;
   const int64_t rows_pad = x_rows ? g.n_pad : g.m_pad;
@@ -352,7 +352,8 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
     lse_combine_kernel<<<grid1(rows_pad, 256), 256, 0, c.st>>>(
         partial, split, rows_pad, n_rows, rows_pad, c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
         c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
-        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr, out_lse2);
+        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr, out_lse2,
+      average ? 1 : 0);
   }
   return launch_check();
 }
@@ -567,12 +568,32 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
       !is_device_ptr(f) || !is_device_ptr(g) || !opt_device_ptr(loss))
     return FLASHOT_ERR_INVALID_ARG;
+  const bool symmetric = (flags & FLASHOT_SYMMETRIC) != 0;
   // Small fp32 problems: every iteration in one launch of one thread-block cluster.
-  if (c.g.prec == FLASHOT_PREC_FP32 && c.g.small &&
+  if (!symmetric && c.g.prec == FLASHOT_PREC_FP32 && c.g.small &&
       small_solve_eligible(n, m, c.g.dpf, n_stages))
     return small_solve(X, Y, a, b, n, m, d, c.g.dpf, eps_sched, n_stages, iters_per_stage,
                        (flags & FLASHOT_WARM_START) != 0, f, g, loss, c.st);
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if (symmetric) {
+    // Both half-steps read the previous iterate; the combines average in place.
+    if (!(flags & FLASHOT_WARM_START)) {
+      cudaError_t e = cudaMemsetAsync(f, 0, (size_t)n * sizeof(float), c.st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(g, 0, (size_t)m * sizeof(float), c.st);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    for (int s = 0; s < n_stages; ++s) {
+      const float eps = eps_sched[s];
+      for (int it = 0; it < iters_per_stage; ++it) {
+        if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+        if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+        if ((rc = run_lse_pass(c, true, eps, eps, f, false, nullptr, true)) != FLASHOT_OK)
+          return rc;
+        if ((rc = run_lse_pass(c, false, eps, eps, g, false, nullptr, true)) != FLASHOT_OK)
+          return rc;
+      }
+    }
+  } else {
   // Initial F-step bias from g (warm start) or g = 0.
   if ((rc = launch_bias(c, (flags & FLASHOT_WARM_START) ? g : nullptr, false, eps_sched[0])) !=
       FLASHOT_OK)
@@ -586,6 +607,7 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
       if ((rc = run_lse_pass(c, false, eps, eps_next, g, true, nullptr)) != FLASHOT_OK) return rc;
     }
   }
+  }
   if (loss) {
     {
       TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
@@ -595,6 +617,59 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
     if ((rc = launch_check()) != FLASHOT_OK) return rc;
   }
   return FLASHOT_OK;
+}
+
+size_t flashot_divergence_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags) {
+  const size_t w1 = flashot_workspace_bytes(n, m, d, 0, flags);
+  const size_t w2 = flashot_workspace_bytes(n, n, d, 0, flags);
+  const size_t w3 = flashot_workspace_bytes(m, m, d, 0, flags);
+  if (w1 == 0 || w2 == 0 || w3 == 0) return 0;
+  // six potential vectors (f, g of the three solves), each 256-byte aligned, then the
+  // largest solve workspace
+  const size_t pots = 2 * ((size_t)(n + 64) * 4 / 256 + 1) * 256 * 2 +
+                      2 * ((size_t)(m + 64) * 4 / 256 + 1) * 256 * 2;
+  return pots + std::max(w1, std::max(w2, w3)) + 256;
+}
+
+int flashot_sinkhorn_divergence(const float* X, const float* Y, const float* a, const float* b,
+                                int64_t n, int64_t m, int64_t d, const float* eps_sched,
+                                int n_stages, int iters_per_stage, int flags, double* out,
+                                void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  const size_t need = flashot_divergence_workspace_bytes(n, m, d, flags);
+  if (need == 0 || !is_device_ptr(out)) return FLASHOT_ERR_INVALID_ARG;
+  if (!is_device_ptr(ws)) return FLASHOT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FLASHOT_ERR_ALIGNMENT;
+  if (ws_bytes < need) return FLASHOT_ERR_WORKSPACE_TOO_SMALL;
+  char* p = static_cast<char*>(ws);
+  auto take = [&](int64_t count) {
+    float* r = reinterpret_cast<float*>(p);
+    p += ((size_t)(count + 64) * 4 / 256 + 1) * 256;
+    return r;
+  };
+  float* f_xy = take(n);
+  float* g_xy = take(m);
+  float* f_xx = take(n);
+  float* g_xx = take(n);
+  float* f_yy = take(m);
+  float* g_yy = take(m);
+  const size_t used = (size_t)(p - static_cast<char*>(ws));
+  void* sub = p;
+  const size_t sub_bytes = ws_bytes - used;
+  const int sflags = flags & ~(FLASHOT_WARM_START | FLASHOT_REUSE_PACK);
+  int rc = flashot_sinkhorn_solve(X, Y, a, b, n, m, d, eps_sched, n_stages, iters_per_stage,
+                                  sflags, f_xy, g_xy, out + 1, sub, sub_bytes, stream);
+  if (rc == FLASHOT_OK)
+    rc = flashot_sinkhorn_solve(X, X, a, a, n, n, d, eps_sched, n_stages, iters_per_stage,
+                                sflags, f_xx, g_xx, out + 2, sub, sub_bytes, stream);
+  if (rc == FLASHOT_OK)
+    rc = flashot_sinkhorn_solve(Y, Y, b, b, m, m, d, eps_sched, n_stages, iters_per_stage,
+                                sflags, f_yy, g_yy, out + 3, sub, sub_bytes, stream);
+  if (rc != FLASHOT_OK) return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, reinterpret_cast<cudaStream_t>(stream));
+    divergence_combine_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(out);
+  }
+  return launch_check();
 }
 
 int flashot_sinkhorn_step_f(const float* X, const float* Y, const float* b, const float* g,

@@ -61,7 +61,8 @@ __global__ void bias_kernel(const float* __restrict__ pot, const float* __restri
 }
 
 // Merge per-split (max, sum) partials of the base-2 LSE and finish the half-step:
-//   L_i  = M + log2 S,   pot_i = norm_i - eps ln2 L_i,
+//   L_i  = M + log2 S,   pot_i = norm_i - eps ln2 L_i   (averaged with the previous out_pot
+//   when `average` is set: the symmetric schedule),
 //   next_bias_i = lw2_i - L_i * (eps / eps_next)   (= (pot_i - norm_i) log2e/eps_next + lw2_i)
 // next_bias is the bias the following pass (the other side's update at eps_next) needs;
 // its padding entries [rows, rows_pad) are set to -inf so padded points carry no mass.
@@ -70,7 +71,7 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
                                    const float* __restrict__ norms, float eps,
                                    const float* __restrict__ lw2, float eps_ratio,
                                    float* __restrict__ out_pot, float* __restrict__ next_bias,
-                                   float* __restrict__ out_lse2) {
+                                   float* __restrict__ out_lse2, int average) {
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= rows) {
     if (i < rows_pad && next_bias) next_bias[i] = neg_inf();
@@ -91,7 +92,9 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
     S += p.y * ex2(p.x - M);
   }
   const float L = M + log2f(S);  // S == 0 (no mass) gives -inf, so pot = +inf
-  const float pot = norms[i] - eps * kLn2 * L;
+  const float fresh = norms[i] - eps * kLn2 * L;
+  // Symmetric schedule: the new potential is the mean of the previous one and the update.
+  const float pot = average ? 0.5f * (out_pot[i] + fresh) : fresh;
   if (out_pot) out_pot[i] = pot;
   if (next_bias) next_bias[i] = lw2[i] - L * eps_ratio;
   if (out_lse2) out_lse2[i] = L;
@@ -118,4 +121,11 @@ dual_loss_kernel(const float* __restrict__ wa, const float* __restrict__ f, int6
   }
 }
 
+}  // namespace flashot
+
+namespace flashot {
+// out[0] = out[1] - out[2] / 2 - out[3] / 2 (the debiased divergence from its three terms).
+__global__ void divergence_combine_kernel(double* __restrict__ out) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) out[0] = out[1] - 0.5 * out[2] - 0.5 * out[3];
+}
 }  // namespace flashot

@@ -21,6 +21,9 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
                              the gradient identity grad_i = 2(a_i x_i - (P~ Y)_i).
   hadamard_xy                h_i = <x_i, (P Y)_i> and d/dt OT(X, tY) finite difference.
   marginals                  row sums = a after F and column sums = b after G.
+  solve_symmetric            X = Y gives f == g at every iteration; same converged loss
+                             as the alternating schedule.
+  sinkhorn_divergence        S(a, a) = 0; S >= 0; eps -> inf limit |mean x - mean y|^2.
 """
 from __future__ import annotations
 
@@ -74,6 +77,10 @@ def _lib():
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _dp, _dp, _dp]
             lib.oracle_solve.restype = ctypes.c_int
+            lib.oracle_solve_symmetric.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _dp,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   _dp, _dp, _dp]
+            lib.oracle_solve_symmetric.restype = ctypes.c_int
             lib.oracle_transport_apply.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
                                                    _i64, ctypes.c_double, _dp, _i64,
                                                    ctypes.c_int, _i64p, _i64, _dp]
@@ -154,6 +161,33 @@ def solve(X, Y, a, b, eps_schedule, iters_per_stage, g0=None):
                         int(iters_per_stage), 0 if g0 is None else 1, _p(f), _p(g),
                         ctypes.byref(loss))
     return f, g, float(loss.value)
+
+
+def solve_symmetric(X, Y, a, b, eps_schedule, iters_per_stage, f0=None, g0=None):
+    """Symmetric (averaged) schedule f' = (f + F(g))/2, g' = (g + G(f))/2 from f = g = 0
+    (or the given f0, g0). Returns (f, g, loss) in fp64."""
+    X, Y, a, b = _f64(X), _f64(Y), _f64(a), _f64(b)
+    n, d = X.shape
+    m = Y.shape[0]
+    sched = _f64(np.atleast_1d(eps_schedule))
+    warm = f0 is not None and g0 is not None
+    f = _f64(f0).copy() if warm else np.zeros(n, dtype=np.float64)
+    g = _f64(g0).copy() if warm else np.zeros(m, dtype=np.float64)
+    loss = ctypes.c_double(0.0)
+    _lib().oracle_solve_symmetric(_p(X), _p(Y), _p(a), _p(b), n, m, d, _p(sched),
+                                  int(sched.size), int(iters_per_stage), 1 if warm else 0,
+                                  _p(f), _p(g), ctypes.byref(loss))
+    return f, g, float(loss.value)
+
+
+def sinkhorn_divergence(X, Y, a, b, eps_schedule, iters_per_stage, symmetric=True):
+    """Debiased Sinkhorn divergence S = OT(a,b) - OT(a,a)/2 - OT(b,b)/2, each term the dual
+    loss of a solve with the chosen schedule. Returns (S, L_xy, L_xx, L_yy)."""
+    run = solve_symmetric if symmetric else solve
+    lxy = run(X, Y, a, b, eps_schedule, iters_per_stage)[2]
+    lxx = run(X, X, a, a, eps_schedule, iters_per_stage)[2]
+    lyy = run(Y, Y, b, b, eps_schedule, iters_per_stage)[2]
+    return lxy - 0.5 * lxx - 0.5 * lyy, lxy, lxx, lyy
 
 
 def transport_apply(X, Y, a, b, f, g, eps, V, transpose=False, rows=None) -> np.ndarray:

@@ -135,6 +135,39 @@ int oracle_solve(const double *X, const double *Y, const double *a, const double
     return 0;
 }
 
+/*
+ * Symmetric (averaged) schedule (the "symmetric-vs-alternating" comparison of the SAI
+ * replication review, "Strengths"): both half-steps use the previous iterate,
+ *     f' = (f + F(g)) / 2,   g' = (g + G(f)) / 2,
+ * starting from f = g = 0 unless warm_start != 0 (then the given f and g are read).
+ * Writes f, g and *loss = <a,f> + <b,g>.
+ */
+int oracle_solve_symmetric(const double *X, const double *Y, const double *a, const double *b,
+                           int64_t n, int64_t m, int64_t d, const double *eps_sched,
+                           int n_stages, int iters_per_stage, int warm_start, double *f,
+                           double *g, double *loss)
+{
+    double *fn = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    double *gn = (double *)malloc((size_t)(m > 0 ? m : 1) * sizeof(double));
+    if (!warm_start) {
+        for (int64_t i = 0; i < n; ++i) f[i] = 0.0;
+        for (int64_t j = 0; j < m; ++j) g[j] = 0.0;
+    }
+    for (int s = 0; s < n_stages; ++s) {
+        double eps = eps_sched[s];
+        for (int it = 0; it < iters_per_stage; ++it) {
+            oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, fn);
+            oracle_half_step(Y, m, X, n, d, a, f, eps, NULL, m, gn);
+            for (int64_t i = 0; i < n; ++i) f[i] = 0.5 * (f[i] + fn[i]);
+            for (int64_t j = 0; j < m; ++j) g[j] = 0.5 * (g[j] + gn[j]);
+        }
+    }
+    if (loss) *loss = oracle_dual_loss(a, b, f, g, n, m);
+    free(fn);
+    free(gn);
+    return 0;
+}
+
 /* P_ij = a_i b_j exp((f_i + g_j - C_ij) / eps): the plan defined by the potentials. */
 static double plan_entry(const double *xi, const double *yj, int64_t d, double ai, double bj,
                          double fi, double gj, double eps)

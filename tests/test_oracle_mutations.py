@@ -30,6 +30,8 @@ MUTATIONS = {
         "oracle_half_step(Y, m, X, n, d, a, f, eps, NULL, m, g);\n"
         "            oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, f);"),
     "row_sum_scaled": ("row_sums[i] = s;", "row_sums[i] = s * 1.0000001;"),
+    "symmetric_no_average": ("f[i] = 0.5 * (f[i] + fn[i]);", "f[i] = fn[i];"),
+    "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
 }
 
 

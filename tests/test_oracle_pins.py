@@ -399,3 +399,59 @@ def test_golden_fixture_regression():
     idx = gold["sample_index"]
     np.testing.assert_allclose(f[idx], gold["f"], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(g[idx], gold["g"], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------
+# Symmetric schedule and the debiased Sinkhorn divergence
+# ---------------------------------------------------------------------------------
+
+def test_symmetric_schedule_keeps_f_equal_g_on_symmetric_problem():
+    """X = Y, a = b, f = g = 0: F and G are the same map, so the averaged updates keep
+    f == g exactly at every iteration."""
+    rng = np.random.default_rng(5)
+    X = rng.normal(size=(13, 3))
+    a = rng.exponential(size=13); a /= a.sum()
+    for iters in (1, 2, 7):
+        f, g, _ = oracle.solve_symmetric(X, X, a, a, [0.3], iters)
+        np.testing.assert_array_equal(f, g)
+
+
+def test_symmetric_and_alternating_reach_the_same_optimum():
+    X, Y, a, b, _, _ = _random_instance(seed=61, n=11, m=9, d=2)
+    a = a / a.sum(); b = b / b.sum()
+    eps = 0.3
+    _, _, l_alt = converge(X, Y, a, b, eps, tol=1e-14)
+    f, g, l_sym = oracle.solve_symmetric(X, Y, a, b, [eps], 3000)
+    assert l_sym == pytest.approx(l_alt, rel=1e-11)
+    # and the symmetric fixed point satisfies both marginal conditions
+    r, c = oracle.marginals(X, Y, a, b, f, g, eps)
+    np.testing.assert_allclose(r, a, atol=1e-12)
+    np.testing.assert_allclose(c, b, atol=1e-12)
+
+
+def test_divergence_is_zero_on_identical_measures_and_nonnegative():
+    """S(a, a) = 0 exactly (the three solves coincide); S >= 0 for the Gaussian kernel of
+    the squared Euclidean cost (debiased divergences are positive)."""
+    rng = np.random.default_rng(8)
+    X = rng.normal(size=(10, 2))
+    a = rng.exponential(size=10); a /= a.sum()
+    s, lxy, lxx, lyy = oracle.sinkhorn_divergence(X, X, a, a, [0.5], 400)
+    assert s == 0.0
+    for seed in range(4):
+        r2 = np.random.default_rng(100 + seed)
+        Y = r2.normal(size=(12, 2)) * 0.7 + 0.2
+        b = r2.exponential(size=12); b /= b.sum()
+        s, *_ = oracle.sinkhorn_divergence(X, Y, a, b, [0.5], 600)
+        assert s > 0.0
+
+
+def test_divergence_large_eps_limit_is_squared_mean_distance():
+    """eps -> inf: each term tends to its independent-coupling cost, so for the squared
+    Euclidean cost S -> E|x-y|^2 - E|x-x'|^2/2 - E|y-y'|^2/2 = |mean x - mean y|^2."""
+    rng = np.random.default_rng(9)
+    X = rng.normal(size=(14, 3))
+    Y = rng.normal(size=(9, 3)) + np.array([0.5, -1.0, 0.2])
+    a = rng.exponential(size=14); a /= a.sum()
+    b = rng.exponential(size=9); b /= b.sum()
+    s, *_ = oracle.sinkhorn_divergence(X, Y, a, b, [1e6], 4)
+    assert s == pytest.approx(float(((a @ X - b @ Y) ** 2).sum()), rel=1e-5)
