@@ -24,6 +24,10 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   solve_symmetric            X = Y gives f == g at every iteration; same converged loss
                              as the alternating schedule.
   sinkhorn_divergence        S(a, a) = 0; S >= 0; eps -> inf limit |mean x - mean y|^2.
+  solve_tol                  with tol = 0 it equals solve; each reported error equals the
+                             row-marginal L1 error recomputed from the plan by
+                             marginals(); it stops at the first check below tol; the
+                             measured errors are non-increasing.
 """
 from __future__ import annotations
 
@@ -81,6 +85,11 @@ def _lib():
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _dp, _dp, _dp]
             lib.oracle_solve_symmetric.restype = ctypes.c_int
+            lib.oracle_solve_tol.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                             ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                                             ctypes.c_int, _dp, _dp, _dp,
+                                             ctypes.POINTER(ctypes.c_int), _dp, _dp]
+            lib.oracle_solve_tol.restype = ctypes.c_int
             lib.oracle_transport_apply.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64,
                                                    _i64, ctypes.c_double, _dp, _i64,
                                                    ctypes.c_int, _i64p, _i64, _dp]
@@ -178,6 +187,33 @@ def solve_symmetric(X, Y, a, b, eps_schedule, iters_per_stage, f0=None, g0=None)
                                   int(sched.size), int(iters_per_stage), 1 if warm else 0,
                                   _p(f), _p(g), ctypes.byref(loss))
     return f, g, float(loss.value)
+
+
+def solve_tol(X, Y, a, b, eps, tol, max_iters, check_every=1, history=False):
+    """Alternating solve at one eps that stops after the first check iteration k (k >= 2,
+    k % check_every == 0) at which the row-marginal L1 error of iterate k-1, measured by
+    the f-update of iteration k, is below tol. Returns (f, g, loss, iters_done, err), err
+    being the last measured error (-1 if none); with history=True also the array of the
+    errors measured at every check."""
+    X, Y, a, b = _f64(X), _f64(Y), _f64(a), _f64(b)
+    n, d = X.shape
+    m = Y.shape[0]
+    if max_iters < 1 or check_every < 1:
+        raise ValueError("max_iters and check_every must be >= 1")
+    f = np.zeros(n, dtype=np.float64)
+    g = np.zeros(m, dtype=np.float64)
+    loss = ctypes.c_double(0.0)
+    done = ctypes.c_int(0)
+    err = ctypes.c_double(0.0)
+    hist = np.full(max(max_iters // check_every, 1), np.nan, dtype=np.float64)
+    _lib().oracle_solve_tol(_p(X), _p(Y), _p(a), _p(b), n, m, d, float(eps), float(tol),
+                            int(max_iters), int(check_every), _p(f), _p(g),
+                            ctypes.byref(loss), ctypes.byref(done), ctypes.byref(err),
+                            _p(hist))
+    out = (f, g, float(loss.value), int(done.value), float(err.value))
+    if history:
+        return out + (hist[: done.value // check_every],)
+    return out
 
 
 def sinkhorn_divergence(X, Y, a, b, eps_schedule, iters_per_stage, symmetric=True):

@@ -168,6 +168,52 @@ int oracle_solve_symmetric(const double *X, const double *Y, const double *a, co
     return 0;
 }
 
+/*
+ * Convergence-driven alternating solve at one eps (SAI replication review, "Strengths":
+ * runs to a marginal-error tolerance and the low-eps regime). Iteration k = 1, 2, ... is
+ * f <- F(g), then g <- G(f). After a g-update the column sums of P equal b exactly, so the
+ * error of an iterate is its row-marginal L1 error
+ *     err(f, g) = sum_i | sum_j P_ij(f, g) - a_i |.
+ * F(g) is the potential that makes row i sum to a_i, hence
+ *     sum_j P_ij(f, g) = a_i exp((f_i - F(g)_i) / eps),
+ * and the f-update of iteration k gives the error of iterate k-1 from its old and new f:
+ *     err_{k-1} = sum_i a_i |exp((f_i^{k-1} - f_i^k) / eps) - 1|.
+ * On check iterations (k >= 2 and k % check_every == 0) that error is measured, stored in
+ * err_hist[k / check_every - 1] if err_hist != NULL, and if it is below tol the loop
+ * stops after iteration k. Otherwise it stops after max_iters iterations.
+ * Writes f, g, *loss = <a,f> + <b,g>, *iters_done and *err (the last measured error, or
+ * -1 if none was measured). g starts at 0.
+ */
+int oracle_solve_tol(const double *X, const double *Y, const double *a, const double *b,
+                     int64_t n, int64_t m, int64_t d, double eps, double tol, int max_iters,
+                     int check_every, double *f, double *g, double *loss, int *iters_done,
+                     double *err, double *err_hist)
+{
+    double *fprev = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    int k = 0;
+    *err = -1.0;
+    for (int64_t j = 0; j < m; ++j) g[j] = 0.0;
+    for (k = 1; k <= max_iters; ++k) {
+        const int check = (k >= 2 && k % check_every == 0);
+        if (check)
+            for (int64_t i = 0; i < n; ++i) fprev[i] = f[i];
+        oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, f);
+        if (check) {
+            double e = 0.0;
+            for (int64_t i = 0; i < n; ++i)
+                if (a[i] > 0.0) e += a[i] * fabs(expm1((fprev[i] - f[i]) / eps));
+            *err = e;
+            if (err_hist) err_hist[k / check_every - 1] = e;
+        }
+        oracle_half_step(Y, m, X, n, d, a, f, eps, NULL, m, g);
+        if (check && *err < tol) break;
+    }
+    *iters_done = k > max_iters ? max_iters : k;
+    if (loss) *loss = oracle_dual_loss(a, b, f, g, n, m);
+    free(fprev);
+    return 0;
+}
+
 /* P_ij = a_i b_j exp((f_i + g_j - C_ij) / eps): the plan defined by the potentials. */
 static double plan_entry(const double *xi, const double *yj, int64_t d, double ai, double bj,
                          double fi, double gj, double eps)

@@ -31,6 +31,9 @@ MUTATIONS = {
         "            oracle_half_step(X, n, Y, m, d, b, g, eps, NULL, n, f);"),
     "row_sum_scaled": ("row_sums[i] = s;", "row_sums[i] = s * 1.0000001;"),
     "symmetric_no_average": ("f[i] = 0.5 * (f[i] + fn[i]);", "f[i] = fn[i];"),
+    "tol_error_wrong_direction": ("expm1((fprev[i] - f[i]) / eps)", "expm1((f[i] - fprev[i]) / eps)"),
+    "tol_error_drops_weight": ("e += a[i] * fabs(", "e += fabs("),
+    "tol_iters_off_by_one": ("max_iters : k;", "max_iters : k - 1;"),
     "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
 }
 

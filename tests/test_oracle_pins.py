@@ -455,3 +455,63 @@ def test_divergence_large_eps_limit_is_squared_mean_distance():
     b = rng.exponential(size=9); b /= b.sum()
     s, *_ = oracle.sinkhorn_divergence(X, Y, a, b, [1e6], 4)
     assert s == pytest.approx(float(((a @ X - b @ Y) ** 2).sum()), rel=1e-5)
+
+
+# ---------------------------------------------------------------------------------
+# Convergence-driven solve (stop on the row-marginal error)
+# ---------------------------------------------------------------------------------
+
+def _row_error(X, Y, a, b, f, g, eps):
+    """sum_i |sum_j P_ij - a_i| from the dense plan (test-side restatement)."""
+    return float(np.abs(plan(X, Y, a, b, f, g, eps).sum(1) - a).sum())
+
+
+def test_solve_tol_without_stopping_equals_fixed_iterations():
+    """tol = 0 never stops: max_iters iterations of the same alternating loop."""
+    X, Y, a, b, _, _ = _random_instance(seed=71, n=23, m=17, d=3)
+    eps = 0.2
+    f, g, loss, done, err = oracle.solve_tol(X, Y, a, b, eps, 0.0, 37, check_every=3)
+    f2, g2, loss2 = oracle.solve(X, Y, a, b, [eps], 37)
+    assert done == 37
+    np.testing.assert_array_equal(f, f2)
+    np.testing.assert_array_equal(g, g2)
+    assert loss == loss2
+    assert err > 0.0
+    # too few iterations for any check: no error measured
+    assert oracle.solve_tol(X, Y, a, b, eps, 1.0, 1, check_every=1)[4] == -1.0
+
+
+def test_solve_tol_error_is_the_row_marginal_error():
+    """The error measured during the f-update of iteration k is the L1 row-marginal error
+    of iterate k-1, recomputed here from the dense plan of that iterate."""
+    X, Y, a, b, _, _ = _random_instance(seed=72, n=19, m=29, d=4)
+    eps = 0.15
+    for K in (2, 5, 12):
+        *_, done, err = oracle.solve_tol(X, Y, a, b, eps, 0.0, K, check_every=K)
+        f, g, _ = oracle.solve(X, Y, a, b, [eps], K - 1)
+        assert done == K
+        assert err == pytest.approx(_row_error(X, Y, a, b, f, g, eps), rel=1e-9, abs=1e-15)
+    # column marginals of an iterate are exact, so the row error is the whole error
+    f, g, _ = oracle.solve(X, Y, a, b, [eps], 4)
+    np.testing.assert_allclose(plan(X, Y, a, b, f, g, eps).sum(0), b, rtol=1e-12)
+
+
+def test_solve_tol_errors_are_nonincreasing_and_stop_at_first_check_below_tol():
+    """Marginal errors of Sinkhorn iterates do not increase (Hilbert-metric contraction);
+    the solve stops at the first check whose error is below tol and returns that iterate."""
+    X, Y, a, b, _, _ = _random_instance(seed=73, n=31, m=27, d=3)
+    eps, c = 0.5, 4
+    *_, done, err, hist = oracle.solve_tol(X, Y, a, b, eps, 0.0, 200, check_every=c,
+                                           history=True)
+    assert done == 200 and hist.size == 50 and err == hist[-1]
+    assert np.all(np.diff(hist) <= 1e-15 + 1e-12 * hist[:-1])
+    assert hist[-1] < 1e-3 * hist[0]
+    for j in (3, 10, 25):
+        tol = math.sqrt(hist[j] * hist[j - 1])
+        f, g, loss, done, err = oracle.solve_tol(X, Y, a, b, eps, tol, 200, check_every=c)
+        assert done == (j + 1) * c and err == hist[j]
+        f2, g2, loss2 = oracle.solve(X, Y, a, b, [eps], done)
+        np.testing.assert_array_equal(f, f2)
+        assert loss == loss2
+        # the returned iterate is at least as good as the measured one
+        assert _row_error(X, Y, a, b, f, g, eps) <= err * (1 + 1e-9)
