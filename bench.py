@@ -60,6 +60,15 @@ def parse_args():
                    help="supplementary lines: iteration schedule of the solves")
     p.add_argument("--divergence", action="store_true",
                    help="supplementary line: debiased Sinkhorn divergence (three solves)")
+    p.add_argument("--tol", type=float, default=None,
+                   help="supplementary line: convergence-driven solve of --workload to this "
+                        "L1 marginal error (with --eps, --max-iters, --check-every)")
+    p.add_argument("--eps", type=float, default=None, help="override eps (--tol, --drift)")
+    p.add_argument("--max-iters", type=int, default=5000)
+    p.add_argument("--check-every", type=int, default=10)
+    p.add_argument("--drift", action="store_true",
+                   help="supplementary line: fp32 GPU vs fp64 oracle drift over a long "
+                        "low-eps run (n = m = 1000, d = 2, eps = 0.001, 3000 iterations)")
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -365,6 +374,137 @@ def run_other_workload(args):
     print(json.dumps(line), flush=True)
 
 
+def _problem_on_device(pr, dev):
+    import torch
+    X = torch.from_numpy(pr.X).to(dev)
+    Y = torch.from_numpy(pr.Y).to(dev)
+    a = None if pr.uniform_weights else torch.from_numpy(pr.a).to(dev)
+    b = None if pr.uniform_weights else torch.from_numpy(pr.b).to(dev)
+    return X, Y, a, b
+
+
+def run_convergence(args):
+    """Supplementary line: the convergence-driven solve (stop when the L1 row-marginal error
+    measured inside the f-update falls below --tol) on a workload at one eps. Reports the
+    iterations and time to tolerance, and the cost of the checks against a fixed-iteration
+    solve of the same length."""
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    from workloads import workload
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pr = workload(args.workload)
+    prec = args.precision or ("fp32" if pr.d < 32 else "bf16")
+    eps = float(args.eps if args.eps is not None else pr.eps_schedule[-1])
+    n, m, d = pr.n, pr.m, pr.d
+    X, Y, a, b = _problem_on_device(pr, dev)
+    ws = lds.Workspace(lds.workspace_bytes(n, m, d, 0, prec))
+    f = torch.empty(n, device=dev)
+    g = torch.empty(m, device=dev)
+    loss = torch.empty((), dtype=torch.float64, device=dev)
+    res = {}
+
+    def tol_solve():
+        res["out"] = lds.sinkhorn_solve_tol(X, Y, a, b, eps, args.tol, args.max_iters,
+                                            args.check_every, precision=prec, f_out=f,
+                                            g_out=g, loss_out=loss, workspace=ws)
+
+    for _ in range(args.warmup):
+        tol_solve()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        tol_solve()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    _, _, _, iters, err, hist = res["out"]
+    ms_tol = statistics.median(times)
+    # the same number of iterations without checks
+    fixed = []
+    for i in range(args.warmup + args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        lds.sinkhorn_solve(X, Y, a, b, eps, iters, precision=prec, f_out=f, g_out=g,
+                           loss_out=loss, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            fixed.append(e0.elapsed_time(e1))
+    ms_fixed = statistics.median(fixed)
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("device timeout reported")
+    line = {"metric": f"workload {args.workload} ({pr.name}) convergence-driven solve",
+            "supplementary": True, "value": iters / (ms_tol / 1e3), "unit": "iters/s",
+            "ms_to_tolerance": ms_tol, "iters_to_tolerance": iters, "final_l1_error": err,
+            "reached": bool(0 <= err < args.tol),
+            "errors_at_checks": [h for h in hist[:: max(1, len(hist) // 20)]],
+            "ms_fixed_same_iters": ms_fixed,
+            "check_overhead_frac": (ms_tol - ms_fixed) / ms_fixed,
+            "steps": args.steps, "warmup": args.warmup, "dtype": prec,
+            "config": {"workload": pr.name, "n": n, "m": m, "d": d, "eps": eps,
+                       "tol": args.tol, "max_iters": args.max_iters,
+                       "check_every": args.check_every, "start": "g = 0"}}
+    print(json.dumps(line), flush=True)
+
+
+def run_drift(args):
+    """Supplementary line: drift of the fp32 GPU iterates from the fp64 oracle over a long
+    low-eps run (Uniform[0,1]^2 clouds, n = m = 1000, eps = 0.001, 3000 iterations; the
+    L1 marginal error falls about 10x per 450 iterations). Reports the potentials' error
+    as given and after removing the constant shift (f + c, g - c) that leaves the plan
+    unchanged, the loss error, and the measured marginal errors of both runs."""
+    import numpy as np
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    import oracle
+    from workloads import make_problem
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    n, d, eps = 1000, 2, float(args.eps if args.eps is not None else 0.001)
+    iters, c = min(args.max_iters, 3000), 100
+    pr = make_problem(n, n, d, x_dist="unif01", weights="uniform", seed=4242)
+    X, Y, a, b = _problem_on_device(pr, dev)
+    out = {}
+    for prec in ([args.precision] if args.precision else ["fp32", "tf32x3"]):
+        f, g, loss, done, err, hist = lds.sinkhorn_solve_tol(X, Y, a, b, eps, 0.0, iters, c,
+                                                             precision=prec)
+        out[prec] = (f.cpu().numpy().astype(np.float64), g.cpu().numpy().astype(np.float64),
+                     float(loss.cpu()), np.asarray(hist))
+    t0 = time.perf_counter()
+    f_r, g_r, loss_r, _, _, hist_r = oracle.solve_tol(pr.X, pr.Y, pr.a, pr.b, eps, 0.0, iters,
+                                                      c, history=True)
+    t_oracle = time.perf_counter() - t0
+    scale = max(np.abs(f_r).max(), np.abs(g_r).max())
+    res = {}
+    for prec, (f, g, loss, hist) in out.items():
+        shift = (np.mean(f - f_r) - np.mean(g - g_r)) / 2.0
+        res[prec] = {
+            "pot_err_raw": float(max(np.abs(f - f_r).max(), np.abs(g - g_r).max()) / scale),
+            "pot_err_shift_removed": float(max(np.abs(f - shift - f_r).max(),
+                                               np.abs(g + shift - g_r).max()) / scale),
+            "constant_shift": float(shift),
+            "loss_rel_err": abs(loss - loss_r) / abs(loss_r),
+            "l1_error_at_checks": [float(x) for x in hist[4::5]],
+        }
+    line = {"metric": "fp32 vs fp64 drift, low-eps long run", "supplementary": True,
+            "value": max(r["pot_err_raw"] for r in res.values()),
+            "unit": "relative L-inf potential error after the run (max over precisions)",
+            "results": res, "oracle_l1_error_at_checks": [float(x) for x in hist_r[4::5]],
+            "fp32_resolution_of_l1_error": 4.0 * float(np.spacing(np.float32(scale))) / eps,
+            "oracle_seconds": t_oracle, "oracle_cores": oracle.num_threads(),
+            "config": {"workload": "unif01 2-D clouds, n=m=1000, uniform weights", "eps": eps,
+                       "iters": iters, "check_every": c, "seed": 4242}}
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -581,6 +721,10 @@ def main():
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.drift:
+        run_drift(args)
+    elif args.tol is not None:
+        run_convergence(args)
     elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":
         run_other_workload(args)
     else:

@@ -135,6 +135,35 @@ int flashot_sinkhorn_solve(const float *X, const float *Y, const float *a, const
                            int n_stages, int iters_per_stage, int flags, float *f, float *g,
                            double *loss, void *ws, size_t ws_bytes, flashot_stream_t stream);
 
+/*
+ * Convergence-driven alternating solve at one eps (the review's "Strengths": the low-eps
+ * regime run to a marginal tolerance; its "Summary": the fused f^/g^ updates). Iteration
+ * k = 1, 2, ... is f = F(g), then g = G(f), from g = 0. After a g-update the column sums of
+ * the plan equal b, so an iterate's error is its row-marginal L1 error
+ *     err = sum_i |sum_j P_ij - a_i| = sum_i a_i |exp((f_i - F(g)_i) / eps) - 1|,
+ * which the f-update of iteration k yields for iterate k-1 inside its LSE combine (no
+ * extra pass over the points). On check iterations (k >= 2, k % check_every == 0) the
+ * error is reduced in fp64 on the device and read back (this SYNCHRONISES `stream`), and
+ * the solve stops after iteration k if err < tol; otherwise after max_iters iterations.
+ * The returned iterate's error is at most the reported one (marginal errors of Sinkhorn
+ * iterates do not increase).
+ *   tol >= 0 (0: never stop early); max_iters >= 1; check_every >= 1.
+ *   iters_done: HOST int, iterations run. err: HOST double or NULL, the last measured
+ *   error (-1 if none). err_hist: HOST array of max_iters / check_every doubles or NULL;
+ *   entry k / check_every - 1 receives the error measured at check iteration k.
+ *   loss: device double or NULL, <a, f> + <b, g> of the returned iterate.
+ * flags: a precision and optionally FLASHOT_REUSE_PACK; anything else returns
+ * FLASHOT_ERR_NOT_IMPLEMENTED. The error is formed from fp32 potentials, so it cannot
+ * resolve much below ~1e-6 * max|f| / eps (the fp32 spacing of f, relative to eps).
+ * Returns FLASHOT_ERR_DEVICE_TIMEOUT (and stops) if a kernel gave up a bounded wait.
+ */
+int flashot_sinkhorn_solve_tol(const float *X, const float *Y, const float *a,
+                               const float *b, int64_t n, int64_t m, int64_t d, float eps,
+                               double tol, int max_iters, int check_every, int flags,
+                               float *f, float *g, double *loss, int *iters_done,
+                               double *err, double *err_hist, void *ws, size_t ws_bytes,
+                               flashot_stream_t stream);
+
 /* One f-update (review "Summary": the f^ update): f = F(g). Reads g (m), writes f (n). */
 int flashot_sinkhorn_step_f(const float *X, const float *Y, const float *b, const float *g,
                             int64_t n, int64_t m, int64_t d, float eps, int flags, float *f,

@@ -24,7 +24,7 @@ __all__ = [
     "Workspace", "workspace_bytes", "sinkhorn_solve", "sinkhorn_step_f", "sinkhorn_step_g",
     "dual_loss", "transport_apply", "transport_hadamard_xy", "ot_grad_x", "workspace_status",
     "FlashotError", "library", "version", "launch_count", "KernelTimer",
-    "sinkhorn_divergence",
+    "sinkhorn_divergence", "sinkhorn_solve_tol",
 ]
 
 
@@ -157,6 +157,43 @@ def sinkhorn_solve(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] =
         _dev_ptr(loss, "loss", (), dtype=torch.float64), ws.ptr, ws.nbytes, _stream())
     _binding.check(st, "flashot_sinkhorn_solve")
     return f, g, loss
+
+
+def sinkhorn_solve_tol(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] = None,
+                       b: Optional[torch.Tensor] = None, eps: float = 0.1, tol: float = 1e-4,
+                       max_iters: int = 1000, check_every: int = 10, *,
+                       precision: str = "auto", f_out: Optional[torch.Tensor] = None,
+                       g_out: Optional[torch.Tensor] = None,
+                       loss_out: Optional[torch.Tensor] = None,
+                       workspace: Optional[Workspace] = None, reuse_pack: bool = False):
+    """Alternating solve from g = 0 that stops after the first check iteration (every
+    ``check_every``) at which the row-marginal L1 error, measured inside the f-update, is
+    below ``tol``. Synchronises the current stream at every check. Returns
+    (f, g, loss, iters_done, err, err_history) with err the last measured error (-1 if
+    none) and err_history a list of the errors measured at each check."""
+    n, m, d = _sizes(X, Y)
+    if max_iters < 1 or check_every < 1:
+        raise ValueError("max_iters and check_every must be >= 1")
+    lib = library()
+    f = f_out if f_out is not None else torch.empty(n, dtype=torch.float32, device=X.device)
+    g = g_out if g_out is not None else torch.empty(m, dtype=torch.float32, device=X.device)
+    loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float64,
+                                                             device=X.device)
+    ws = _ws(workspace, workspace_bytes(n, m, d, 0, precision))
+    done = ctypes.c_int(0)
+    err = ctypes.c_double(-1.0)
+    n_hist = max(max_iters // check_every, 1)
+    hist = (ctypes.c_double * n_hist)(*([float("nan")] * n_hist))
+    st = lib.flashot_sinkhorn_solve_tol(
+        _dev_ptr(X, "X", (n, d)), _dev_ptr(Y, "Y", (m, d)),
+        _dev_ptr(a, "a", (n,), optional=True), _dev_ptr(b, "b", (m,), optional=True),
+        n, m, d, float(eps), float(tol), int(max_iters), int(check_every),
+        _flags(precision, reuse=reuse_pack), _dev_ptr(f, "f", (n,)), _dev_ptr(g, "g", (m,)),
+        _dev_ptr(loss, "loss", (), dtype=torch.float64), ctypes.byref(done),
+        ctypes.byref(err), hist, ws.ptr, ws.nbytes, _stream())
+    _binding.check(st, "flashot_sinkhorn_solve_tol")
+    history = list(hist)[: done.value // check_every]
+    return f, g, loss, int(done.value), float(err.value), history
 
 
 def sinkhorn_step_f(X, Y, g, eps: float, b=None, *, precision="auto", out=None,

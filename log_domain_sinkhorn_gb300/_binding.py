@@ -59,6 +59,11 @@ SIGNATURES = {
     "flashot_sinkhorn_solve": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.POINTER(ctypes.c_float),
         ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "flashot_sinkhorn_solve_tol": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_double,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, ctypes.POINTER(ctypes.c_int),
+        ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), _vp, ctypes.c_size_t,
+        _vp]),
     "flashot_sinkhorn_step_f": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int, _vp, _vp,
         ctypes.c_size_t, _vp]),

@@ -286,8 +286,10 @@ int launch_bias(const Ctx& c, const float* pot, bool x_side, float eps) {
 // F-type (x_rows = true): rows X, columns Y, column bias biasF; writes out_pot (= f),
 // the next pass's bias biasG (at eps_next), and optionally the row LSE (base 2).
 // G-type: the same with X and Y exchanged.
+// err_rows: see lse_combine_kernel (the convergence check; NULL otherwise).
 int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* out_pot,
-                 bool write_next_bias, float* out_lse2, bool average = false) {
+                 bool write_next_bias, float* out_lse2, bool average = false,
+                 float* err_rows = nullptr) {
   const Geometry& g = c.g;
   const int64_t n_rows = x_rows ? g.n : g.m;
   const int64_t rows_pad = x_rows ? g.n_pad : g.m_pad;
@@ -353,7 +355,7 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
         partial, split, rows_pad, n_rows, rows_pad, c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
         c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
         write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr, out_lse2,
-      average ? 1 : 0);
+        average ? 1 : 0, c.at<float>(x_rows ? c.L.wa : c.L.wb), err_rows);
   }
   return launch_check();
 }
@@ -608,6 +610,72 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
     }
   }
   }
+  if (loss) {
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      dual_loss_kernel<<<1, 1024, 0, c.st>>>(c.at<float>(c.L.wa), f, n, c.at<float>(c.L.wb), g, m,
+                                             loss);
+    }
+    if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  }
+  return FLASHOT_OK;
+}
+
+int flashot_sinkhorn_solve_tol(const float* X, const float* Y, const float* a, const float* b,
+                               int64_t n, int64_t m, int64_t d, float eps, double tol,
+                               int max_iters, int check_every, int flags, float* f, float* g,
+                               double* loss, int* iters_done, double* err, double* err_hist,
+                               void* ws, size_t ws_bytes, flashot_stream_t stream) {
+  if (!eps_ok(eps) || !std::isfinite(tol) || tol < 0.0 || max_iters < 1 || check_every < 1 ||
+      iters_done == nullptr)
+    return FLASHOT_ERR_INVALID_ARG;
+  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  Ctx c;
+  int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !opt_device_ptr(loss))
+    return FLASHOT_ERR_INVALID_ARG;
+  *iters_done = 0;
+  if (err) *err = -1.0;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, nullptr, false, eps)) != FLASHOT_OK) return rc;
+  float* err_rows = c.at<float>(c.L.lse2);
+  double* err_dev = c.at<double>(c.L.loss);
+  int k = 1;
+  for (; k <= max_iters; ++k) {
+    // Iteration k measures, inside its f-update, the row-marginal error of iterate k-1.
+    const bool check = k >= 2 && k % check_every == 0;
+    if ((rc = run_lse_pass(c, true, eps, eps, f, true, nullptr, false,
+                           check ? err_rows : nullptr)) != FLASHOT_OK)
+      return rc;
+    if (check) {
+      {
+        TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+        sum_rows_kernel<<<1, 1024, 0, c.st>>>(err_rows, n, err_dev);
+      }
+      if ((rc = launch_check()) != FLASHOT_OK) return rc;
+    }
+    if ((rc = run_lse_pass(c, false, eps, eps, g, true, nullptr)) != FLASHOT_OK) return rc;
+    if (check) {
+      double e_host = 0.0;
+      unsigned word = 0;
+      cudaError_t e = cudaMemcpyAsync(&e_host, err_dev, sizeof(double), cudaMemcpyDeviceToHost,
+                                      c.st);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&word, c.at<unsigned>(c.L.status), sizeof(word),
+                            cudaMemcpyDeviceToHost, c.st);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
+      if (e != cudaSuccess) return cuda_fail(e);
+      // A kernel that gave up a bounded wait left garbage: stop (the word stays set for
+      // flashot_workspace_status).
+      if (word != 0) return FLASHOT_ERR_DEVICE_TIMEOUT;
+      if (err) *err = e_host;
+      if (err_hist) err_hist[k / check_every - 1] = e_host;
+      if (e_host < tol) break;
+    }
+  }
+  *iters_done = std::min(k, max_iters);
   if (loss) {
     {
       TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);

@@ -66,15 +66,22 @@ __global__ void bias_kernel(const float* __restrict__ pot, const float* __restri
 //   next_bias_i = lw2_i - L_i * (eps / eps_next)   (= (pot_i - norm_i) log2e/eps_next + lw2_i)
 // next_bias is the bias the following pass (the other side's update at eps_next) needs;
 // its padding entries [rows, rows_pad) are set to -inf so padded points carry no mass.
+// err_rows != NULL (the convergence check): before out_pot is overwritten, the row's share
+// of the L1 marginal error of the previous iterate,
+//   err_rows_i = w_i |exp((old_i - new_i) / eps) - 1|  (= |sum_j P_ij(old) - w_i|),
+// is written, with 0 for padding rows.
 __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo split,
                                    int64_t ld, int64_t rows, int64_t rows_pad,
                                    const float* __restrict__ norms, float eps,
                                    const float* __restrict__ lw2, float eps_ratio,
                                    float* __restrict__ out_pot, float* __restrict__ next_bias,
-                                   float* __restrict__ out_lse2, int average) {
+                                   float* __restrict__ out_lse2, int average,
+                                   const float* __restrict__ err_w = nullptr,
+                                   float* __restrict__ err_rows = nullptr) {
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= rows) {
     if (i < rows_pad && next_bias) next_bias[i] = neg_inf();
+    if (i < rows_pad && err_rows) err_rows[i] = 0.0f;
     return;
   }
   int n_splits = split.n_splits;
@@ -95,6 +102,10 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
   const float fresh = norms[i] - eps * kLn2 * L;
   // Symmetric schedule: the new potential is the mean of the previous one and the update.
   const float pot = average ? 0.5f * (out_pot[i] + fresh) : fresh;
+  if (err_rows) {
+    const float w = err_w[i];
+    err_rows[i] = w > 0.0f ? w * fabsf(expm1f((out_pot[i] - fresh) / eps)) : 0.0f;
+  }
   if (out_pot) out_pot[i] = pot;
   if (next_bias) next_bias[i] = lw2[i] - L * eps_ratio;
   if (out_lse2) out_lse2[i] = L;
@@ -118,6 +129,24 @@ dual_loss_kernel(const float* __restrict__ wa, const float* __restrict__ f, int6
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (threadIdx.x == 0) *loss = s;
+  }
+}
+
+// out = sum_i v_i in fp64; one block, deterministic order (the convergence check's error).
+__global__ void __launch_bounds__(1024)
+sum_rows_kernel(const float* __restrict__ v, int64_t rows, double* __restrict__ out) {
+  __shared__ double red[32];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) s += (double)v[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    s = (threadIdx.x < (blockDim.x >> 5)) ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) *out = s;
   }
 }
 
