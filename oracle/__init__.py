@@ -6,7 +6,9 @@ binding) never imports, links or executes anything here, and this package import
 nothing from the product path.
 
 The arithmetic lives in ``sinkhorn_oracle.c`` (plain loops, fp64, OpenMP over output
-rows); this module compiles it with gcc on first use and wraps it with numpy. All
+rows); this module compiles it with gcc on first use and wraps it with numpy. The dense
+Hessian-vector product (``hvp_x``) is plain numpy: it builds the second-derivative blocks
+as dense arrays and uses a Moore-Penrose pseudo-inverse (small problems only). All
 inputs are promoted to fp64 before the call (fp32 -> fp64 is exact).
 
 Parity status of each function (what pins it, in tests/test_oracle_pins.py):
@@ -24,6 +26,9 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   solve_symmetric            X = Y gives f == g at every iteration; same converged loss
                              as the alternating schedule.
   sinkhorn_divergence        S(a, a) = 0; S >= 0; eps -> inf limit |mean x - mean y|^2.
+  hvp_x                      central finite differences of the converged gradient;
+                             uniform translation V = 1 t gives 2 r_i t exactly;
+                             eps -> inf limit 2 a_i v_i; Hessian symmetry.
   solve_tol                  with tol = 0 it equals solve; each reported error equals the
                              row-marginal L1 error recomputed from the plan by
                              marginals(); it stops at the first check below tol; the
@@ -273,3 +278,46 @@ def marginals(X, Y, a, b, f, g, eps):
     _lib().oracle_marginals(_p(X), _p(Y), _p(a), _p(b), _p(f), _p(g), n, m, d, float(eps),
                             _p(r), _p(c))
     return r, c
+
+
+def hvp_x(X, Y, a, b, f, g, eps, V):
+    """Hessian-vector product of the entropic OT loss w.r.t. X, dense fp64 reference with a
+    Moore-Penrose pseudo-inverse (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU,
+    SAI replication review, "Summary" (iii): the HVP oracle through a Schur solve; "Strengths":
+    parity against a dense Moore-Penrose HVP). Small n, m only.
+
+    With the Lagrangian L(X, f, g) = <a,f> + <b,g> - eps sum_ij (P_ij - a_i b_j) and
+    P_ij = a_i b_j exp((f_i + g_j - |x_i - y_j|^2)/eps), its blocks at the given (f, g) are
+    (D_ij = x_i - y_j, r = P 1, c = P^T 1):
+      L_XX  block i:      2 r_i I - (4/eps) sum_j P_ij D_ij D_ij^T
+      L_Xf  (i, i):       (2/eps) sum_j P_ij D_ij
+      L_Xg  (i, j):       (2/eps) P_ij D_ij
+      L_phiphi:           -(1/eps) K,  K = [[diag r, P], [P^T, diag c]]
+    The potentials move with X by d(phi) = -L_phiphi^+ L_phiX V (implicit function theorem,
+    the pseudo-inverse fixing the gauge direction (1, -1), which L_Xphi annihilates), so
+      H V = L_XX V + L_Xphi (eps K^+ L_phiX V).
+    At optimal potentials this is the Hessian of OT_eps(X, Y) applied to V (n x d)."""
+    X, Y, a, b, f, g, V = map(_f64, (X, Y, a, b, f, g, V))
+    n, d = X.shape
+    m = Y.shape[0]
+    D = X[:, None, :] - Y[None, :, :]                      # n x m x d
+    C = (D * D).sum(-1)
+    P = a[:, None] * b[None, :] * np.exp((f[:, None] + g[None, :] - C) / eps)
+    r = P.sum(1)
+    c = P.sum(0)
+    nd = n * d
+    Lxx = np.zeros((nd, nd))
+    for i in range(n):
+        blk = 2.0 * r[i] * np.eye(d)
+        for j in range(m):
+            blk -= (4.0 / eps) * P[i, j] * np.outer(D[i, j], D[i, j])
+        Lxx[i * d:(i + 1) * d, i * d:(i + 1) * d] = blk
+    B = np.zeros((nd, n + m))
+    for i in range(n):
+        for j in range(m):
+            B[i * d:(i + 1) * d, i] += (2.0 / eps) * P[i, j] * D[i, j]
+            B[i * d:(i + 1) * d, n + j] = (2.0 / eps) * P[i, j] * D[i, j]
+    K = np.block([[np.diag(r), P], [P.T, np.diag(c)]])
+    v = V.reshape(nd)
+    dphi = eps * (np.linalg.pinv(K, rcond=1e-13, hermitian=True) @ (B.T @ v))
+    return (Lxx @ v + B @ dphi).reshape(n, d)

@@ -1,6 +1,6 @@
 """Planted-mistake check for the oracle pins (CPU only).
 
-Each case copies the oracle source into a temporary directory, plants one plausible
+Each case copies the oracle sources into a temporary directory, plants one plausible
 mistake (a dropped term, a wrong sign or factor, a transposed index, a swapped update
 order), rebuilds it there and runs the pin suite against the copy. Every mutant must
 fail at least one pin; the real oracle is never modified.
@@ -38,16 +38,27 @@ MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
+# Mistakes planted in the dense Hessian-vector product (oracle/__init__.py).
+PY_MUTATIONS = {
+    "hvp_drops_potential_response": ("return (Lxx @ v + B @ dphi)", "return (Lxx @ v + 0.0 * (B @ dphi))"),
+    "hvp_outer_product_sign": ("blk -= (4.0 / eps)", "blk += (4.0 / eps)"),
+    "hvp_drops_eps_in_response": ("dphi = eps * (", "dphi = ("),
+    "hvp_self_term_sign": ("B[i * d:(i + 1) * d, i] += (2.0 / eps)", "B[i * d:(i + 1) * d, i] -= (2.0 / eps)"),
+}
+_TARGETS = {**{k: ("sinkhorn_oracle.c", v) for k, v in MUTATIONS.items()},
+            **{k: ("__init__.py", v) for k, v in PY_MUTATIONS.items()}}
+
+
+@pytest.mark.parametrize("name", sorted(_TARGETS))
 def test_pins_catch_planted_mistake(name, tmp_path):
-    old, new = MUTATIONS[name]
-    src = open(os.path.join(ROOT, "oracle", "sinkhorn_oracle.c")).read()
+    fname, (old, new) = _TARGETS[name]
+    src = open(os.path.join(ROOT, "oracle", fname)).read()
     assert old in src, f"mutation site for {name} no longer exists"
     ign = shutil.ignore_patterns("_build", "__pycache__")
     for sub in ("oracle", "workloads", "tests"):
         shutil.copytree(os.path.join(ROOT, sub), tmp_path / sub, ignore=ign)
     shutil.copy(os.path.join(ROOT, "pytest.ini"), tmp_path)
-    (tmp_path / "oracle" / "sinkhorn_oracle.c").write_text(src.replace(old, new, 1))
+    (tmp_path / "oracle" / fname).write_text(src.replace(old, new, 1))
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-q", "-x"],
                        cwd=tmp_path, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -515,3 +515,71 @@ def test_solve_tol_errors_are_nonincreasing_and_stop_at_first_check_below_tol():
         assert loss == loss2
         # the returned iterate is at least as good as the measured one
         assert _row_error(X, Y, a, b, f, g, eps) <= err * (1 + 1e-9)
+
+
+# ---------------------------------------------------------------------------------
+# Hessian-vector product w.r.t. X (dense Moore-Penrose reference)
+# ---------------------------------------------------------------------------------
+
+def _converged(X, Y, a, b, eps):
+    f, g, _, done, err = oracle.solve_tol(X, Y, a, b, eps, 1e-15, 40000, 10)
+    assert 0 <= err < 1e-13
+    return f, g
+
+
+@pytest.mark.parametrize("eps,d", [(0.5, 2), (0.2, 3), (2.0, 1)])
+def test_hvp_matches_finite_difference_of_converged_gradient(eps, d):
+    """H V = d/dt grad_X OT(X + t V) at t = 0, by central differences of the gradient at
+    re-converged potentials (the gradient itself is pinned by finite differences of the
+    loss)."""
+    rng = np.random.default_rng(int(eps * 10) + d)
+    n, m = 6, 8
+    X = rng.normal(size=(n, d))
+    Y = rng.normal(size=(m, d)) * 0.8 + 0.3
+    a = rng.exponential(size=n); a /= a.sum()
+    b = rng.exponential(size=m); b /= b.sum()
+    V = rng.normal(size=(n, d))
+    f, g = _converged(X, Y, a, b, eps)
+    H = oracle.hvp_x(X, Y, a, b, f, g, eps, V)
+
+    def grad(Xp):
+        fp, gp = _converged(Xp, Y, a, b, eps)
+        return oracle.grad_x(Xp, Y, a, b, gp, eps)
+    h = 1e-5
+    fd = (grad(X + h * V) - grad(X - h * V)) / (2 * h)
+    assert np.abs(H - fd).max() <= 1e-7 * np.abs(fd).max()
+
+
+def test_hvp_uniform_translation_closed_form():
+    """Moving every x_i by t changes each cost by 2t.(x_i - y_j) + |t|^2, which the potentials
+    absorb exactly; the Hessian along V = 1 t is therefore 2 r_i t (r = P 1), at any
+    potentials (2 a_i t at the optimum)."""
+    X, Y, a, b, f, g = _random_instance(seed=81, n=9, m=7, d=3)
+    t = np.array([0.4, -1.1, 0.25])
+    V = np.tile(t, (9, 1))
+    eps = 0.3
+    r, _ = oracle.marginals(X, Y, a, b, f, g, eps)
+    H = oracle.hvp_x(X, Y, a, b, f, g, eps, V)
+    # (random potentials make K ill-conditioned: the pseudo-inverse costs a few digits)
+    np.testing.assert_allclose(H, 2.0 * r[:, None] * t[None, :], rtol=1e-8, atol=1e-12)
+
+
+def test_hvp_large_eps_limit_and_symmetry():
+    """eps -> inf: P -> a b^T and the loss tends to sum_ij a_i b_j |x_i - y_j|^2, whose
+    Hessian is 2 diag(a) (x) I. And <V1, H V2> = <V2, H V1>."""
+    rng = np.random.default_rng(82)
+    n, m, d = 5, 6, 2
+    X = rng.normal(size=(n, d)); Y = rng.normal(size=(m, d))
+    a = rng.exponential(size=n); a /= a.sum()
+    b = rng.exponential(size=m); b /= b.sum()
+    V = rng.normal(size=(n, d))
+    eps = 1e6
+    f, g = _converged(X, Y, a, b, eps)
+    H = oracle.hvp_x(X, Y, a, b, f, g, eps, V)
+    np.testing.assert_allclose(H, 2.0 * a[:, None] * V, rtol=1e-4, atol=1e-6)
+    eps = 0.4
+    f, g = _converged(X, Y, a, b, eps)
+    V2 = rng.normal(size=(n, d))
+    s12 = float((V * oracle.hvp_x(X, Y, a, b, f, g, eps, V2)).sum())
+    s21 = float((V2 * oracle.hvp_x(X, Y, a, b, f, g, eps, V)).sum())
+    assert s12 == pytest.approx(s21, rel=1e-10)
