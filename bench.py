@@ -69,6 +69,9 @@ def parse_args():
     p.add_argument("--drift", action="store_true",
                    help="supplementary line: fp32 GPU vs fp64 oracle drift over a long "
                         "low-eps run (n = m = 1000, d = 2, eps = 0.001, 3000 iterations)")
+    p.add_argument("--hvp", action="store_true",
+                   help="supplementary line: Hessian-vector product of the OT loss w.r.t. X "
+                        "on n = m = 50000 points in Uniform[0,1]^3 (eps = 0.05, CG to 1e-6)")
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -505,6 +508,80 @@ def run_drift(args):
     print(json.dumps(line), flush=True)
 
 
+def run_hvp(args):
+    """Supplementary line: the streaming Hessian-vector product (fp32 CUDA-core passes, CG
+    Schur solve to a relative residual of 1e-6) on n = m = 50000 points in Uniform[0,1]^3,
+    uniform weights, eps = 0.05, at potentials from a convergence-driven solve (L1 marginal
+    error < 1e-5), V ~ N(0, 1). One step = one H V."""
+    import numpy as np
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    from workloads import make_problem
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    n = args.n or 50000
+    d, eps = 3, float(args.eps if args.eps is not None else 0.05)
+    pr = make_problem(n, n, d, x_dist="unif01", weights="uniform", seed=5150)
+    X, Y, a, b = _problem_on_device(pr, dev)
+    V = torch.from_numpy(np.random.default_rng(5151).normal(size=(n, d)).astype(np.float32)).to(dev)
+    f, g, _, iters_solve, err, _ = lds.sinkhorn_solve_tol(X, Y, a, b, eps, 1e-5, 5000, 10,
+                                                          precision="fp32")
+    ws = lds.Workspace(int(lds.library().flashot_hvp_workspace_bytes(n, n, d, 1)))
+    out = torch.empty((n, d), device=dev)
+    res = {}
+
+    def step():
+        res["r"] = lds.ot_hvp_x(X, Y, f, g, eps, V, a, b, cg_tol=1e-6, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    timer = lds.KernelTimer(cap=args.steps * 4000).start()
+    launches0 = lds.launch_count()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    launches = lds.launch_count() - launches0
+    n_ws, ms_ws = timer.read(lds.KernelTimer.WSUM)
+    n_ot, ms_ot = timer.read(lds.KernelTimer.OTHER)
+    timer.stop()
+    if lds.workspace_status(ws) != 0:
+        raise RuntimeError("device timeout reported")
+    _, cg_iters, rel = res["r"]
+    ms = statistics.median(times)
+    peaks, _ = load_peaks()
+    clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    nm = float(n) * float(n)
+    passes = 2 * cg_iters + 5  # CG: P p and P^T t; plus [PY|r], [P^T V|P^T s|c], T, rhs, final
+    pass_avg = ms_ws / max(n_ws, 1) / 1e3
+    line = {"metric": "Hessian-vector products of the OT loss w.r.t. X", "supplementary": True,
+            "value": 1e3 / ms, "unit": "HVPs/s", "ms_per_hvp": ms, "cg_iterations": cg_iters,
+            "cg_rel_residual": rel, "streaming_passes_per_hvp": passes,
+            "ms_per_cg_iteration": ms / max(cg_iters, 1),
+            "kernels_ms_per_hvp": {"streaming_passes": ms_ws / args.steps,
+                                   "other": ms_ot / args.steps},
+            "roofline": {"bound": "alu (SFU ex2)", "kernel": "wsum_fma_small (streaming pass)",
+                         "achieved": nm / pass_avg / 1e9,
+                         "peak": N_SMS * SFU_EX2_PER_SM_CLK * clk / 1e9,
+                         "unit": "G ex2/s", "avg_pass_ms": pass_avg * 1e3},
+            "steps": args.steps, "warmup": args.warmup, "dtype": "fp32",
+            "gpu_launches": int(launches),
+            "config": {"workload": "hvp50k_d3: n=m=%d, d=3, Uniform[0,1]^3, uniform weights" % n,
+                       "eps": eps, "potentials": f"solve to L1 marginal error {err:.2e} "
+                                                 f"({iters_solve} iterations)",
+                       "V": "N(0,1), seed 5151", "cg_tol": 1e-6}}
+    line["roofline"]["frac"] = line["roofline"]["achieved"] / line["roofline"]["peak"]
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -723,6 +800,8 @@ def main():
         run_reference(args)
     elif args.drift:
         run_drift(args)
+    elif args.hvp:
+        run_hvp(args)
     elif args.tol is not None:
         run_convergence(args)
     elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":

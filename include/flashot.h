@@ -224,6 +224,36 @@ int flashot_ot_grad_x(const float *X, const float *Y, const float *a, const floa
                       const float *g, int64_t n, int64_t m, int64_t d, float eps, float *grad,
                       int flags, void *ws, size_t ws_bytes, flashot_stream_t stream);
 
+/*
+ * Hessian-vector product of the OT loss w.r.t. X (the review's "Summary" (iii): a streaming
+ * HVP oracle for O((n + m) d)-memory Newton-CG, through a Schur solve with streaming P and
+ * P^T products; "Strengths": parity against a dense Moore-Penrose HVP).
+ * At the potentials (f, g), with P_ij = a_i b_j exp((f_i + g_j - |x_i - y_j|^2)/eps),
+ * r = P 1 and c = P^T 1, the Lagrangian L = <a,f> + <b,g> - eps sum_ij (P_ij - a_i b_j) has
+ *   L_XX   block i: 2 r_i I - (4/eps) sum_j P_ij (x_i - y_j)(x_i - y_j)^T,
+ *   L_Xf (i, i) = (2/eps) sum_j P_ij (x_i - y_j),  L_Xg (i, j) = (2/eps) P_ij (x_i - y_j),
+ *   L_phiphi = -K/eps,  K = [[diag r, P], [P^T, diag c]],
+ * and out = H V = L_XX V + L_Xphi (eps K^+ L_phiX V) (the potentials' response by the
+ * implicit function theorem; K^+ fixes the gauge direction, which L_Xphi annihilates). At
+ * optimal potentials this is the Hessian of OT_eps(X, Y) applied to V.
+ * K (u, z) = w is solved by conjugate gradients on the Schur complement
+ * S = diag(c) - P^T diag(1/r) P with preconditioner diag(c), stopping when the residual
+ * falls below cg_tol times the initial one (checked after every iteration, which
+ * SYNCHRONISES `stream`) or after cg_max_iters iterations. Each CG iteration is two
+ * streaming passes (P p and P^T t); the rest is five more passes and O((n + m) d) work.
+ *   V, out: n x d device floats (out must not alias V). f (n), g (m): device floats.
+ *   cg_iters, cg_rel_residual: HOST pointers or NULL (iterations run; final residual ratio).
+ *   flags: FLASHOT_PREC_AUTO or FLASHOT_PREC_FP32 (the passes run on fp32 CUDA cores),
+ *   optionally FLASHOT_REUSE_PACK; anything else returns FLASHOT_ERR_NOT_IMPLEMENTED.
+ *   ws: at least flashot_hvp_workspace_bytes(n, m, d, flags) bytes.
+ */
+size_t flashot_hvp_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags);
+int flashot_ot_hvp_x(const float *X, const float *Y, const float *a, const float *b,
+                     const float *f, const float *g, int64_t n, int64_t m, int64_t d,
+                     float eps, const float *V, float *out, double cg_tol, int cg_max_iters,
+                     int flags, int *cg_iters, double *cg_rel_residual, void *ws,
+                     size_t ws_bytes, flashot_stream_t stream);
+
 /* ---- allocation-free variant -------------------------------------------------------- */
 /*
  * The paper has no counterpart to this entry point; it exists for callers that cannot give

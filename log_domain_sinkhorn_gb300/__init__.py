@@ -24,7 +24,7 @@ __all__ = [
     "Workspace", "workspace_bytes", "sinkhorn_solve", "sinkhorn_step_f", "sinkhorn_step_g",
     "dual_loss", "transport_apply", "transport_hadamard_xy", "ot_grad_x", "workspace_status",
     "FlashotError", "library", "version", "launch_count", "KernelTimer",
-    "sinkhorn_divergence", "sinkhorn_solve_tol",
+    "sinkhorn_divergence", "sinkhorn_solve_tol", "ot_hvp_x",
 ]
 
 
@@ -291,6 +291,33 @@ def ot_grad_x(X, Y, g, eps: float, a=None, b=None, *, precision="auto", out=None
         _flags(precision, reuse=reuse_pack), ws.ptr, ws.nbytes, _stream())
     _binding.check(st, "flashot_ot_grad_x")
     return grad
+
+
+def ot_hvp_x(X, Y, f, g, eps: float, V, a=None, b=None, *, cg_tol: float = 1e-6,
+             cg_max_iters: int = 1000, out=None, workspace=None, reuse_pack=False):
+    """Hessian of the OT loss w.r.t. X, applied to V (n x d), at the potentials (f, g)
+    (optimal potentials give the Hessian of OT_eps); fp32 CUDA-core passes and a CG Schur
+    solve. Synchronises the current stream once per CG iteration. Returns
+    (HV, cg_iterations, cg_relative_residual)."""
+    n, m, d = _sizes(X, Y)
+    lib = library()
+    nb = int(lib.flashot_hvp_workspace_bytes(n, m, d, _binding.PREC_FP32))
+    if nb == 0:
+        raise ValueError(f"invalid sizes n={n} m={m} d={d}")
+    ws = _ws(workspace, nb)
+    o = out if out is not None else torch.empty((n, d), dtype=torch.float32, device=X.device)
+    iters = ctypes.c_int(0)
+    rel = ctypes.c_double(0.0)
+    flags = _binding.PREC_FP32 | (_binding.REUSE_PACK if reuse_pack else 0)
+    st = lib.flashot_ot_hvp_x(
+        _dev_ptr(X, "X", (n, d)), _dev_ptr(Y, "Y", (m, d)),
+        _dev_ptr(a, "a", (n,), optional=True), _dev_ptr(b, "b", (m,), optional=True),
+        _dev_ptr(f, "f", (n,)), _dev_ptr(g, "g", (m,)), n, m, d, float(eps),
+        _dev_ptr(V, "V", (n, d)), _dev_ptr(o, "out", (n, d)), float(cg_tol),
+        int(cg_max_iters), flags, ctypes.byref(iters), ctypes.byref(rel), ws.ptr, ws.nbytes,
+        _stream())
+    _binding.check(st, "flashot_ot_hvp_x")
+    return o, int(iters.value), float(rel.value)
 
 
 def workspace_status(workspace: Workspace) -> int:

@@ -83,6 +83,11 @@ SIGNATURES = {
     "flashot_transport_hadamard_xy": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, _vp,
         ctypes.c_int, _vp, ctypes.c_size_t, _vp]),
+    "flashot_hvp_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64, ctypes.c_int]),
+    "flashot_ot_hvp_x": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, _vp, _vp,
+        ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+        ctypes.POINTER(ctypes.c_double), _vp, ctypes.c_size_t, _vp]),
     "flashot_sinkhorn_step_f_noalloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int, _vp, _vp]),
     "flashot_ot_grad_x": (ctypes.c_int, [

@@ -29,8 +29,10 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 // What a weighted-sum pass produces: transport application P V, the barycentric gradient,
-// or the Hadamard-weighted transport (P .* X Y^T) 1.
-enum WsumMode : int { kWsumApply = 0, kWsumGrad = 1, kWsumHadamard = 2 };
+// the Hadamard-weighted transport (P .* X Y^T) 1, or the Hadamard-weighted transport
+// matrix application (P .* U Q^T) Q (weights P_ij <u_i, q_j> applied to the column points;
+// the curvature term of the Hessian-vector product).
+enum WsumMode : int { kWsumApply = 0, kWsumGrad = 1, kWsumHadamard = 2, kWsumHessT = 3 };
 
 // Status bits written into the workspace status word by kernels that give up a wait.
 constexpr unsigned kErrTimeout = 1u;

@@ -14,6 +14,7 @@
 #include "flashot.h"
 #include "common.cuh"
 #include "fma_kernels.cuh"
+#include "hvp_kernels.cuh"
 #include "prep_kernels.cuh"
 #include "small_solve.h"
 #include "tc_api.h"
@@ -360,10 +361,12 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
   return launch_check();
 }
 
-// ---- weighted-sum passes (apply, grad, Hadamard) -----------------------------------------
+// ---- weighted-sum passes (apply, grad, Hadamard, Hessian curvature) ----------------------
 // rows on the X side unless `transpose`; rowBias / colBias as prepared by the caller.
+// rowU (kWsumHessT only): the packed fp32 rows u_i (same layout as the packed row points).
 int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float* V, int64_t ldv,
-                  int64_t k, const float* X, const float* Y, float* out, int64_t ldo) {
+                  int64_t k, const float* X, const float* Y, float* out, int64_t ldo,
+                  const float* rowU = nullptr) {
   const Geometry& g = c.g;
   const bool x_rows = !transpose;
   const int64_t n_rows = x_rows ? g.n : g.m;
@@ -374,6 +377,7 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
   const float* rowW = c.at<float>(x_rows ? c.L.wa : c.L.wb);
   const float kappa = 2.0f * kLog2e / eps;
   if (g.prec != FLASHOT_PREC_FP32) {
+    if (mode == kWsumHessT) return FLASHOT_ERR_NOT_IMPLEMENTED;
     if (mode == kWsumGrad) {  // right operand of the second contraction: the column points
       V = x_rows ? Y : X;
       ldv = g.d;
@@ -398,20 +402,26 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
     ldv = g.dpf;
     k = g.d;
   }
+  if (mode == kWsumHessT && rowU == nullptr) return FLASHOT_ERR_INVALID_ARG;
   const int64_t kk = (mode == kWsumHadamard) ? 1 : k;
-  dim3 grid((unsigned)ceil_div(n_rows, kFmaThreads), (unsigned)ceil_div(kk, 32));
+  // One output column (a transport-vector application): a narrow accumulator.
+  const bool narrow = (mode == kWsumApply && k == 1);
+  const int KO = narrow ? 1 : 32;
+  dim3 grid((unsigned)ceil_div(n_rows, kFmaThreads), (unsigned)ceil_div(kk, KO));
   const int n_tiles = (int)(cols_pad / 32);
   TraceScope ts_(FLASHOT_KERNEL_WSUM, c.st);
   if (g.small) {
-#define FLASHOT_WSUM_SMALL(DPV, MODEV)                                                     \
-  wsum_fma_small_kernel<DPV, MODEV><<<grid, kFmaThreads, 0, c.st>>>(                       \
+#define FLASHOT_WSUM_SMALL(DPV, MODEV, KOV)                                                  \
+  wsum_fma_small_kernel<DPV, MODEV, KOV><<<grid, kFmaThreads, 0, c.st>>>(                    \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
-      out, ldo)
-#define FLASHOT_WSUM_MODES(DPV)                                    \
-  case DPV:                                                        \
-    if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply);   \
-    else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad); \
-    else FLASHOT_WSUM_SMALL(DPV, kWsumHadamard);                   \
+      out, ldo, rowU)
+#define FLASHOT_WSUM_MODES(DPV)                                             \
+  case DPV:                                                                 \
+    if (narrow) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 1);                     \
+    else if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 32);   \
+    else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad, 32);     \
+    else if (mode == kWsumHessT) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 32);   \
+    else FLASHOT_WSUM_SMALL(DPV, kWsumHadamard, 32);                        \
     break;
     switch (g.dpf) {
       FLASHOT_WSUM_MODES(4)
@@ -427,16 +437,61 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
 #undef FLASHOT_WSUM_MODES
 #undef FLASHOT_WSUM_SMALL
   } else {
-#define FLASHOT_WSUM_GENERIC(MODEV)                                                           \
-  wsum_fma_generic_kernel<MODEV><<<grid, kFmaThreads, 0, c.st>>>(                             \
+#define FLASHOT_WSUM_GENERIC(MODEV, KOV)                                                      \
+  wsum_fma_generic_kernel<MODEV, KOV><<<grid, kFmaThreads, 0, c.st>>>(                        \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, g.dpf, kappa, V, ldv, k, rowW, X, \
-      g.d, out, ldo)
-    if (mode == kWsumApply) FLASHOT_WSUM_GENERIC(kWsumApply);
-    else if (mode == kWsumGrad) FLASHOT_WSUM_GENERIC(kWsumGrad);
-    else FLASHOT_WSUM_GENERIC(kWsumHadamard);
+      g.d, out, ldo, rowU)
+    if (narrow) FLASHOT_WSUM_GENERIC(kWsumApply, 1);
+    else if (mode == kWsumApply) FLASHOT_WSUM_GENERIC(kWsumApply, 32);
+    else if (mode == kWsumGrad) FLASHOT_WSUM_GENERIC(kWsumGrad, 32);
+    else if (mode == kWsumHessT) FLASHOT_WSUM_GENERIC(kWsumHessT, 32);
+    else FLASHOT_WSUM_GENERIC(kWsumHadamard, 32);
 #undef FLASHOT_WSUM_GENERIC
   }
   return launch_check();
+}
+
+// ---- Hessian-vector product scratch (after the ordinary workspace) ----------------------
+struct HvpLayout {
+  size_t vp, VA, OA, VB, OB, T, wf, t1, PtT, z, res, yv, p, Pp, tn, VD, OD, sc, total;
+};
+
+HvpLayout make_hvp_layout(const Geometry& g, size_t base) {
+  HvpLayout H{};
+  size_t off = base;
+  auto take = [&](size_t floats) {
+    size_t o = off;
+    off = (off + floats * 4 + 255) / 256 * 256;
+    return o;
+  };
+  const size_t n = (size_t)g.n, m = (size_t)g.m, d = (size_t)g.d;
+  H.vp = take((size_t)g.n_pad * g.dpf);
+  H.VA = take(m * (d + 1));
+  H.OA = take(n * (d + 1));
+  H.VB = take(n * (d + 2));
+  H.OB = take(m * (d + 2));
+  H.T = take(n * d);
+  H.wf = take(n);
+  H.t1 = take(n);
+  H.PtT = take(m);
+  H.z = take(m);
+  H.res = take(m);
+  H.yv = take(m);
+  H.p = take(m);
+  H.Pp = take(n);
+  H.tn = take(n);
+  H.VD = take(m * (d + 1));
+  H.OD = take(n * (d + 1));
+  H.sc = take(2 * kHvpScalars);
+  H.total = off + 256;
+  return H;
+}
+
+// The Hessian-vector product runs on the fp32 CUDA-core passes; its geometry.
+bool hvp_geometry(int64_t n, int64_t m, int64_t d, int flags, Geometry* g) {
+  const int p = flags & FLASHOT_PREC_MASK;
+  if (p != FLASHOT_PREC_AUTO && p != FLASHOT_PREC_FP32) return false;
+  return make_geometry(n, m, d, d + 2, FLASHOT_PREC_FP32, g);
 }
 
 // Common prologue of every hot-path entry point.
@@ -685,6 +740,147 @@ int flashot_sinkhorn_solve_tol(const float* X, const float* Y, const float* a, c
     if ((rc = launch_check()) != FLASHOT_OK) return rc;
   }
   return FLASHOT_OK;
+}
+
+size_t flashot_hvp_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags) {
+  Geometry g;
+  if (!hvp_geometry(n, m, d, flags, &g)) return 0;
+  return make_hvp_layout(g, make_layout(g).total).total;
+}
+
+int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float* b,
+                     const float* f, const float* g, int64_t n, int64_t m, int64_t d, float eps,
+                     const float* V, float* out, double cg_tol, int cg_max_iters, int flags,
+                     int* cg_iters, double* cg_rel_residual, void* ws, size_t ws_bytes,
+                     flashot_stream_t stream) {
+  if (!eps_ok(eps) || !std::isfinite(cg_tol) || cg_tol < 0.0 || cg_max_iters < 0)
+    return FLASHOT_ERR_INVALID_ARG;
+  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  {
+    const int p = flags & FLASHOT_PREC_MASK;
+    if (p != FLASHOT_PREC_AUTO && p != FLASHOT_PREC_FP32) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  }
+  const int fl = (flags & FLASHOT_REUSE_PACK) | FLASHOT_PREC_FP32;
+  Ctx c;
+  int rc = begin(n, m, d, d + 2, fl, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  const HvpLayout H = make_hvp_layout(c.g, c.L.total);
+  if (ws_bytes < H.total) return FLASHOT_ERR_WORKSPACE_TOO_SMALL;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(V) || !is_device_ptr(out) ||
+      (const void*)out == (const void*)V)
+    return FLASHOT_ERR_INVALID_ARG;
+  if (cg_iters) *cg_iters = 0;
+  if (cg_rel_residual) *cg_rel_residual = 0.0;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+  float* vp = c.at<float>(H.vp);
+  float* VA = c.at<float>(H.VA);
+  float* OA = c.at<float>(H.OA);
+  float* VB = c.at<float>(H.VB);
+  float* OB = c.at<float>(H.OB);
+  float* T = c.at<float>(H.T);
+  float* wf = c.at<float>(H.wf);
+  float* t1 = c.at<float>(H.t1);
+  float* PtT = c.at<float>(H.PtT);
+  float* z = c.at<float>(H.z);
+  float* res = c.at<float>(H.res);
+  float* yv = c.at<float>(H.yv);
+  float* pv = c.at<float>(H.p);
+  float* Pp = c.at<float>(H.Pp);
+  float* tn = c.at<float>(H.tn);
+  float* VD = c.at<float>(H.VD);
+  float* OD = c.at<float>(H.OD);
+  double* sc = c.at<double>(H.sc);
+  const int T256 = 256;
+  const int64_t nm = std::max(n, m);
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    pack_rows_kernel<PackKind::F32><<<grid1(c.g.n_pad * c.g.dpf, T256), T256, 0, c.st>>>(
+        V, vp, n, d, c.g.n_pad, c.g.dpf);
+  }
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    hvp_prep_kernel<<<grid1(nm, T256), T256, 0, c.st>>>(X, Y, V, n, m, d, VA, VB);
+  }
+  if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  // [PY | r], [P^T V | P^T s | c] and the curvature term T.
+  if ((rc = run_wsum_pass(c, kWsumApply, false, eps, VA, d + 1, d + 1, X, Y, OA, d + 1)) !=
+      FLASHOT_OK)
+    return rc;
+  if ((rc = run_wsum_pass(c, kWsumApply, true, eps, VB, d + 2, d + 2, X, Y, OB, d + 2)) !=
+      FLASHOT_OK)
+    return rc;
+  if ((rc = run_wsum_pass(c, kWsumHessT, false, eps, Y, d, d, X, Y, T, d, vp)) != FLASHOT_OK)
+    return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    hvp_rhs_kernel<<<grid1(n, T256), T256, 0, c.st>>>(OA, VB, n, d, eps, wf, t1);
+  }
+  if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  if ((rc = run_wsum_pass(c, kWsumApply, true, eps, t1, 1, 1, X, Y, PtT, 1)) != FLASHOT_OK)
+    return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    hvp_cg_init_kernel<<<1, 1024, 0, c.st>>>(Y, OB, PtT, m, d, eps, z, res, yv, pv, sc);
+  }
+  if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  // Preconditioned CG on the Schur complement S = diag(c) - P^T diag(1/r) P.
+  double host_sc[kHvpScalars];
+  auto read_scalars = [&]() -> int {
+    cudaError_t e = cudaMemcpyAsync(host_sc, sc, sizeof(host_sc), cudaMemcpyDeviceToHost, c.st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
+    return e == cudaSuccess ? FLASHOT_OK : cuda_fail(e);
+  };
+  if ((rc = read_scalars()) != FLASHOT_OK) return rc;
+  const double rr0 = host_sc[kHvpRR0];
+  double rel = rr0 > 0.0 ? 1.0 : 0.0;
+  int it = 0;
+  while (rr0 > 0.0 && rel > cg_tol && it < cg_max_iters) {
+    if ((rc = run_wsum_pass(c, kWsumApply, false, eps, pv, 1, 1, X, Y, Pp, 1)) != FLASHOT_OK)
+      return rc;
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      hvp_div_kernel<<<grid1(n, T256), T256, 0, c.st>>>(Pp, OA + d, d + 1, n, tn);
+    }
+    if ((rc = launch_check()) != FLASHOT_OK) return rc;
+    if ((rc = run_wsum_pass(c, kWsumApply, true, eps, tn, 1, 1, X, Y, PtT, 1)) != FLASHOT_OK)
+      return rc;
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      hvp_cg_step_kernel<<<1, 1024, 0, c.st>>>(OB, PtT, m, d, z, res, yv, pv, sc);
+    }
+    if ((rc = launch_check()) != FLASHOT_OK) return rc;
+    if ((rc = read_scalars()) != FLASHOT_OK) return rc;
+    ++it;
+    if (host_sc[kHvpBreak] != 0.0) break;
+    rel = std::sqrt(std::max(host_sc[kHvpRR], 0.0) / rr0);
+  }
+  unsigned word = 0;
+  {
+    cudaError_t e = cudaMemcpyAsync(&word, c.at<unsigned>(c.L.status), sizeof(word),
+                                    cudaMemcpyDeviceToHost, c.st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (word != 0) return FLASHOT_ERR_DEVICE_TIMEOUT;
+  if (cg_iters) *cg_iters = it;
+  if (cg_rel_residual) *cg_rel_residual = rel;
+  // [P diag(z) Y | P z], then assemble H V.
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    hvp_vd_kernel<<<grid1(m, T256), T256, 0, c.st>>>(Y, z, m, d, VD);
+  }
+  if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  if ((rc = run_wsum_pass(c, kWsumApply, false, eps, VD, d + 1, d + 1, X, Y, OD, d + 1)) !=
+      FLASHOT_OK)
+    return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    hvp_final_kernel<<<grid1(n, T256), T256, 0, c.st>>>(X, OA, VB, T, wf, OD, n, d, eps, out);
+  }
+  return launch_check();
 }
 
 size_t flashot_divergence_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags) {

@@ -12,7 +12,8 @@
 //              each split writes a (max, sum) partial, lse_combine_kernel merges them.
 //  * wsum_*  : weighted sums with weights w_ij = exp2(kappa <p_i, q_j> + c_j + r_i):
 //              transport application (P V), the barycentric gradient (softmax-weighted
-//              Y) and the Hadamard-weighted transport (sum_j P_ij <x_i, y_j>).
+//              Y), the Hadamard-weighted transport (sum_j P_ij <x_i, y_j>) and the
+//              Hessian curvature term (sum_j P_ij <u_i, y_j> y_j).
 #pragma once
 
 #include "common.cuh"
@@ -169,9 +170,9 @@ lse_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict__
   if (row < n_rows) partial[blockIdx.y * ld + row] = make_float2(M, S);
 }
 
-// Final write of a weighted-sum row (shared by the two wsum kernels).
-template <int MODE>
-__device__ __forceinline__ void wsum_store(const float (&acc)[32], float sumw, float had,
+// Final write of a weighted-sum row (shared by the two wsum kernels); KO output columns.
+template <int MODE, int KO>
+__device__ __forceinline__ void wsum_store(const float (&acc)[KO], float sumw, float had,
                                            int64_t row, int64_t o0, int64_t k,
                                            const float* __restrict__ rowW,
                                            const float* __restrict__ Xrow, int64_t d,
@@ -183,115 +184,141 @@ __device__ __forceinline__ void wsum_store(const float (&acc)[32], float sumw, f
     const float a = rowW[row];
     const float inv = sumw > 0.0f ? 1.0f / sumw : 0.0f;
 #pragma unroll
-    for (int o = 0; o < 32; ++o) {
+    for (int o = 0; o < KO; ++o) {
       const int64_t oo = o0 + o;
       if (oo < d) out[row * ldo + oo] = a > 0.0f ? 2.0f * a * (Xrow[row * d + oo] - acc[o] * inv)
                                                  : 0.0f;
     }
   } else {
 #pragma unroll
-    for (int o = 0; o < 32; ++o) {
+    for (int o = 0; o < KO; ++o) {
       const int64_t oo = o0 + o;
       if (oo < k) out[row * ldo + oo] = acc[o];
     }
   }
 }
 
-// Stage a 32-column x 32-output tile of V (rows of V are the pass's columns j), zero
+// Stage a 32-column x KO-output tile of V (rows of V are the pass's columns j), zero
 // padded in both directions.
-__device__ __forceinline__ void stage_v_tile(float (*vs)[33], const float* __restrict__ V,
+template <int KO>
+__device__ __forceinline__ void stage_v_tile(float (*vs)[KO + 1], const float* __restrict__ V,
                                              int64_t ldv, int64_t n_cols, int64_t k,
                                              int64_t j0, int64_t o0, int tid) {
-  for (int e = tid; e < 32 * 32; e += kFmaThreads) {
-    const int c = e >> 5, o = e & 31;
+  for (int e = tid; e < 32 * KO; e += kFmaThreads) {
+    const int c = e / KO, o = e % KO;
     const int64_t j = j0 + c, oo = o0 + o;
     vs[c][o] = (j < n_cols && oo < k) ? V[j * ldv + oo] : 0.0f;
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// Weighted sums, d_pad = DP <= 32. One row per thread; output columns [o0, o0+32) per
+// Weighted sums, d_pad = DP <= 32. One row per thread; output columns [o0, o0+KO) per
 // blockIdx.y. w_ij = exp2(kappa <p_i, q_j> + c_j + r_i).
 //  Apply:    out_i[o] = sum_j w_ij V_j[o]
 //  Grad:     V = packed column points; out_i = 2 a_i (x_i - sum_j w_ij q_j / sum_j w_ij)
 //  Hadamard: out_i = sum_j w_ij <p_i, q_j>
+//  HessT:    out_i[o] = sum_j w_ij <u_i, q_j> V_j[o], u_i the rows of rowU (packed like
+//            rowP) and V the column points
 // ---------------------------------------------------------------------------------------
-template <int DP, int MODE>
+template <int DP, int MODE, int KO = 32>
 __global__ void __launch_bounds__(kFmaThreads)
 wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                       const float* __restrict__ colBias, const float* __restrict__ rowBias,
                       int64_t n_rows, int64_t n_cols, int n_col_tiles, float kappa,
                       const float* __restrict__ V, int64_t ldv, int64_t k,
                       const float* __restrict__ rowW, const float* __restrict__ Xrow,
-                      int64_t d, float* __restrict__ out, int64_t ldo) {
+                      int64_t d, float* __restrict__ out, int64_t ldo,
+                      const float* __restrict__ rowU) {
   constexpr int Q = DP / 4;
+  constexpr bool kHess = (MODE == kWsumHessT);
   __shared__ float4 ys[32 * Q];
   __shared__ float cs[32];
-  __shared__ float vs[32][33];
+  __shared__ float vs[32][KO + 1];
   const int tid = threadIdx.x;
   const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
-  const int64_t o0 = (int64_t)blockIdx.y * 32;
-  float4 x[Q];
-  const float4* xr = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * DP);
+  const int64_t o0 = (int64_t)blockIdx.y * KO;
+  float4 x[Q], u[kHess ? Q : 1];
+  const int64_t rr = row < n_rows ? row : 0;
+  const float4* xr = reinterpret_cast<const float4*>(rowP + rr * DP);
 #pragma unroll
   for (int q = 0; q < Q; ++q) x[q] = xr[q];
-  const float rb = row < n_rows ? rowBias[row] : neg_inf();
-  float acc[32];
+  if constexpr (kHess) {
+    const float4* ur = reinterpret_cast<const float4*>(rowU + rr * DP);
 #pragma unroll
-  for (int o = 0; o < 32; ++o) acc[o] = 0.0f;
+    for (int q = 0; q < Q; ++q) u[q] = ur[q];
+  }
+  const float rb = row < n_rows ? rowBias[row] : neg_inf();
+  float acc[KO];
+#pragma unroll
+  for (int o = 0; o < KO; ++o) acc[o] = 0.0f;
   float sumw = 0.0f, had = 0.0f;
   for (int t = 0; t < n_col_tiles; ++t) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(colP + (int64_t)t * 32 * DP);
     for (int e = tid; e < 32 * Q; e += kFmaThreads) ys[e] = src[e];
     if (tid < 32) cs[tid] = colBias[(int64_t)t * 32 + tid];
-    if constexpr (MODE != kWsumHadamard) stage_v_tile(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
+    if constexpr (MODE != kWsumHadamard)
+      stage_v_tile<KO>(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
     __syncthreads();
 #pragma unroll 4
     for (int c = 0; c < 32; ++c) {
       float dot = 0.0f;
 #pragma unroll
       for (int q = 0; q < Q; ++q) dot = dot4(x[q], ys[c * Q + q], dot);
-      const float w = ex2(fmaf(kappa, dot, cs[c]) + rb);
+      float w = ex2(fmaf(kappa, dot, cs[c]) + rb);
       if constexpr (MODE == kWsumHadamard) {
         had = fmaf(w, dot, had);
       } else {
+        if constexpr (kHess) {
+          float tu = 0.0f;
 #pragma unroll
-        for (int o = 0; o < 32; ++o) acc[o] = fmaf(w, vs[c][o], acc[o]);
+          for (int q = 0; q < Q; ++q) tu = dot4(u[q], ys[c * Q + q], tu);
+          w *= tu;
+        }
+#pragma unroll
+        for (int o = 0; o < KO; ++o) acc[o] = fmaf(w, vs[c][o], acc[o]);
         if constexpr (MODE == kWsumGrad) sumw += w;
       }
     }
   }
-  if (row < n_rows) wsum_store<MODE>(acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+  if (row < n_rows) wsum_store<MODE, KO>(acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
 }
 
 // Weighted sums, any d_pad (multiple of 32): dots for 32 columns accumulated over 32-wide
 // k-chunks, then the same epilogue as the small-d kernel.
-template <int MODE>
+template <int MODE, int KO = 32>
 __global__ void __launch_bounds__(kFmaThreads)
 wsum_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                         const float* __restrict__ colBias, const float* __restrict__ rowBias,
                         int64_t n_rows, int64_t n_cols, int n_col_tiles, int64_t d_pad,
                         float kappa, const float* __restrict__ V, int64_t ldv, int64_t k,
                         const float* __restrict__ rowW, const float* __restrict__ Xrow,
-                        int64_t d, float* __restrict__ out, int64_t ldo) {
+                        int64_t d, float* __restrict__ out, int64_t ldo,
+                        const float* __restrict__ rowU) {
+  constexpr bool kHess = (MODE == kWsumHessT);
   __shared__ float4 ys[32 * 8];
   __shared__ float cs[32];
-  __shared__ float vs[32][33];
+  __shared__ float vs[32][KO + 1];
   const int tid = threadIdx.x;
   const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
-  const int64_t o0 = (int64_t)blockIdx.y * 32;
-  const float4* xr = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * d_pad);
+  const int64_t o0 = (int64_t)blockIdx.y * KO;
+  const int64_t rr = row < n_rows ? row : 0;
+  const float4* xr = reinterpret_cast<const float4*>(rowP + rr * d_pad);
+  const float4* ur = kHess ? reinterpret_cast<const float4*>(rowU + rr * d_pad) : nullptr;
   const int nkc = (int)(d_pad / 32);
   const float rb = row < n_rows ? rowBias[row] : neg_inf();
-  float out_acc[32];
+  float out_acc[KO];
 #pragma unroll
-  for (int o = 0; o < 32; ++o) out_acc[o] = 0.0f;
+  for (int o = 0; o < KO; ++o) out_acc[o] = 0.0f;
   float sumw = 0.0f, had = 0.0f;
   for (int t = 0; t < n_col_tiles; ++t) {
-    float acc[32];
+    float acc[32], tacc[kHess ? 32 : 1];
 #pragma unroll
     for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+    if constexpr (kHess) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) tacc[c] = 0.0f;
+    }
     for (int kc = 0; kc < nkc; ++kc) {
       __syncthreads();
       for (int e = tid; e < 256; e += kFmaThreads) {
@@ -302,7 +329,7 @@ wsum_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict_
       if (kc == 0) {
         if (tid < 32) cs[tid] = colBias[(int64_t)t * 32 + tid];
         if constexpr (MODE != kWsumHadamard)
-          stage_v_tile(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
+          stage_v_tile<KO>(vs, V, ldv, n_cols, k, (int64_t)t * 32, o0, tid);
       }
       __syncthreads();
       float4 xv[8];
@@ -313,20 +340,31 @@ wsum_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict_
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[c] = dot4(xv[q], ys[c * 8 + q], acc[c]);
       }
+      if constexpr (kHess) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[q] = ur[kc * 8 + q];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) tacc[c] = dot4(xv[q], ys[c * 8 + q], tacc[c]);
+        }
+      }
     }
 #pragma unroll 4
     for (int c = 0; c < 32; ++c) {
-      const float w = ex2(fmaf(kappa, acc[c], cs[c]) + rb);
+      float w = ex2(fmaf(kappa, acc[c], cs[c]) + rb);
       if constexpr (MODE == kWsumHadamard) {
         had = fmaf(w, acc[c], had);
       } else {
+        if constexpr (kHess) w *= tacc[c];
 #pragma unroll
-        for (int o = 0; o < 32; ++o) out_acc[o] = fmaf(w, vs[c][o], out_acc[o]);
+        for (int o = 0; o < KO; ++o) out_acc[o] = fmaf(w, vs[c][o], out_acc[o]);
         if constexpr (MODE == kWsumGrad) sumw += w;
       }
     }
   }
-  if (row < n_rows) wsum_store<MODE>(out_acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+  if (row < n_rows)
+    wsum_store<MODE, KO>(out_acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
 }
 
 }  // namespace flashot

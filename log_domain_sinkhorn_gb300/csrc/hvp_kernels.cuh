@@ -1,0 +1,230 @@
+// hvp_kernels.cuh -- the O((n + m) d) steps of the streaming Hessian-vector product of the
+// OT loss w.r.t. X (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, SAI
+// replication review, "Summary" (iii): an HVP oracle built from streaming transport
+// applications and a Schur solve, for O((n + m) d)-memory Newton-CG).
+//
+// At potentials (f, g), with P_ij = a_i b_j exp((f_i + g_j - |x_i - y_j|^2)/eps), r = P 1,
+// c = P^T 1, s_i = <x_i, v_i>, (PY)_i = sum_j P_ij y_j and T_i = sum_j P_ij <v_i, y_j> y_j:
+//   w_f,i = (2/eps) (r_i s_i - <v_i, (PY)_i>)
+//   w_g,j = (2/eps) ((P^T s)_j - <y_j, (P^T V)_j>)
+//   K (u, z) = (w_f, w_g),  K = [[diag r, P], [P^T, diag c]]  (solved through the Schur
+//      complement S = diag c - P^T diag(1/r) P on z, then u = (w_f - P z) / r)
+//   (H V)_i = 2 r_i v_i - (4/eps) (x_i (eps/2) w_f,i - s_i (PY)_i + T_i)
+//             + 2 ((r_i x_i - (PY)_i) u_i + x_i (P z)_i - (P diag(z) Y)_i).
+// The streaming passes (P [Y | 1], P^T [V | s | 1], T, the CG's P p and P^T t, and
+// P [diag(z) Y | z]) run in the weighted-sum kernels; the kernels here assemble their
+// inputs and outputs. Every reduction is one block in a fixed order (deterministic).
+#pragma once
+
+#include "common.cuh"
+
+namespace flashot {
+
+// Scalars the CG keeps on the device (doubles).
+enum HvpScalar : int { kHvpRho = 0, kHvpRR = 1, kHvpRR0 = 2, kHvpBreak = 3, kHvpScalars = 8 };
+
+// VA (m x (d+1)) = [Y | 1];  VB (n x (d+2)) = [V | s | 1] with s_i = <x_i, v_i>.
+__global__ void hvp_prep_kernel(const float* __restrict__ X, const float* __restrict__ Y,
+                                const float* __restrict__ V, int64_t n, int64_t m, int64_t d,
+                                float* __restrict__ VA, float* __restrict__ VB) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t < m) {
+    for (int64_t k = 0; k < d; ++k) VA[t * (d + 1) + k] = Y[t * d + k];
+    VA[t * (d + 1) + d] = 1.0f;
+  }
+  if (t < n) {
+    float s = 0.0f;
+    for (int64_t k = 0; k < d; ++k) {
+      const float v = V[t * d + k];
+      VB[t * (d + 2) + k] = v;
+      s = fmaf(X[t * d + k], v, s);
+    }
+    VB[t * (d + 2) + d] = s;
+    VB[t * (d + 2) + d + 1] = 1.0f;
+  }
+}
+
+// w_f,i from OA = [PY | r] and VB; t1_i = w_f,i / r_i (0 for rows without mass).
+__global__ void hvp_rhs_kernel(const float* __restrict__ OA, const float* __restrict__ VB,
+                               int64_t n, int64_t d, float eps, float* __restrict__ wf,
+                               float* __restrict__ t1) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float* pa = OA + i * (d + 1);
+  const float* vb = VB + i * (d + 2);
+  float vpy = 0.0f;
+  for (int64_t k = 0; k < d; ++k) vpy = fmaf(vb[k], pa[k], vpy);
+  const float r = pa[d];
+  const float w = (2.0f / eps) * (r * vb[d] - vpy);
+  wf[i] = w;
+  t1[i] = r > 0.0f ? w / r : 0.0f;
+}
+
+// y = a / b elementwise (0 where b <= 0), reading b with a stride (a column of a matrix).
+__global__ void hvp_div_kernel(const float* __restrict__ a, const float* __restrict__ b,
+                               int64_t ldb, int64_t n, float* __restrict__ y) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float bi = b[i * ldb];
+  y[i] = bi > 0.0f ? a[i] / bi : 0.0f;
+}
+
+// Block-wide fp64 sum (blockDim.x == 1024); every thread receives the result.
+__device__ __forceinline__ double block_sum(double v, double* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double s = red[threadIdx.x];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) red[32] = s;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// S is singular: S 1 = 0, and rows / columns of points without mass (c_j = 0) are zero. Its
+// range is {v : v_j = 0 where c_j = 0, sum of the other v_j = 0}. The right-hand side lies
+// there analytically, but for smooth V it is a small difference of large terms, and fp32
+// rounding leaves a null-space component that CG cannot remove (the residual stalls). So
+// the right-hand side and every S p are projected onto the range: the mean over the
+// columns with mass is subtracted from them.
+
+// CG start on S z = rhs, rhs_j = w_g,j - PtT_j (projected), w_g from OB = [P^T V | P^T s | c];
+// preconditioner diag(c). z = 0, res = rhs, yv = res / c, p = yv.
+__global__ void __launch_bounds__(1024)
+hvp_cg_init_kernel(const float* __restrict__ Y, const float* __restrict__ OB,
+                   const float* __restrict__ PtT, int64_t m, int64_t d, float eps,
+                   float* __restrict__ z, float* __restrict__ res, float* __restrict__ yv,
+                   float* __restrict__ p, double* __restrict__ sc) {
+  __shared__ double red[33];
+  double sum = 0.0, cnt = 0.0;
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const float* ob = OB + j * (d + 2);
+    float rhs = 0.0f;
+    if (ob[d + 1] > 0.0f) {
+      float yptv = 0.0f;
+      for (int64_t k = 0; k < d; ++k) yptv = fmaf(Y[j * d + k], ob[k], yptv);
+      rhs = (2.0f / eps) * (ob[d] - yptv) - PtT[j];
+      sum += (double)rhs;
+      cnt += 1.0;
+    }
+    res[j] = rhs;
+  }
+  sum = block_sum(sum, red);
+  cnt = block_sum(cnt, red);
+  const float mean = cnt > 0.0 ? (float)(sum / cnt) : 0.0f;
+  double rho = 0.0, rr = 0.0;
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const float cj = OB[j * (d + 2) + d + 1];
+    const float r = cj > 0.0f ? res[j] - mean : 0.0f;
+    const float y = cj > 0.0f ? r / cj : 0.0f;
+    z[j] = 0.0f;
+    res[j] = r;
+    yv[j] = y;
+    p[j] = y;
+    rho += (double)r * (double)y;
+    rr += (double)r * (double)r;
+  }
+  rho = block_sum(rho, red);
+  rr = block_sum(rr, red);
+  if (threadIdx.x == 0) {
+    sc[kHvpRho] = rho;
+    sc[kHvpRR] = rr;
+    sc[kHvpRR0] = rr;
+    sc[kHvpBreak] = 0.0;
+  }
+}
+
+// One preconditioned CG step given PtT = P^T diag(1/r) P p:
+//   q = c p - PtT (projected), alpha = rho / <p, q>, z += alpha p, res -= alpha q,
+//   yv = res / c, rho' = <res, yv>, p = yv + (rho'/rho) p.  <p, q> <= 0 (S is PSD, so only
+//   round-off gives it) stops the iteration (kHvpBreak = 1) without changing z.
+__global__ void __launch_bounds__(1024)
+hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, int64_t m,
+                   int64_t d, float* __restrict__ z, float* __restrict__ res,
+                   float* __restrict__ yv, float* __restrict__ p, double* __restrict__ sc) {
+  __shared__ double red[33];
+  double sq = 0.0, spq = 0.0, sp = 0.0, cnt = 0.0;
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const float cj = OB[j * (d + 2) + d + 1];
+    if (cj > 0.0f) {
+      const float q = cj * p[j] - PtT[j];
+      sq += (double)q;
+      spq += (double)p[j] * (double)q;
+      sp += (double)p[j];
+      cnt += 1.0;
+    }
+  }
+  sq = block_sum(sq, red);
+  spq = block_sum(spq, red);
+  sp = block_sum(sp, red);
+  cnt = block_sum(cnt, red);
+  const double qbar = cnt > 0.0 ? sq / cnt : 0.0;
+  const double pq = spq - qbar * sp;
+  const double rho = sc[kHvpRho];
+  if (!(pq > 0.0) || !(rho > 0.0)) {
+    if (threadIdx.x == 0) sc[kHvpBreak] = 1.0;
+    return;
+  }
+  const float alpha = (float)(rho / pq);
+  const float qb = (float)qbar;
+  double rho_new = 0.0, rr = 0.0;
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const float cj = OB[j * (d + 2) + d + 1];
+    if (cj > 0.0f) {
+      const float q = (cj * p[j] - PtT[j]) - qb;
+      z[j] = fmaf(alpha, p[j], z[j]);
+      const float rj = fmaf(-alpha, q, res[j]);
+      res[j] = rj;
+      const float y = rj / cj;
+      yv[j] = y;
+      rho_new += (double)rj * (double)y;
+      rr += (double)rj * (double)rj;
+    }
+  }
+  rho_new = block_sum(rho_new, red);
+  rr = block_sum(rr, red);
+  const float beta = (float)(rho_new / rho);
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) p[j] = fmaf(beta, p[j], yv[j]);
+  if (threadIdx.x == 0) {
+    sc[kHvpRho] = rho_new;
+    sc[kHvpRR] = rr;
+  }
+}
+
+// VD (m x (d+1)) = [diag(z) Y | z].
+__global__ void hvp_vd_kernel(const float* __restrict__ Y, const float* __restrict__ z,
+                              int64_t m, int64_t d, float* __restrict__ VD) {
+  const int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (j >= m) return;
+  const float zj = z[j];
+  for (int64_t k = 0; k < d; ++k) VD[j * (d + 1) + k] = zj * Y[j * d + k];
+  VD[j * (d + 1) + d] = zj;
+}
+
+// (H V)_i from the pass outputs: OA = [PY | r], VB = [V | s | 1], T, wf, OD = [P diag(z) Y | P z].
+__global__ void hvp_final_kernel(const float* __restrict__ X, const float* __restrict__ OA,
+                                 const float* __restrict__ VB, const float* __restrict__ T,
+                                 const float* __restrict__ wf, const float* __restrict__ OD,
+                                 int64_t n, int64_t d, float eps, float* __restrict__ out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float* pa = OA + i * (d + 1);
+  const float* vb = VB + i * (d + 2);
+  const float* od = OD + i * (d + 1);
+  const float r = pa[d], s = vb[d], w = wf[i], pz = od[d];
+  const float u = r > 0.0f ? (w - pz) / r : 0.0f;
+  const float c4 = 4.0f / eps;
+  for (int64_t k = 0; k < d; ++k) {
+    const float x = X[i * d + k], py = pa[k];
+    const float lxx = 2.0f * r * vb[k] - c4 * (x * (0.5f * eps * w) - s * py + T[i * d + k]);
+    const float lxp = 2.0f * ((r * x - py) * u + x * pz - od[k]);
+    out[i * d + k] = lxx + lxp;
+  }
+}
+
+}  // namespace flashot

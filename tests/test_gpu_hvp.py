@@ -1,0 +1,131 @@
+"""GPU parity of the streaming Hessian-vector product of the OT loss w.r.t. X against the
+dense fp64 Moore-Penrose reference (FlashSinkhorn SAI replication review, "Summary" (iii)
+and "Strengths": HVP through a Schur solve with streaming P / P^T products, checked against
+a dense Moore-Penrose HVP for eps down to 0.01).
+
+Tolerance. The pages report relative errors below 1% down to eps = 0.01. Here the Schur
+system is solved to a relative residual of 1e-6 in fp32, and every streaming pass carries
+fp32 rounding (~1e-6 relative); the HVP formula subtracts terms up to (4/eps) max|x - y|^2
+larger than the result. For eps >= 0.05 on unit-scale clouds that predicts errors of order
+1e-4, so the bar is a relative L2 error of 1e-3; at eps = 0.01 the cancellation factor is
+5x larger and the Schur complement worse conditioned, so the bar is the pages' 1e-2.
+The potentials are the oracle's converged ones cast to fp32, and the oracle evaluates the
+HVP at those same fp32 values (so solve error does not enter)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import to_dev
+from workloads import make_problem
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(n, m, d, seed, dist="unif01"):
+    pr = make_problem(n, m, d, x_dist=dist, weights="dirichlet1", seed=seed)
+    return pr
+
+
+def _converged_fp32(pr, eps):
+    f, g, _, _, err = oracle.solve_tol(pr.X, pr.Y, pr.a, pr.b, eps, 1e-12, 200000, 10)
+    return f.astype(np.float32), g.astype(np.float32)
+
+
+def _rel_l2(got, ref):
+    return float(np.linalg.norm(np.asarray(got, np.float64) - ref) / np.linalg.norm(ref))
+
+
+@pytest.mark.parametrize("n,m,d,eps", [(60, 80, 2, 0.1), (130, 97, 3, 0.05), (64, 64, 3, 0.01),
+                                       (90, 70, 16, 0.1), (50, 66, 40, 0.2)])
+def test_hvp_matches_dense_moore_penrose(cuda_lib, n, m, d, eps):
+    pr = _problem(n, m, d, seed=n + m + d)
+    scale = 1.0 if d <= 3 else (3.0 / d) ** 0.5  # keep squared distances of order 1
+    Xs = (pr.X * scale).astype(np.float32)
+    Ys = (pr.Y * scale).astype(np.float32)
+    pr.X, pr.Y = Xs, Ys
+    f, g = _converged_fp32(pr, eps)
+    V = np.random.default_rng(5).normal(size=(n, d)).astype(np.float32)
+    ref = oracle.hvp_x(Xs, Ys, pr.a, pr.b, f, g, eps, V)
+    HV, iters, rel = cuda_lib.ot_hvp_x(to_dev(Xs), to_dev(Ys), to_dev(f), to_dev(g), eps,
+                                      to_dev(V), to_dev(pr.a), to_dev(pr.b), cg_tol=1e-6)
+    assert 0 < iters < 1000 and rel <= 1e-6
+    bar = 1e-2 if eps < 0.05 else 1e-3
+    assert _rel_l2(HV.cpu().numpy(), ref) <= bar
+
+
+def test_hvp_uniform_translation_closed_form(cuda_lib):
+    """V = 1 t: H V = 2 r_i t at any potentials (the translation is absorbed by the
+    potentials), here at converged potentials where r = a; 5000 x 4000 points (several
+    column tiles and a ragged tail)."""
+    n, m, d, eps = 5000, 4000, 3, 0.05
+    pr = _problem(n, m, d, seed=11)
+    X, Y = to_dev(pr.X), to_dev(pr.Y)
+    a, b = to_dev(pr.a), to_dev(pr.b)
+    f, g, _, _, err, _ = cuda_lib.sinkhorn_solve_tol(X, Y, a, b, eps, 1e-5, 3000, 10,
+                                                     precision="fp32")
+    t = np.array([0.7, -0.2, 0.45], np.float32)
+    V = np.tile(t, (n, 1)).astype(np.float32)
+    HV, iters, rel = cuda_lib.ot_hvp_x(X, Y, f, g, eps, to_dev(V), a, b, cg_tol=1e-6)
+    assert rel <= 1e-6
+    want = 2.0 * pr.a.astype(np.float64)[:, None] * t[None, :]
+    # r differs from a by the solve's marginal error (L1 <= 1e-5), plus the HVP's own error
+    # (the 1e-3 bar of the dense comparison)
+    err_abs = np.abs(HV.cpu().numpy() - want).sum(0)
+    assert np.all(err_abs <= 2.0 * np.abs(t) * 1e-5 + 1e-3 * np.abs(want).sum(0))
+
+
+def test_hvp_is_symmetric_at_scale(cuda_lib):
+    """<V1, H V2> = <V2, H V1> on 4000 x 5000 points, d = 3."""
+    n, m, d, eps = 4000, 5000, 3, 0.05
+    pr = _problem(n, m, d, seed=12, dist="normal")
+    X, Y = to_dev(pr.X * 0.3), to_dev(pr.Y * 0.3)
+    a, b = to_dev(pr.a), to_dev(pr.b)
+    f, g, _, _, err, _ = cuda_lib.sinkhorn_solve_tol(X, Y, a, b, eps, 1e-5, 3000, 10,
+                                                     precision="fp32")
+    rng = np.random.default_rng(2)
+    V1 = rng.normal(size=(n, d)).astype(np.float32)
+    V2 = rng.normal(size=(n, d)).astype(np.float32)
+    H1, _, rel1 = cuda_lib.ot_hvp_x(X, Y, f, g, eps, to_dev(V1), a, b, cg_tol=1e-6)
+    H2, _, rel2 = cuda_lib.ot_hvp_x(X, Y, f, g, eps, to_dev(V2), a, b, cg_tol=1e-6)
+    assert rel1 <= 1e-6 and rel2 <= 1e-6
+    s12 = float((V1.astype(np.float64) * H2.cpu().numpy()).sum())
+    s21 = float((V2.astype(np.float64) * H1.cpu().numpy()).sum())
+    assert abs(s12 - s21) <= 1e-3 * max(abs(s12), abs(s21))
+
+
+def test_hvp_rejects_bad_arguments(cuda_lib):
+    from log_domain_sinkhorn_gb300 import _binding as B
+    n, m, d = 40, 30, 3
+    pr = _problem(n, m, d, seed=13)
+    X, Y = to_dev(pr.X), to_dev(pr.Y)
+    f = torch.zeros(n, device="cuda")
+    g = torch.zeros(m, device="cuda")
+    V = torch.ones((n, d), device="cuda")
+    out = torch.empty((n, d), device="cuda")
+    lib = cuda_lib.library()
+    nb = int(lib.flashot_hvp_workspace_bytes(n, m, d, B.PREC_FP32))
+    assert nb > 0 and lib.flashot_hvp_workspace_bytes(n, m, d, B.PREC_BF16) == 0
+    ws = cuda_lib.Workspace(nb)
+    it = ctypes.c_int(0)
+    rel = ctypes.c_double(0.0)
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(eps=0.1, o=out, tol=1e-6, mx=100, flags=B.PREC_FP32, nbytes=nb):
+        return lib.flashot_ot_hvp_x(X.data_ptr(), Y.data_ptr(), None, None, f.data_ptr(),
+                                    g.data_ptr(), n, m, d, eps, V.data_ptr(), o.data_ptr(),
+                                    tol, mx, flags, ctypes.byref(it), ctypes.byref(rel),
+                                    ws.ptr, nbytes, s)
+
+    assert call(o=V) == B.ERR_INVALID_ARG
+    assert call(eps=-1.0) == B.ERR_INVALID_ARG
+    assert call(tol=float("nan")) == B.ERR_INVALID_ARG
+    assert call(mx=-1) == B.ERR_INVALID_ARG
+    assert call(flags=B.PREC_BF16) == B.ERR_NOT_IMPLEMENTED
+    assert call(flags=B.PREC_FP32 | B.SYMMETRIC) == B.ERR_NOT_IMPLEMENTED
+    assert call(nbytes=nb - 1) == B.ERR_WORKSPACE_TOO_SMALL
+    assert call() == B.OK
+    torch.cuda.synchronize()
+    assert np.isfinite(out.cpu().numpy()).all()
