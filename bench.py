@@ -72,6 +72,9 @@ def parse_args():
     p.add_argument("--hvp", action="store_true",
                    help="supplementary line: Hessian-vector product of the OT loss w.r.t. X "
                         "on n = m = 50000 points in Uniform[0,1]^3 (eps = 0.05, CG to 1e-6)")
+    p.add_argument("--hvp-sweep", action="store_true",
+                   help="supplementary line: HVP accuracy against the dense fp64 "
+                        "Moore-Penrose reference for eps = 0.1 .. 0.01 (n = m = 200, d = 3)")
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -582,6 +585,40 @@ def run_hvp(args):
     print(json.dumps(line), flush=True)
 
 
+def run_hvp_sweep(args):
+    """Supplementary line: relative L2 error of the streaming HVP against the dense fp64
+    Moore-Penrose reference, and CG iterations, for eps = 0.1, 0.05, 0.02, 0.01 (n = m = 200
+    points in Uniform[0,1]^3, uniform weights, potentials converged by the oracle and cast to
+    fp32, V ~ N(0, 1), CG to a relative residual of 1e-6)."""
+    import numpy as np
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    import oracle
+    from workloads import make_problem
+    torch.cuda.set_device(0)
+    n, d = 200, 3
+    pr = make_problem(n, n, d, x_dist="unif01", weights="uniform", seed=6060)
+    V = np.random.default_rng(6061).normal(size=(n, d)).astype(np.float32)
+    dv = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    rows = []
+    for eps in (0.1, 0.05, 0.02, 0.01):
+        f, g, _, it, err = oracle.solve_tol(pr.X, pr.Y, pr.a, pr.b, eps, 1e-12, 400000, 10)
+        f32, g32 = f.astype(np.float32), g.astype(np.float32)
+        ref = oracle.hvp_x(pr.X, pr.Y, pr.a, pr.b, f32, g32, eps, V)
+        HV, cg_it, rel = lds.ot_hvp_x(dv(pr.X), dv(pr.Y), dv(f32), dv(g32), eps, dv(V),
+                                      dv(pr.a), dv(pr.b), cg_tol=1e-6)
+        e = float(np.linalg.norm(HV.cpu().numpy() - ref) / np.linalg.norm(ref))
+        rows.append({"eps": eps, "rel_l2_error": e, "cg_iterations": cg_it,
+                     "cg_rel_residual": rel, "oracle_solve_iterations": it})
+    line = {"metric": "HVP accuracy vs dense Moore-Penrose reference", "supplementary": True,
+            "value": max(r["rel_l2_error"] for r in rows),
+            "unit": "max relative L2 error over eps", "results": rows, "dtype": "fp32",
+            "config": {"workload": "n=m=200, d=3, Uniform[0,1]^3, uniform weights",
+                       "V": "N(0,1), seed 6061", "cg_tol": 1e-6}}
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -802,6 +839,8 @@ def main():
         run_drift(args)
     elif args.hvp:
         run_hvp(args)
+    elif args.hvp_sweep:
+        run_hvp_sweep(args)
     elif args.tol is not None:
         run_convergence(args)
     elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":

@@ -29,6 +29,10 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   hvp_x                      central finite differences of the converged gradient;
                              uniform translation V = 1 t gives 2 r_i t exactly;
                              eps -> inf limit 2 a_i v_i; Hessian symmetry.
+  sinkhorn_knopp             2 x 2 cross-ratio closed form of the limit; column sums 1
+                             after every iteration; rank-one logits give 1/n after one
+                             iteration; invariance to shifts of H and equivariance to row /
+                             column permutations; monotone row-sum error.
   solve_tol                  with tol = 0 it equals solve; each reported error equals the
                              row-marginal L1 error recomputed from the plan by
                              marginals(); it stops at the first check below tol; the
@@ -108,6 +112,8 @@ def _lib():
             lib.oracle_marginals.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
                                              ctypes.c_double, _dp, _dp]
             lib.oracle_marginals.restype = None
+            lib.oracle_sinkhorn_knopp.argtypes = [_dp, _i64, ctypes.c_int, ctypes.c_int, _dp]
+            lib.oracle_sinkhorn_knopp.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _LIB = lib
@@ -321,3 +327,16 @@ def hvp_x(X, Y, a, b, f, g, eps, V):
     v = V.reshape(nd)
     dphi = eps * (np.linalg.pinv(K, rcond=1e-13, hermitian=True) @ (B.T @ v))
     return (Lxx @ v + B @ dphi).reshape(n, d)
+
+
+def sinkhorn_knopp(H, n_iter):
+    """Batched Sinkhorn-Knopp projection of B tiny matrices: H (B, n, n) logits, returns
+    P = diag(u) exp(H) diag(v) after n_iter alternations u = 1/(M v), v = 1/(M^T u) from
+    v = 1, as fp64 (B, n, n)."""
+    H = _f64(H)
+    if H.ndim != 3 or H.shape[1] != H.shape[2]:
+        raise ValueError("H must be (B, n, n)")
+    B, n = H.shape[0], H.shape[1]
+    P = np.empty_like(H)
+    _lib().oracle_sinkhorn_knopp(_p(H), B, n, int(n_iter), _p(P))
+    return P

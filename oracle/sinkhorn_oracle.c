@@ -321,3 +321,45 @@ void oracle_marginals(const double *X, const double *Y, const double *a, const d
         col_sums[j] = s;
     }
 }
+
+/*
+ * Batched Sinkhorn-Knopp projection of tiny matrices onto the Birkhoff polytope ("Fused &
+ * Furious: Sinkhorn Triton Kernels", section II: the KL projection of M = exp(H) onto the
+ * doubly stochastic matrices, P = diag(u) M diag(v), with u = 1 / (M v) and
+ * v = 1 / (M^T u) alternated n_iter times starting from v = 1; section III: one H per
+ * token, n = 4, n_iter = 20 in the mHC setting).
+ * H: B matrices of n x n logits, row-major, contiguous; P: the same layout.
+ */
+void oracle_sinkhorn_knopp(const double *H, int64_t B, int n, int n_iter, double *P)
+{
+#pragma omp parallel
+    {
+        double *M = (double *)malloc((size_t)n * n * sizeof(double));
+        double *u = (double *)malloc((size_t)n * sizeof(double));
+        double *v = (double *)malloc((size_t)n * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t bi = 0; bi < B; ++bi) {
+            const double *h = H + bi * n * n;
+            double *p = P + bi * n * n;
+            for (int k = 0; k < n * n; ++k) M[k] = exp(h[k]);
+            for (int j = 0; j < n; ++j) v[j] = 1.0;
+            for (int it = 0; it < n_iter; ++it) {
+                for (int i = 0; i < n; ++i) {
+                    double s = 0.0;
+                    for (int j = 0; j < n; ++j) s += M[i * n + j] * v[j];
+                    u[i] = 1.0 / s;
+                }
+                for (int j = 0; j < n; ++j) {
+                    double s = 0.0;
+                    for (int i = 0; i < n; ++i) s += M[i * n + j] * u[i];
+                    v[j] = 1.0 / s;
+                }
+            }
+            for (int i = 0; i < n; ++i)
+                for (int j = 0; j < n; ++j) p[i * n + j] = u[i] * M[i * n + j] * v[j];
+        }
+        free(M);
+        free(u);
+        free(v);
+    }
+}

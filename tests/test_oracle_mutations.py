@@ -34,6 +34,9 @@ MUTATIONS = {
     "tol_error_wrong_direction": ("expm1((fprev[i] - f[i]) / eps)", "expm1((f[i] - fprev[i]) / eps)"),
     "tol_error_drops_weight": ("e += a[i] * fabs(", "e += fabs("),
     "tol_iters_off_by_one": ("max_iters : k;", "max_iters : k - 1;"),
+    "sk_row_uses_transpose": ("s += M[i * n + j] * v[j];", "s += M[j * n + i] * v[j];"),
+    "sk_missing_exp": ("M[k] = exp(h[k]);", "M[k] = h[k] * h[k] + 1.0;"),
+    "sk_output_drops_u": ("p[i * n + j] = u[i] * M[i * n + j] * v[j];", "p[i * n + j] = M[i * n + j] * v[j];"),
     "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
 }
 

@@ -583,3 +583,55 @@ def test_hvp_large_eps_limit_and_symmetry():
     s12 = float((V * oracle.hvp_x(X, Y, a, b, f, g, eps, V2)).sum())
     s21 = float((V2 * oracle.hvp_x(X, Y, a, b, f, g, eps, V)).sum())
     assert s12 == pytest.approx(s21, rel=1e-10)
+
+
+# ---------------------------------------------------------------------------------
+# Batched Sinkhorn-Knopp of tiny matrices (scaling domain)
+# ---------------------------------------------------------------------------------
+
+def test_sinkhorn_knopp_2x2_cross_ratio_limit():
+    """Diagonal scaling keeps the cross ratio P11 P22 / (P12 P21) = M11 M22 / (M12 M21) = rho,
+    and the only doubly stochastic 2 x 2 matrix with that ratio has P11 = P22 =
+    sqrt(rho) / (1 + sqrt(rho))."""
+    rng = np.random.default_rng(90)
+    H = rng.normal(size=(50, 2, 2))
+    P = oracle.sinkhorn_knopp(H, 400)
+    rho = np.exp(H[:, 0, 0] + H[:, 1, 1] - H[:, 0, 1] - H[:, 1, 0])
+    p = np.sqrt(rho) / (1 + np.sqrt(rho))
+    np.testing.assert_allclose(P[:, 0, 0], p, rtol=1e-12)
+    np.testing.assert_allclose(P[:, 1, 1], p, rtol=1e-12)
+    np.testing.assert_allclose(P[:, 0, 1], 1 - p, rtol=1e-12)
+    # the cross ratio holds after any number of iterations
+    P3 = oracle.sinkhorn_knopp(H, 3)
+    cr = P3[:, 0, 0] * P3[:, 1, 1] / (P3[:, 0, 1] * P3[:, 1, 0])
+    np.testing.assert_allclose(cr, rho, rtol=1e-12)
+
+
+def test_sinkhorn_knopp_marginals_and_convergence():
+    """The last step is the column scaling, so columns sum to 1 after every iteration; the
+    row-sum error decreases with the iteration count."""
+    rng = np.random.default_rng(91)
+    H = rng.normal(size=(200, 4, 4)) * 1.5
+    errs = []
+    for it in (1, 2, 5, 10, 20, 40):
+        P = oracle.sinkhorn_knopp(H, it)
+        np.testing.assert_allclose(P.sum(1), 1.0, atol=1e-14)
+        errs.append(np.abs(P.sum(2) - 1.0).max())
+    assert all(e2 < e1 for e1, e2 in zip(errs, errs[1:]))
+    assert errs[-1] < 1e-4
+
+
+def test_sinkhorn_knopp_rank_one_and_invariances():
+    """Rank-one logits H_ij = alpha_i + beta_j give M = a b^T, whose projection is the
+    uniform matrix 1/n after one iteration. Adding a constant to H changes nothing, and
+    permuting rows and columns of H permutes P the same way."""
+    rng = np.random.default_rng(92)
+    al, be = rng.normal(size=(30, 5, 1)), rng.normal(size=(30, 1, 5))
+    P = oracle.sinkhorn_knopp(al + be, 1)
+    np.testing.assert_allclose(P, 0.2, rtol=1e-13)
+    H = rng.normal(size=(30, 4, 4))
+    P = oracle.sinkhorn_knopp(H, 20)
+    np.testing.assert_allclose(oracle.sinkhorn_knopp(H + 3.5, 20), P, rtol=1e-12)
+    pr, pc = rng.permutation(4), rng.permutation(4)
+    Pp = oracle.sinkhorn_knopp(H[:, pr][:, :, pc], 20)
+    np.testing.assert_allclose(Pp, P[:, pr][:, :, pc], rtol=1e-12)
