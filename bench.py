@@ -75,6 +75,11 @@ def parse_args():
     p.add_argument("--hvp-sweep", action="store_true",
                    help="supplementary line: HVP accuracy against the dense fp64 "
                         "Moore-Penrose reference for eps = 0.1 .. 0.01 (n = m = 200, d = 3)")
+    p.add_argument("--sk", action="store_true",
+                   help="supplementary line: batched Sinkhorn-Knopp of 4 x 4 matrices "
+                        "(B = 2^24 unless --sk-batch, 20 iterations)")
+    p.add_argument("--sk-batch", type=int, default=1 << 24)
+    p.add_argument("--sk-n", type=int, default=4)
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -619,6 +624,69 @@ def run_hvp_sweep(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sk(args):
+    """Supplementary line: batched Sinkhorn-Knopp projection of B tiny n x n matrices (the
+    mHC setting of "Fused & Furious": n = 4, 20 iterations, B up to 2^24), logits ~ N(0, 1).
+    Algorithmic bytes: the logits read and P written, 2 B n^2 4 bytes. Inputs larger than
+    L2 at the default B (1.07 GB each way); smaller batches flush L2 between steps."""
+    import numpy as np
+    import torch
+
+    import log_domain_sinkhorn_gb300 as lds
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    B, n, n_iter = args.sk_batch, args.sk_n, 20
+    g = torch.Generator(device=dev).manual_seed(4444)
+    H = torch.randn((B, n, n), device=dev, generator=g)
+    P = torch.empty_like(H)
+    bytes_step = 2.0 * B * n * n * 4
+    flush = None if bytes_step > 4 * L2_FLUSH_BYTES else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        lds.sinkhorn_knopp_batched(H, n_iter, out=P)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0).start()
+    times = []
+    for _ in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        lds.sinkhorn_knopp_batched(H, n_iter, out=P)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    clk = clocks.stop()
+    ms = statistics.median(times)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        Bs = min(B, 1 << 20)
+        Hs = H[:Bs].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.sinkhorn_knopp(Hs, n_iter)
+        dt = time.perf_counter() - t0
+        cpu = {"value": Bs / dt, "unit": "matrices/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"the first {Bs} matrices, {dt:.2f} s"}
+    line = {"metric": "batched Sinkhorn-Knopp (mHC %dx%d, %d iterations)" % (n, n, n_iter),
+            "supplementary": True, "value": B / (ms / 1e3), "unit": "matrices/s",
+            "ms_per_step": ms, "ms_q01_q99": [float(np.quantile(times, 0.01)),
+                                               float(np.quantile(times, 0.99))],
+            "steps": args.steps, "warmup": args.warmup, "dtype": "fp32",
+            "roofline": {"bound": "hbm", "achieved": bytes_step / (ms / 1e3) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": bytes_step / (ms / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes_per_launch": bytes_step,
+                         "peak_source": f"{src} hbm_gbs"},
+            "clocks": clk, "cpu_baseline": cpu, "gpu_launches": args.steps,
+            "config": {"workload": "B=%d matrices %dx%d, logits N(0,1), %d iterations" % (B, n, n, n_iter),
+                       "l2": "inputs larger than L2" if flush is None else "L2 flushed before each step"}}
+    print(json.dumps(line), flush=True)
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -841,6 +909,8 @@ def main():
         run_hvp(args)
     elif args.hvp_sweep:
         run_hvp_sweep(args)
+    elif args.sk:
+        run_sk(args)
     elif args.tol is not None:
         run_convergence(args)
     elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":

@@ -254,6 +254,23 @@ int flashot_ot_hvp_x(const float *X, const float *Y, const float *a, const float
                      int flags, int *cg_iters, double *cg_rel_residual, void *ws,
                      size_t ws_bytes, flashot_stream_t stream);
 
+/*
+ * Batched Sinkhorn-Knopp projection of tiny matrices onto the doubly stochastic matrices
+ * ("Fused & Furious: Sinkhorn Triton Kernels", section II: the KL projection of M = exp(H)
+ * onto the Birkhoff polytope; section III: one matrix per token, n = 4, n_iter = 20):
+ *   M = exp(H_b), v = 1; n_iter times: u = 1 / (M v), v = 1 / (M^T u);
+ *   P_b = diag(u) M diag(v)      (its columns sum to 1; its rows approach 1).
+ *   H, P: B matrices of n x n fp32, row-major, contiguous, device memory; P may equal H
+ *   (in place). 1 <= n <= 8, n_iter >= 1, B >= 0 (B = 0 does nothing). When n*n is a
+ *   multiple of 4, H and P must be 16-byte aligned (else FLASHOT_ERR_ALIGNMENT).
+ * Needs no workspace. Each matrix's largest logit is subtracted before exp (P does not
+ * change); logits that lie more than about 87 below a matrix's largest underflow to 0 in
+ * fp32, and a row or column of such zeros makes that matrix's P undefined. The scalings use
+ * the SFU reciprocal (rcp.approx, about 1 ulp).
+ */
+int flashot_sinkhorn_knopp_batched(const float *H, int64_t B, int n, int n_iter, float *P,
+                                   flashot_stream_t stream);
+
 /* ---- allocation-free variant -------------------------------------------------------- */
 /*
  * The paper has no counterpart to this entry point; it exists for callers that cannot give

@@ -24,7 +24,7 @@ __all__ = [
     "Workspace", "workspace_bytes", "sinkhorn_solve", "sinkhorn_step_f", "sinkhorn_step_g",
     "dual_loss", "transport_apply", "transport_hadamard_xy", "ot_grad_x", "workspace_status",
     "FlashotError", "library", "version", "launch_count", "KernelTimer",
-    "sinkhorn_divergence", "sinkhorn_solve_tol", "ot_hvp_x",
+    "sinkhorn_divergence", "sinkhorn_solve_tol", "ot_hvp_x", "sinkhorn_knopp_batched",
 ]
 
 
@@ -318,6 +318,21 @@ def ot_hvp_x(X, Y, f, g, eps: float, V, a=None, b=None, *, cg_tol: float = 1e-6,
         _stream())
     _binding.check(st, "flashot_ot_hvp_x")
     return o, int(iters.value), float(rel.value)
+
+
+def sinkhorn_knopp_batched(H: torch.Tensor, n_iter: int = 20, *, out=None):
+    """Project each of the B tiny matrices exp(H_b) (H: (B, n, n) fp32 logits, n <= 8) onto
+    the doubly stochastic matrices by n_iter Sinkhorn-Knopp alternations from v = 1.
+    ``out`` may be H itself (in place). Returns P (B, n, n)."""
+    if H.dim() != 3 or H.shape[1] != H.shape[2]:
+        raise ValueError("H must be (B, n, n)")
+    B, n = H.shape[0], H.shape[1]
+    P = out if out is not None else torch.empty_like(H)
+    st = library().flashot_sinkhorn_knopp_batched(
+        _dev_ptr(H, "H", (B, n, n)), B, n, int(n_iter), _dev_ptr(P, "out", (B, n, n)),
+        _stream())
+    _binding.check(st, "flashot_sinkhorn_knopp_batched")
+    return P
 
 
 def workspace_status(workspace: Workspace) -> int:
