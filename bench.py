@@ -671,16 +671,32 @@ def run_sk(args):
         dt = time.perf_counter() - t0
         cpu = {"value": Bs / dt, "unit": "matrices/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": f"the first {Bs} matrices, {dt:.2f} s"}
+    # Roofline: the algorithm as stated needs per matrix 2 n^2 n_iter + 2 n^2 FMA-pipe ops
+    # (row and column sums, the final scaling), n^2 + 2 n n_iter SFU ops (exp and one
+    # reciprocal per sum) and 2 n^2 4 bytes of HBM traffic. Its time floor is the largest of
+    # the three at FP32 = 128 lanes, SFU reciprocal = 16 lanes per clock per SM.
+    clk_hz = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    fma_ops = 2 * n * n * n_iter + 2 * n * n
+    xu_ops = n * n + 2 * n * n_iter
+    t_fma = B * fma_ops / (N_SMS * FP32_LANES_PER_SM * clk_hz)
+    t_xu = B * xu_ops / (N_SMS * 16 * clk_hz)
+    t_hbm = bytes_step / (hbm * 1e9)
+    t_floor = max(t_fma, t_xu, t_hbm)
     line = {"metric": "batched Sinkhorn-Knopp (mHC %dx%d, %d iterations)" % (n, n, n_iter),
             "supplementary": True, "value": B / (ms / 1e3), "unit": "matrices/s",
             "ms_per_step": ms, "ms_q01_q99": [float(np.quantile(times, 0.01)),
                                                float(np.quantile(times, 0.99))],
             "steps": args.steps, "warmup": args.warmup, "dtype": "fp32",
-            "roofline": {"bound": "hbm", "achieved": bytes_step / (ms / 1e3) / 1e9,
-                         "peak": hbm, "unit": "GB/s",
-                         "frac": bytes_step / (ms / 1e3) / 1e9 / hbm,
-                         "algorithmic_bytes_per_launch": bytes_step,
-                         "peak_source": f"{src} hbm_gbs"},
+            "roofline": {"bound": "alu", "achieved": B / (ms / 1e3), "peak": B / t_floor,
+                         "unit": "matrices/s", "frac": t_floor / (ms / 1e3),
+                         "floor_ms": {"fma_pipe": t_fma * 1e3, "sfu": t_xu * 1e3,
+                                      "hbm": t_hbm * 1e3},
+                         "per_matrix": {"fma_ops": fma_ops, "sfu_ops": xu_ops,
+                                        "bytes": 2 * n * n * 4},
+                         "hbm_achieved_gbs": bytes_step / (ms / 1e3) / 1e9,
+                         "hbm_frac": bytes_step / (ms / 1e3) / 1e9 / hbm,
+                         "peak_source": f"{src} hbm_gbs; FP32 and SFU from unit counts x "
+                                        "max SM clock"},
             "clocks": clk, "cpu_baseline": cpu, "gpu_launches": args.steps,
             "config": {"workload": "B=%d matrices %dx%d, logits N(0,1), %d iterations" % (B, n, n, n_iter),
                        "l2": "inputs larger than L2" if flush is None else "L2 flushed before each step"}}

@@ -266,7 +266,9 @@ int flashot_ot_hvp_x(const float *X, const float *Y, const float *a, const float
  * Needs no workspace. Each matrix's largest logit is subtracted before exp (P does not
  * change); logits that lie more than about 87 below a matrix's largest underflow to 0 in
  * fp32, and a row or column of such zeros makes that matrix's P undefined. The scalings use
- * the SFU reciprocal (rcp.approx, about 1 ulp).
+ * one SFU reciprocal (rcp.approx, about 1 ulp) per pair of sums, 1/s0 = s1 / (s0 s1), so
+ * products of two row (or column) sums must stay in the fp32 range: logits of one matrix
+ * should span less than about 40.
  */
 int flashot_sinkhorn_knopp_batched(const float *H, int64_t B, int n, int n_iter, float *P,
                                    flashot_stream_t stream);
