@@ -406,22 +406,47 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
   const int64_t kk = (mode == kWsumHadamard) ? 1 : k;
   // One output column (a transport-vector application): a narrow accumulator.
   const bool narrow = (mode == kWsumApply && k == 1);
-  const int KO = narrow ? 1 : 32;
-  dim3 grid((unsigned)ceil_div(n_rows, kFmaThreads), (unsigned)ceil_div(kk, KO));
+  // Up to 8 output columns (apply / curvature passes of small d): an 8-wide accumulator.
+  const bool mid = g.small && !narrow && k <= 8 && (mode == kWsumApply || mode == kWsumHessT);
+  const int KO = narrow ? 1 : (mid ? 8 : 32);
+  // Rows per thread of the small-d kernel: 4 for the narrow pass (2 when d_pad > 16), 2 for
+  // the 8-wide one.
+  const int R = (g.small && narrow) ? (g.dpf <= 16 ? 4 : 2) : (mid ? 2 : 1);
+  const int64_t row_blocks = ceil_div(n_rows, (int64_t)kFmaThreads * R);
+  const int64_t k_groups = ceil_div(kk, KO);
   const int n_tiles = (int)(cols_pad / 32);
+  // Column splits for the small-d kernel when rows x output groups give fewer than 8 CTAs
+  // per SM; the partials ([split][row][kp] floats) live in the workspace's partial region.
+  int n_splits = 1, tps = n_tiles, kp = 0;
+  if (g.small) {
+    kp = (int)(mode == kWsumHadamard ? 1 : k_groups * KO) + 1;
+    const int64_t cap_floats = (int64_t)kMaxSplits * std::max(g.n_pad, g.m_pad) * 2;
+    const int64_t rows_pad_ = x_rows ? g.n_pad : g.m_pad;
+    const int64_t max_splits = std::min<int64_t>(cap_floats / (rows_pad_ * kp), n_tiles);
+    const int64_t want = ceil_div((int64_t)c.sms * 8, row_blocks * k_groups);
+    n_splits = (int)std::max<int64_t>(1, std::min(want, max_splits));
+    tps = (int)ceil_div(n_tiles, n_splits);
+    n_splits = (int)ceil_div(n_tiles, tps);
+  }
+  float* part = n_splits > 1 ? c.at<float>(c.L.partial) : nullptr;
+  const int64_t rows_pad = x_rows ? g.n_pad : g.m_pad;
+  dim3 grid((unsigned)row_blocks, (unsigned)k_groups, (unsigned)n_splits);
+  {
   TraceScope ts_(FLASHOT_KERNEL_WSUM, c.st);
   if (g.small) {
-#define FLASHOT_WSUM_SMALL(DPV, MODEV, KOV)                                                  \
-  wsum_fma_small_kernel<DPV, MODEV, KOV><<<grid, kFmaThreads, 0, c.st>>>(                    \
+#define FLASHOT_WSUM_SMALL(DPV, MODEV, KOV, RV)                                              \
+  wsum_fma_small_kernel<DPV, MODEV, KOV, RV><<<grid, kFmaThreads, 0, c.st>>>(                \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
-      out, ldo, rowU)
-#define FLASHOT_WSUM_MODES(DPV)                                             \
-  case DPV:                                                                 \
-    if (narrow) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 1);                     \
-    else if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 32);   \
-    else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad, 32);     \
-    else if (mode == kWsumHessT) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 32);   \
-    else FLASHOT_WSUM_SMALL(DPV, kWsumHadamard, 32);                        \
+      out, ldo, rowU, tps, part, rows_pad, kp)
+#define FLASHOT_WSUM_MODES(DPV)                                                     \
+  case DPV:                                                                         \
+    if (narrow) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 1, ((DPV) <= 16 ? 4 : 2));      \
+    else if (mid && mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 8, 2);  \
+    else if (mid) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 8, 2);                        \
+    else if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 32, 1);        \
+    else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad, 32, 1);          \
+    else if (mode == kWsumHessT) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 32, 1);        \
+    else FLASHOT_WSUM_SMALL(DPV, kWsumHadamard, 32, 1);                             \
     break;
     switch (g.dpf) {
       FLASHOT_WSUM_MODES(4)
@@ -447,6 +472,22 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
     else if (mode == kWsumHessT) FLASHOT_WSUM_GENERIC(kWsumHessT, 32);
     else FLASHOT_WSUM_GENERIC(kWsumHadamard, 32);
 #undef FLASHOT_WSUM_GENERIC
+  }
+  }
+  if (n_splits > 1) {
+    int rc = launch_check();
+    if (rc != FLASHOT_OK) return rc;
+    const int64_t total = n_rows * kk;
+    TraceScope ts2_(FLASHOT_KERNEL_OTHER, c.st);
+#define FLASHOT_WSUM_REDUCE(MODEV)                                                          \
+  wsum_split_reduce_kernel<MODEV><<<grid1(total, 256), 256, 0, c.st>>>(part, n_splits, rows_pad, \
+                                                                    kp, n_rows, k, rowW, X,   \
+                                                                    g.d, out, ldo)
+    if (mode == kWsumApply) FLASHOT_WSUM_REDUCE(kWsumApply);
+    else if (mode == kWsumGrad) FLASHOT_WSUM_REDUCE(kWsumGrad);
+    else if (mode == kWsumHessT) FLASHOT_WSUM_REDUCE(kWsumHessT);
+    else FLASHOT_WSUM_REDUCE(kWsumHadamard);
+#undef FLASHOT_WSUM_REDUCE
   }
   return launch_check();
 }

@@ -220,7 +220,12 @@ __device__ __forceinline__ void stage_v_tile(float (*vs)[KO + 1], const float* _
 //  HessT:    out_i[o] = sum_j w_ij <u_i, q_j> V_j[o], u_i the rows of rowU (packed like
 //            rowP) and V the column points
 // ---------------------------------------------------------------------------------------
-template <int DP, int MODE, int KO = 32>
+// Column splits: with part != NULL, CTA (x, y, z) covers the column tiles
+// [z tps, (z+1) tps) and writes its raw sums to part[(z rows_pad + row) kp + o] (and sum w
+// or the Hadamard sum to column kp - 1); wsum_split_reduce_kernel adds the splits in a fixed
+// order and applies the mode's epilogue. This gives the small-d passes enough CTAs when the
+// rows alone would leave most SMs idle.
+template <int DP, int MODE, int KO = 32, int R = 1>
 __global__ void __launch_bounds__(kFmaThreads)
 wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                       const float* __restrict__ colBias, const float* __restrict__ rowBias,
@@ -228,31 +233,49 @@ wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ 
                       const float* __restrict__ V, int64_t ldv, int64_t k,
                       const float* __restrict__ rowW, const float* __restrict__ Xrow,
                       int64_t d, float* __restrict__ out, int64_t ldo,
-                      const float* __restrict__ rowU) {
+                      const float* __restrict__ rowU, int tiles_per_split = 0,
+                      float* __restrict__ part = nullptr, int64_t rows_pad = 0, int kp = 0) {
+  // R rows per thread (rows tid + r kFmaThreads of the CTA's block of kFmaThreads R rows):
+  // every staged column is read from shared memory once for R rows.
   constexpr int Q = DP / 4;
   constexpr bool kHess = (MODE == kWsumHessT);
   __shared__ float4 ys[32 * Q];
   __shared__ float cs[32];
   __shared__ float vs[32][KO + 1];
   const int tid = threadIdx.x;
-  const int64_t row = (int64_t)blockIdx.x * kFmaThreads + tid;
+  const int64_t row0 = (int64_t)blockIdx.x * kFmaThreads * R + tid;
   const int64_t o0 = (int64_t)blockIdx.y * KO;
-  float4 x[Q], u[kHess ? Q : 1];
-  const int64_t rr = row < n_rows ? row : 0;
-  const float4* xr = reinterpret_cast<const float4*>(rowP + rr * DP);
+  float4 x[R][Q], u[R][kHess ? Q : 1];
+  float rb[R];
 #pragma unroll
-  for (int q = 0; q < Q; ++q) x[q] = xr[q];
-  if constexpr (kHess) {
-    const float4* ur = reinterpret_cast<const float4*>(rowU + rr * DP);
+  for (int r = 0; r < R; ++r) {
+    const int64_t row = row0 + (int64_t)r * kFmaThreads;
+    const int64_t rr = row < n_rows ? row : 0;
+    const float4* xr = reinterpret_cast<const float4*>(rowP + rr * DP);
 #pragma unroll
-    for (int q = 0; q < Q; ++q) u[q] = ur[q];
+    for (int q = 0; q < Q; ++q) x[r][q] = xr[q];
+    if constexpr (kHess) {
+      const float4* ur = reinterpret_cast<const float4*>(rowU + rr * DP);
+#pragma unroll
+      for (int q = 0; q < Q; ++q) u[r][q] = ur[q];
+    }
+    rb[r] = row < n_rows ? rowBias[row] : neg_inf();
   }
-  const float rb = row < n_rows ? rowBias[row] : neg_inf();
-  float acc[KO];
+  float acc[R][KO];
+  float sumw[R], had[R];
 #pragma unroll
-  for (int o = 0; o < KO; ++o) acc[o] = 0.0f;
-  float sumw = 0.0f, had = 0.0f;
-  for (int t = 0; t < n_col_tiles; ++t) {
+  for (int r = 0; r < R; ++r) {
+    sumw[r] = 0.0f;
+    had[r] = 0.0f;
+#pragma unroll
+    for (int o = 0; o < KO; ++o) acc[r][o] = 0.0f;
+  }
+  int t_begin = 0, t_end = n_col_tiles;
+  if (part != nullptr) {
+    t_begin = (int)blockIdx.z * tiles_per_split;
+    t_end = min(n_col_tiles, t_begin + tiles_per_split);
+  }
+  for (int t = t_begin; t < t_end; ++t) {
     __syncthreads();
     const float4* src = reinterpret_cast<const float4*>(colP + (int64_t)t * 32 * DP);
     for (int e = tid; e < 32 * Q; e += kFmaThreads) ys[e] = src[e];
@@ -262,26 +285,84 @@ wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ 
     __syncthreads();
 #pragma unroll 4
     for (int c = 0; c < 32; ++c) {
-      float dot = 0.0f;
+      float4 y[Q];
 #pragma unroll
-      for (int q = 0; q < Q; ++q) dot = dot4(x[q], ys[c * Q + q], dot);
-      float w = ex2(fmaf(kappa, dot, cs[c]) + rb);
-      if constexpr (MODE == kWsumHadamard) {
-        had = fmaf(w, dot, had);
-      } else {
-        if constexpr (kHess) {
-          float tu = 0.0f;
+      for (int q = 0; q < Q; ++q) y[q] = ys[c * Q + q];
+      const float cc = cs[c];
+      float vv[MODE == kWsumHadamard ? 1 : KO];
+      if constexpr (MODE != kWsumHadamard) {
 #pragma unroll
-          for (int q = 0; q < Q; ++q) tu = dot4(u[q], ys[c * Q + q], tu);
-          w *= tu;
+        for (int o = 0; o < KO; ++o) vv[o] = vs[c][o];
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float dot = 0.0f;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) dot = dot4(x[r][q], y[q], dot);
+        float w = ex2(fmaf(kappa, dot, cc) + rb[r]);
+        if constexpr (MODE == kWsumHadamard) {
+          had[r] = fmaf(w, dot, had[r]);
+        } else {
+          if constexpr (kHess) {
+            float tu = 0.0f;
+#pragma unroll
+            for (int q = 0; q < Q; ++q) tu = dot4(u[r][q], y[q], tu);
+            w *= tu;
+          }
+#pragma unroll
+          for (int o = 0; o < KO; ++o) acc[r][o] = fmaf(w, vv[o], acc[r][o]);
+          if constexpr (MODE == kWsumGrad) sumw[r] += w;
         }
-#pragma unroll
-        for (int o = 0; o < KO; ++o) acc[o] = fmaf(w, vs[c][o], acc[o]);
-        if constexpr (MODE == kWsumGrad) sumw += w;
       }
     }
   }
-  if (row < n_rows) wsum_store<MODE, KO>(acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int64_t row = row0 + (int64_t)r * kFmaThreads;
+    if (row >= n_rows) continue;
+    if (part != nullptr) {
+      float* pr = part + ((int64_t)blockIdx.z * rows_pad + row) * kp;
+      if constexpr (MODE != kWsumHadamard) {
+#pragma unroll
+        for (int o = 0; o < KO; ++o)
+          if (o0 + o < kp - 1) pr[o0 + o] = acc[r][o];
+      }
+      if (blockIdx.y == 0) pr[kp - 1] = (MODE == kWsumHadamard) ? had[r] : sumw[r];
+    } else {
+      wsum_store<MODE, KO>(acc[r], sumw[r], had[r], row, o0, k, rowW, Xrow, d, out, ldo);
+    }
+  }
+}
+
+// Sum of the column splits of a weighted-sum pass (fixed order) and the mode's epilogue
+// (see wsum_store). One thread per (row, output column); column kp - 1 holds sum w or the
+// Hadamard sum.
+template <int MODE>
+__global__ void wsum_split_reduce_kernel(const float* __restrict__ part, int n_splits,
+                                         int64_t rows_pad, int kp, int64_t n_rows, int64_t k,
+                                         const float* __restrict__ rowW,
+                                         const float* __restrict__ Xrow, int64_t d,
+                                         float* __restrict__ out, int64_t ldo) {
+  const int64_t kk = (MODE == kWsumHadamard) ? 1 : k;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n_rows * kk;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = e / kk, o = e - row * kk;
+    const int col = (MODE == kWsumHadamard) ? kp - 1 : (int)o;
+    float acc = 0.0f;
+    for (int sp = 0; sp < n_splits; ++sp) acc += part[((int64_t)sp * rows_pad + row) * kp + col];
+    if constexpr (MODE == kWsumGrad) {
+      float sumw = 0.0f;
+      for (int sp = 0; sp < n_splits; ++sp)
+        sumw += part[((int64_t)sp * rows_pad + row) * kp + kp - 1];
+      const float a = rowW[row];
+      const float inv = sumw > 0.0f ? 1.0f / sumw : 0.0f;
+      out[row * ldo + o] = a > 0.0f ? 2.0f * a * (Xrow[row * d + o] - acc * inv) : 0.0f;
+    } else if constexpr (MODE == kWsumHadamard) {
+      out[row] = acc;
+    } else {
+      out[row * ldo + o] = acc;
+    }
+  }
 }
 
 // Weighted sums, any d_pad (multiple of 32): dots for 32 columns accumulated over 32-wide

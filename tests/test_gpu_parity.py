@@ -153,7 +153,13 @@ def _potentials(pr, iters=30):
 
 
 @pytest.mark.parametrize("precision", PRECS_SMALL_D)
-@pytest.mark.parametrize("n,m,d,k", [(130, 257, 3, 5), (300, 200, 16, 40), (129, 131, 64, 33)])
+@pytest.mark.parametrize("n,m,d,k", [(130, 257, 3, 5), (300, 200, 16, 40), (129, 131, 64, 33),
+                                     # transport-vector (k = 1) passes: several rows per
+                                     # thread, column splits, ragged row blocks
+                                     (1000, 700, 3, 1), (513, 1200, 20, 1), (700, 500, 30, 1),
+                                     (2000, 3000, 16, 2), (300, 257, 64, 1),
+                                     # 8-wide accumulator, two rows per thread
+                                     (1500, 900, 3, 5), (777, 1300, 28, 8)])
 def test_transport_apply_matches_oracle(cuda_lib, precision, n, m, d, k):
     lds = cuda_lib
     pr = make_problem(n, m, d, x_dist="normal_over_d", weights="dirichlet1", eps=0.1,
