@@ -355,7 +355,10 @@ def run_other_workload(args):
     peaks, _ = load_peaks()
     clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
     avg = ms_hot / max(n_hot, 1) / 1e3
-    per_launch_scores = locals().get("per_launch_override", nm)
+    # Scores per timed launch of the hot kernel class: the streaming solve launches one LSE
+    # pass per half-step; the single-launch cluster solve covers the whole solve.
+    per_launch_scores = locals().get("per_launch_override",
+                                     scores_per_step * args.steps / max(n_hot, 1))
     if prec == "fp32":
         roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
                 "peak": N_SMS * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)"}

@@ -6,9 +6,10 @@
 // single kernel (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract: the
 // f- and g-updates as row-wise log-sum-exps; arithmetic identical to the CUDA-core path):
 //  - every CTA keeps X, Y, |x|^2, |y|^2, log2 a, log2 b and full copies of f and g;
-//  - for an f-update each CTA computes its slice of rows, each row split over kTPR threads
-//    whose (max, sum) pairs are merged with warp shuffles, and stores its f values into the
-//    shared memory of every CTA of the cluster (DSMEM);
+//  - for an f-update each CTA computes its slice of rows: lanes own rows, warps own slices
+//    of the columns, and the per-warp (max, sum) pairs of a row are merged through shared
+//    memory; the CTA then stores its f values into the shared memory of every CTA of the
+//    cluster (DSMEM);
 //  - a cluster barrier (release / acquire) separates the half-steps.
 // All CTAs of a cluster are co-scheduled, and every CTA reaches every barrier, so the
 // barriers need no time limit.
@@ -26,7 +27,6 @@ namespace small {
 
 constexpr int kCluster = 8;
 constexpr int kThreads = 512;
-constexpr int kTPR = 4;  // threads per row
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -46,64 +46,106 @@ __device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v)
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
 }
 
+// Rows per lane in a half-step (registers hold R points of DP floats).
+template <int DP>
+constexpr int rows_per_lane() {
+  return DP <= 16 ? 2 : 1;
+}
+
 // One half-step for the rows [r0, r1) of the side P against the nq points of the other
 // side Q, whose column biases cq fold in their potential, norm and log-weight:
 // out_i = nrmp_i - eps ln2 LSE2_j(kappa <p_i, q_j> + cq_j), stored into every CTA.
+// Lanes own rows (R per lane, 32 R per group) and warps own column slices, so each column's
+// point and bias are one broadcast shared-memory read per warp; each warp keeps an online
+// (max, sum) per row over its slice in chunks of 8 columns, and the kWarps partials of a row
+// are merged through shared memory before the row's value is broadcast to the cluster.
 template <int DP>
 __device__ __forceinline__ void half_step(const float* __restrict__ P, const float* __restrict__ Q,
                                           int nq, const float* __restrict__ cq,
                                           const float* __restrict__ nrmp, int r0, int r1,
-                                          float kappa, float eps, float* out) {
-  const int tid = threadIdx.x;
-  for (int base = r0; base < r1; base += kThreads / kTPR) {
-    const int i = base + tid / kTPR;
-    const int part = tid % kTPR;
-    float M = kNegBig, S = 0.0f;
-    if (i < r1) {
-      float x[DP];
+                                          float kappa, float eps, float* out, float2* red) {
+  constexpr int R = rows_per_lane<DP>();
+  constexpr int kWarps = kThreads / 32;
+  constexpr int Q4 = DP / 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cs = (nq + kWarps - 1) / kWarps;
+  const int j0 = min(nq, warp * cs), j1 = min(nq, j0 + cs);
+  for (int base = r0; base < r1; base += 32 * R) {
+    float4 x[R][Q4];
+    float M[R], S[R];
 #pragma unroll
-      for (int c = 0; c < DP; ++c) x[c] = P[i * DP + c];
-      for (int j0 = part * 8; j0 < nq; j0 += kTPR * 8) {
-        float s[8];
+    for (int r = 0; r < R; ++r) {
+      const int i = base + lane + 32 * r;
+      const float4* src = reinterpret_cast<const float4*>(P + (i < r1 ? i : r0) * DP);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = j0 + u;
-          float dot = 0.0f;
-          if (j < nq) {
+      for (int q = 0; q < Q4; ++q) x[r][q] = src[q];
+      M[r] = kNegBig;
+      S[r] = 0.0f;
+    }
+    for (int j = j0; j < j1; j += 8) {
+      float sc[R][8];
 #pragma unroll
-            for (int c = 0; c < DP; ++c) dot = fmaf(x[c], Q[j * DP + c], dot);
-            s[u] = fmaf(kappa, dot, cq[j]);
-          } else {
-            s[u] = neg_inf();
+      for (int u = 0; u < 8; ++u) {
+        const int jj = j + u;
+        if (jj < j1) {
+          const float4* yq = reinterpret_cast<const float4*>(Q + jj * DP);
+          float4 y[Q4];
+#pragma unroll
+          for (int q = 0; q < Q4; ++q) y[q] = yq[q];
+          const float c = cq[jj];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float dot = 0.0f;
+#pragma unroll
+            for (int q = 0; q < Q4; ++q) {
+              dot = fmaf(x[r][q].x, y[q].x, dot);
+              dot = fmaf(x[r][q].y, y[q].y, dot);
+              dot = fmaf(x[r][q].z, y[q].z, dot);
+              dot = fmaf(x[r][q].w, y[q].w, dot);
+            }
+            sc[r][u] = fmaf(kappa, dot, c);
           }
-        }
-        float mx = s[0];
+        } else {
 #pragma unroll
-        for (int u = 1; u < 8; ++u) mx = fmaxf(mx, s[u]);
-        if (mx > M) {
-          S *= ex2(M - mx);
-          M = mx;
+          for (int r = 0; r < R; ++r) sc[r][u] = neg_inf();
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float mx = sc[r][0];
+#pragma unroll
+        for (int u = 1; u < 8; ++u) mx = fmaxf(mx, sc[r][u]);
+        if (mx > M[r]) {
+          S[r] *= ex2(M[r] - mx);
+          M[r] = mx;
         }
         float acc = 0.0f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) acc += ex2(s[u] - M);
-        S += acc;
+        for (int u = 0; u < 8; ++u) acc += ex2(sc[r][u] - M[r]);
+        S[r] += acc;
       }
     }
-    // Merge the kTPR partial (max, sum) pairs of a row (adjacent lanes).
 #pragma unroll
-    for (int o = 1; o < kTPR; o <<= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, o);
-      const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
-      const float Mn = fmaxf(M, M2);
-      S = S * ex2(M - Mn) + S2 * ex2(M2 - Mn);
-      M = Mn;
+    for (int r = 0; r < R; ++r) red[warp * 32 * R + lane + 32 * r] = make_float2(M[r], S[r]);
+    __syncthreads();
+    if (tid < 32 * R) {
+      const int i = base + tid;
+      if (i < r1) {
+        float Mx = kNegBig;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, red[w * 32 * R + tid].x);
+        float Sm = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float2 p = red[w * 32 * R + tid];
+          Sm += p.y * ex2(p.x - Mx);
+        }
+        const float L = Mx + log2f(Sm);
+        const float v = nrmp[i] - eps * kLn2 * L;
+        for (uint32_t rk = 0; rk < (uint32_t)kCluster; ++rk) st_cluster(out + i, rk, v);
+      }
     }
-    if (i < r1 && part == 0) {
-      const float L = M + log2f(S);
-      const float v = nrmp[i] - eps * kLn2 * L;
-      for (uint32_t r = 0; r < (uint32_t)kCluster; ++r) st_cluster(out + i, r, v);
-    }
+    __syncthreads();
   }
 }
 
@@ -125,6 +167,8 @@ small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
   float* wa = lb + m;             // n
   float* wb = wa + n;             // m
   float* cb = wb + m;             // max(n, m): bias of the current pass
+  // kThreads/32 x 32 R (max, sum) partials of a row group, 8-byte aligned after cb.
+  float2* red = reinterpret_cast<float2*>(cb + ((n > m ? n : m) + 1) / 2 * 2);
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_rank();
 
@@ -166,12 +210,12 @@ small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
       // f-update: bias of the columns (Y side) from g
       for (int j = tid; j < m; j += kThreads) cb[j] = (ga[j] - be[j]) * inv + lb[j];
       __syncthreads();
-      half_step<DP>(Xs, Ys, m, cb, al, fr0, fr1, kappa, eps, fa);
+      half_step<DP>(Xs, Ys, m, cb, al, fr0, fr1, kappa, eps, fa, red);
       cluster_sync();
       // g-update: bias of the columns (X side) from f
       for (int i = tid; i < n; i += kThreads) cb[i] = (fa[i] - al[i]) * inv + la[i];
       __syncthreads();
-      half_step<DP>(Ys, Xs, n, cb, be, gr0, gr1, kappa, eps, ga);
+      half_step<DP>(Ys, Xs, n, cb, be, gr0, gr1, kappa, eps, ga, red);
       cluster_sync();
     }
   }
@@ -198,7 +242,10 @@ small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
 }
 
 size_t smem_bytes(int64_t n, int64_t m, int dp) {
-  return (size_t)((n + m) * dp + 5 * (n + m) + (n > m ? n : m)) * sizeof(float);
+  const int64_t mx = n > m ? n : m;
+  const int64_t floats = (n + m) * dp + 5 * (n + m) + (mx + 1) / 2 * 2;
+  // partials: kThreads/32 warps x 32 rows-per-group x up to 2 rows per lane, float2 each
+  return (size_t)floats * sizeof(float) + (size_t)(kThreads / 32) * 64 * sizeof(float2);
 }
 
 template <int DP>
