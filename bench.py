@@ -885,16 +885,17 @@ def run_gpu(args):
 
 def run_profile_driver(args):
     """A short, self-contained sequence of the hot kernel for profilers: one pack, then
-    alternating f- and g-updates of the workload (optionally with n = m overridden)."""
+    alternating f- and g-updates of --workload (default: the 50k benchmark workload;
+    optionally with n = m overridden)."""
     import torch
 
     import log_domain_sinkhorn_gb300 as lds
     from workloads import make_problem, WORKLOADS
-    spec = dict(WORKLOADS[WORKLOAD_IDX])
+    spec = dict(WORKLOADS[args.workload])
     if args.n:
         spec["n"] = spec["m"] = args.n
     spec.pop("k", None)
-    pr = make_problem(seed=1000 + WORKLOAD_IDX, **spec)
+    pr = make_problem(seed=1000 + args.workload, **spec)
     X = torch.from_numpy(pr.X).cuda()
     Y = torch.from_numpy(pr.Y).cuda()
     eps = float(pr.eps_schedule[0])
