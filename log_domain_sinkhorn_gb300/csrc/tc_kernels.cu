@@ -103,6 +103,41 @@ __device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __rest
   S += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
+// The same for biases staged in shared memory (plain loads).
+__device__ __forceinline__ void lse_chunk64_sb(float (&v)[64], const float4* cb, float kappa,
+                                               float& M, float& S) {
+  float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
+#pragma unroll
+  for (int j = 0; j < 64; j += 8) {
+    const float4 b4 = cb[j / 4];
+    const float4 b5 = cb[j / 4 + 1];
+    v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
+    v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
+    v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
+    v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
+    v[j + 4] = fmaf(kappa, v[j + 4], b5.x);
+    v[j + 5] = fmaf(kappa, v[j + 5], b5.y);
+    v[j + 6] = fmaf(kappa, v[j + 6], b5.z);
+    v[j + 7] = fmaf(kappa, v[j + 7], b5.w);
+    m0 = ptx::max3(m0, v[j + 0], v[j + 1]);
+    m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
+    m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
+    m3 = ptx::max3(m3, v[j + 6], v[j + 7]);
+  }
+  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
+  if (mx > M) {
+    S *= ex2(M - mx);
+    M = mx;
+  }
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 64; j += 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s[u] += ex2(v[j + u] - M);
+  }
+  S += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
 // ---------------------------------------------------------------------------------------
 // LSE pass: partial[slot * ld + row] = (max_j s2_ij, sum_j 2^(s2_ij - max)) over the
 // column tiles of this CTA's range, s2_ij = kappa <p_i, q_j> + colBias_j.
@@ -111,7 +146,11 @@ __device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __rest
 // stage holds one 256-row x 128-byte K-chunk of the column cloud; otherwise each stage
 // holds a K-chunk of both.
 // ---------------------------------------------------------------------------------------
-template <bool kBF16, bool kARes>
+// kStageBias: the epilogue copies each tile's column biases into shared memory one tile
+// ahead (cp.async). Used for short contractions, where the epilogue bounds a tile and a
+// direct read would wait on L2 (L1 is small next to the operand stages); long contractions
+// keep all shared memory for operand stages and read the biases directly.
+template <bool kBF16, bool kARes, bool kStageBias>
 __global__ void __launch_bounds__(kLseThreads, 1)
 lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
@@ -119,6 +158,9 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
               unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
+  // Column biases of the current and the next tile, per epilogue warp (its 128 columns).
+  __shared__ __align__(16) float bias_s[kStageBias ? kLseEpiThreads / 32 : 1][2]
+                                       [kStageBias ? 128 : 4];
   constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
   constexpr uint32_t kBChunk = 2u * kChunk;  // 256 rows x 128 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -252,6 +294,58 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    if constexpr (kStageBias) {
+    uint32_t ab = 0, acc_ph = 0;
+    bool ok = true;
+    // The warp's 128 biases of a tile (512 B, 16 per lane) are copied global -> shared with
+    // cp.async one tile ahead into one of two slots.
+    float (*bslot)[kStageBias ? 128 : 4] = bias_s[kStageBias ? warp - 2 : 0];
+    auto stage_bias = [&](int64_t tile, int slot) {
+      const float* src = colBias + (tile % NT) * kLseBN + h * 128 + lane * 4;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       ptx::smem_u32(&bslot[slot][lane * 4])),
+                   "l"(src)
+                   : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int bs = 0;
+    if (t_begin < t_end) stage_bias(t_begin, 0);
+    for (int64_t t = t_begin; ok && t < t_end;) {
+      const int64_t rt = t / NT;
+      const int64_t seg_end = min(t_end, (rt + 1) * NT);
+      float M = kNegBig, S = 0.0f;
+      for (int64_t tt = t; tt < seg_end; ++tt) {
+        if (tt + 1 < t_end) {
+          stage_bias(tt + 1, bs ^ 1);
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncwarp();
+        const float4* cb = reinterpret_cast<const float4*>(bslot[bs]);
+        if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
+        float v[64];
+        ptx::tmem_ld_x64_sync(taddr, v);
+        lse_chunk64_sb(v, cb, kappa, M, S);
+        ptx::tmem_ld_x64_sync(taddr + 64, v);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
+        if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+        lse_chunk64_sb(v, cb + 16, kappa, M, S);
+        __syncwarp();  // every lane is done with bslot[bs] before it is refilled
+        bs ^= 1;
+      }
+      if (!ok) break;
+      const int64_t row = rt * kBM + q * 32 + lane;
+      const int64_t slot = 2 * (cta - sk_owner(rt * NT, T, G)) + h;
+      if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
+      t = seg_end;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy outlives the CTA
+    if (!ok) flag_error(ctl, status);
+    } else {
     uint32_t ab = 0, acc_ph = 0;
     bool ok = true;
     if (t_begin < t_end && lane < 4)   // 512 B of bias per half-tile: one line per lane
@@ -284,6 +378,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       t = seg_end;
     }
     if (!ok) flag_error(ctl, status);
+    }
   }
 
   ptx::tc_fence_before();
@@ -651,18 +746,20 @@ int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t 
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
 
-template <bool kBF16, bool kARes>
+template <bool kBF16, bool kARes, bool kStageBias>
 static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float* colBias,
                       int64_t n_rows, int64_t NT, int64_t T, int kc, int64_t G, float kappa,
                       float2* partial, int64_t ld, unsigned* status, cudaStream_t st) {
-  const int ctrl = (int)sizeof(Ctrl);
+  // Static shared memory: the control block and the staged column biases.
+  const int ctrl = (int)sizeof(Ctrl) +
+                   (kStageBias ? kLseEpiThreads / 32 * 2 * 128 : 2 * 4) * (int)sizeof(float);
   const int a_bytes = kARes ? kc * kChunk : 0;
   const int stage_bytes = kARes ? 2 * kChunk : 3 * kChunk;
   const int budget = kSmemLimit - ctrl - 1024 - a_bytes;
   const int stages = std::min(kMaxStages, budget / stage_bytes);
   if (stages < 2) return FLASHOT_ERR_INVALID_ARG;
   const int dyn = a_bytes + stages * stage_bytes + 1024;
-  auto kern = lse_tc_kernel<kBF16, kARes>;
+  auto kern = lse_tc_kernel<kBF16, kARes, kStageBias>;
   int rc = set_smem(kern, dyn);
   if (rc != FLASHOT_OK) return rc;
   {
@@ -694,16 +791,17 @@ int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colB
   info->sk_G = G;
   info->sk_NT = NT;
   const bool ares = kc * kChunk <= 128 * 1024;
-  if (bf16) {
-    return ares ? launch_lse<true, true>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
-                                         rows_pad, status, st)
-                : launch_lse<true, false>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
-                                          rows_pad, status, st);
-  }
-  return ares ? launch_lse<false, true>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
-                                        rows_pad, status, st)
-              : launch_lse<false, false>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial,
-                                         rows_pad, status, st);
+  // Stage the biases in shared memory when the contraction is short (at most 6 K-chunks,
+  // e.g. d <= 192 in bf16 or d <= 64 in split tf32: the epilogue bounds the tile, and at
+  // least 3 operand stages still fit).
+  const bool stage = kc <= 6;
+#define FLASHOT_LAUNCH_LSE(BF, AR, SB)                                                        \
+  launch_lse<BF, AR, SB>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial, rows_pad, \
+                         status, st)
+  if (stage) return bf16 ? FLASHOT_LAUNCH_LSE(true, true, true) : FLASHOT_LAUNCH_LSE(false, true, true);
+  if (bf16) return ares ? FLASHOT_LAUNCH_LSE(true, true, false) : FLASHOT_LAUNCH_LSE(true, false, false);
+  return ares ? FLASHOT_LAUNCH_LSE(false, true, false) : FLASHOT_LAUNCH_LSE(false, false, false);
+#undef FLASHOT_LAUNCH_LSE
 }
 
 template <bool kBF16, int kMode, int kKV>
