@@ -323,9 +323,11 @@ def run_other_workload(args):
             lds.sinkhorn_divergence(X, Y, a, b, sched, pr.iters_per_stage, precision=prec,
                                     schedule=args.schedule, out=res, workspace=dws)
         units_per_step, unit = 1, "divergences/s"
-        scores_per_step = 2 * (n * m + n * n + m * m) * pr.total_iters
+        # Scores evaluated: the X-Y solve runs two passes per iteration; with the symmetric
+        # schedule the self-transport solves (X-X, Y-Y) run one (f == g throughout).
+        self_passes = 1 if args.schedule == "symmetric" else 2
+        scores_per_step = (2 * n * m + self_passes * (n * n + m * m)) * pr.total_iters
         hot = lds.KernelTimer.LSE
-        per_launch_override = (n * m + n * n + m * m) / 3.0
     else:
         def step():
             lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
@@ -357,8 +359,7 @@ def run_other_workload(args):
     avg = ms_hot / max(n_hot, 1) / 1e3
     # Scores per timed launch of the hot kernel class: the streaming solve launches one LSE
     # pass per half-step; the single-launch cluster solve covers the whole solve.
-    per_launch_scores = locals().get("per_launch_override",
-                                     scores_per_step * args.steps / max(n_hot, 1))
+    per_launch_scores = scores_per_step * args.steps / max(n_hot, 1)
     if prec == "fp32":
         roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
                 "peak": N_SMS * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)"}

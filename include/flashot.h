@@ -75,7 +75,9 @@ typedef struct CUstream_st *flashot_stream_t;
 #define FLASHOT_REUSE_PACK  0x20
 /* solve: symmetric (averaged) schedule, f' = (f + F(g))/2 and g' = (g + G(f))/2 from the
  * same previous iterate (the review's "Strengths": symmetric-vs-alternating comparison).
- * Starts from f = g = 0, or with FLASHOT_WARM_START from the f and g passed in. */
+ * Starts from f = g = 0, or with FLASHOT_WARM_START from the f and g passed in. When X == Y
+ * and a == b (the same pointers) without a warm start, f == g at every iteration, and the
+ * solve runs one pass per iteration instead of two. */
 #define FLASHOT_SYMMETRIC   0x40
 
 /* ---- library information ------------------------------------------------------------ */

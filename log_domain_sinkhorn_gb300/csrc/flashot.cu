@@ -680,16 +680,27 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
       if (e == cudaSuccess) e = cudaMemsetAsync(g, 0, (size_t)m * sizeof(float), c.st);
       if (e != cudaSuccess) return cuda_fail(e);
     }
+    // A self-transport problem (the same cloud and weights on both sides, e.g. the OT(a, a)
+    // terms of the debiased divergence) started from f = g keeps f == g: the g-update is
+    // the f-update's arithmetic on identical inputs. One pass per iteration then suffices,
+    // and g is copied from f at the end.
+    const bool self = X == Y && a == b && n == m && !(flags & FLASHOT_WARM_START);
     for (int s = 0; s < n_stages; ++s) {
       const float eps = eps_sched[s];
       for (int it = 0; it < iters_per_stage; ++it) {
-        if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
-        if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+        if ((rc = launch_bias(c, self ? f : g, false, eps)) != FLASHOT_OK) return rc;
+        if (!self && (rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
         if ((rc = run_lse_pass(c, true, eps, eps, f, false, nullptr, true)) != FLASHOT_OK)
           return rc;
-        if ((rc = run_lse_pass(c, false, eps, eps, g, false, nullptr, true)) != FLASHOT_OK)
+        if (!self && (rc = run_lse_pass(c, false, eps, eps, g, false, nullptr, true)) !=
+                         FLASHOT_OK)
           return rc;
       }
+    }
+    if (self) {
+      cudaError_t e = cudaMemcpyAsync(g, f, (size_t)m * sizeof(float), cudaMemcpyDeviceToDevice,
+                                      c.st);
+      if (e != cudaSuccess) return cuda_fail(e);
     }
   } else {
   // Initial F-step bias from g (warm start) or g = 0.
