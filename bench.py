@@ -80,6 +80,9 @@ def parse_args():
                         "(B = 2^24 unless --sk-batch, 20 iterations)")
     p.add_argument("--sk-batch", type=int, default=1 << 24)
     p.add_argument("--sk-n", type=int, default=4)
+    p.add_argument("--graph", action="store_true",
+                   help="supplementary solve lines: also capture one solve into a CUDA graph "
+                        "and time its replays")
     p.add_argument("--workload", type=int, default=WORKLOAD_IDX, choices=[1, 2, 3, 4, 5],
                    help="3 (default) is the benchmark line; 1, 2, 4, 5 print supplementary "
                         "lines for the other point-cloud workloads")
@@ -380,6 +383,35 @@ def run_other_workload(args):
     roof["sfu_frac"] = (per_launch_scores / avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk)
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
+    graph = None
+    if args.graph and idx != 5 and not args.divergence:
+        # The same solve captured once into a CUDA graph (torch's capture stream is the
+        # current stream the binding passes) and replayed: no per-launch host work.
+        cg = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()  # the first call on a stream may set kernel attributes; keep it out
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        l0 = lds.launch_count()
+        with torch.cuda.graph(cg):
+            step()
+        per_solve_launches = lds.launch_count() - l0
+        for _ in range(args.warmup):
+            cg.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(args.steps):
+            cg.replay()
+        g1.record()
+        torch.cuda.synchronize()
+        gms = g0.elapsed_time(g1)
+        graph = {"value": units_per_step * args.steps / (gms / 1e3), "unit": unit,
+                 "ms_per_step": gms / args.steps, "kernels_per_replay": int(per_solve_launches),
+                 "speedup_vs_direct": ms / gms}
     line = {"metric": f"workload {idx} ({pr.name}) throughput"
                       + (" [debiased divergence]" if args.divergence else "")
                       + (" [symmetric schedule]" if args.schedule == "symmetric" else ""),
@@ -391,6 +423,8 @@ def run_other_workload(args):
                                       "eps": sched if len(sched) > 1 else sched[0],
                                       "iters_per_stage": pr.iters_per_stage},
             "roofline": roof, "gpu_launches": int(launches)}
+    if graph is not None:
+        line["cuda_graph"] = graph
     print(json.dumps(line), flush=True)
 
 
