@@ -28,6 +28,18 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Programmatic dependent launch (sm_90+). A kernel launched with the programmatic
+// stream-serialization attribute may start before the kernel ahead of it in the stream has
+// finished; griddep_wait() blocks the calling thread until that kernel (and so every
+// earlier one) has completed and its writes are visible. griddep_launch_dependents() lets
+// the next such kernel start early. Both are no-ops for a kernel launched normally.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // What a weighted-sum pass produces: transport application P V, the barycentric gradient,
 // the Hadamard-weighted transport (P .* X Y^T) 1, or the Hadamard-weighted transport
 // matrix application (P .* U Q^T) Q (weights P_ij <u_i, q_j> applied to the column points;

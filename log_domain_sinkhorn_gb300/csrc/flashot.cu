@@ -351,12 +351,26 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
   int rc = launch_check();
   if (rc != FLASHOT_OK) return rc;
   {
+    // Programmatic dependent of the LSE pass (the kernel waits for it at entry): the launch
+    // latency overlaps the pass's tail.
     TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
-    lse_combine_kernel<<<grid1(rows_pad, 256), 256, 0, c.st>>>(
-        partial, split, rows_pad, n_rows, rows_pad, c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
-        c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
-        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr, out_lse2,
-        average ? 1 : 0, c.at<float>(x_rows ? c.L.wa : c.L.wb), err_rows);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid1(rows_pad, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = c.st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(
+        &cfg, lse_combine_kernel, (const float2*)partial, split, (int64_t)rows_pad, n_rows,
+        (int64_t)rows_pad, (const float*)c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
+        (const float*)c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
+        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : (float*)nullptr,
+        out_lse2, average ? 1 : 0, (const float*)c.at<float>(x_rows ? c.L.wa : c.L.wb),
+        err_rows);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
   return launch_check();
 }

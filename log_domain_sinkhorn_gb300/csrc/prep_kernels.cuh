@@ -78,6 +78,10 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
                                    float* __restrict__ out_lse2, int average,
                                    const float* __restrict__ err_w = nullptr,
                                    float* __restrict__ err_rows = nullptr) {
+  // Launched as a programmatic dependent of the LSE pass: everything below reads its
+  // partials, so wait for it first; the next pass may then start its own prologue.
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= rows) {
     if (i < rows_pad && next_bias) next_bias[i] = neg_inf();

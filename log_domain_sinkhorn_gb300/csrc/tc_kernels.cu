@@ -200,6 +200,11 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
+  // Short contractions run as programmatic dependents of the previous combine: let the
+  // next kernel (this pass's combine) get ready now. The operand loads and MMAs below read
+  // only the packed clouds, which no kernel of the solve writes; the epilogue waits for
+  // the previous kernel before it reads the biases that kernel wrote.
+  if constexpr (kStageBias) griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -309,6 +314,7 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
     int bs = 0;
+    griddep_wait();  // the biases (and the partial buffer) belong to the previous kernel
     if (t_begin < t_end) stage_bias(t_begin, 0);
     for (int64_t t = t_begin; ok && t < t_end;) {
       const int64_t rt = t / NT;
@@ -764,8 +770,25 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
   if (rc != FLASHOT_OK) return rc;
   {
     TraceScope ts_(FLASHOT_KERNEL_LSE, st);
-    kern<<<(unsigned)G, kLseThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages,
-                                                kappa, partial, ld, status);
+    if constexpr (kStageBias) {
+      // Programmatic dependent of the kernel ahead of it (see the kernel's epilogue).
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)G);
+      cfg.blockDim = dim3(kLseThreads);
+      cfg.dynamicSmemBytes = (size_t)dyn;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, kappa,
+                             partial, ld, status) != cudaSuccess)
+        return FLASHOT_ERR_CUDA;
+    } else {
+      kern<<<(unsigned)G, kLseThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages,
+                                                  kappa, partial, ld, status);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
