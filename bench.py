@@ -826,13 +826,17 @@ def run_gpu(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     launches0 = lds.launch_count()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     e0.record(stream)
-    for _ in range(args.steps):
+    marks[0].record(stream)
+    for i in range(args.steps):
         step(X, Y, V, U)
+        marks[i + 1].record(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     launches = lds.launch_count() - launches0
+    per_step = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1))
     n_lse, ms_lse = timer.read(lds.KernelTimer.LSE)
@@ -903,6 +907,9 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "ms_per_step_median": float(np.median(per_step)),
+            "ms_per_step_q01_q99": [float(np.quantile(per_step, 0.01)),
+                                    float(np.quantile(per_step, 0.99))],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": prec, "data": "synthetic (seeded numpy PCG64, N(0,I/d) point clouds)",
             "config": workload_config(prec),
