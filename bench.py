@@ -99,6 +99,25 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x, world, device):
+    """The largest of x over all ranks (the timed region ends when the slowest rank does);
+    x itself with one rank. device: where the collective's buffer lives (cuda for NCCL,
+    cpu for gloo)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank, ms_max, world):
+    """Whole-job throughput of independent replicas: every rank processes units_per_rank
+    units, the job takes the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -802,14 +821,6 @@ def run_gpu(args):
             import torch.distributed as dist
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step(X, Y, V, U)
@@ -838,7 +849,7 @@ def run_gpu(args):
     launches = lds.launch_count() - launches0
     per_step = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     n_lse, ms_lse = timer.read(lds.KernelTimer.LSE)
     n_ws, ms_ws = timer.read(lds.KernelTimer.WSUM)
     n_ot, ms_ot = timer.read(lds.KernelTimer.OTHER)
@@ -847,7 +858,7 @@ def run_gpu(args):
         raise RuntimeError("a kernel reported a device timeout in the timed region")
 
     total_iters = args.steps * iters * world
-    value = total_iters / (ms / 1e3)
+    value = replica_throughput(args.steps * iters, ms, world)
     nm = float(n) * float(m)
     scores_per_step = (2 * iters + 5) * nm  # solve + grad (2 passes) + 2 applies + Hadamard
     score_evals = scores_per_step * args.steps * world / (ms / 1e3)
@@ -893,7 +904,7 @@ def run_gpu(args):
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_e2e = max_over_ranks(t0.elapsed_time(t1))
+        ms_e2e = max_over_ranks(t0.elapsed_time(t1), world, dev)
         e2e = {"value": total_iters / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps,
                "note": "pinned host -> device copy of X, Y, V, U, the step, device -> host "
