@@ -18,7 +18,7 @@
  *    and contiguous (X: n*d floats, Y: m*d floats). Vectors are contiguous.
  *  - a == NULL (b == NULL) means uniform weights 1/n (1/m). Weights are used as given:
  *    they are not renormalised; a zero weight removes its point; negative or NaN weights
- *    give undefined results (no device-side check, which would need a synchronisation).
+ *    give undefined results unless FLASHOT_VALIDATE is set (the check synchronises).
  *  - Work is enqueued asynchronously on `stream` (NULL = legacy default stream). The
  *    library allocates no device memory: all scratch comes from the caller's workspace
  *    `ws` of `ws_bytes` bytes, at least flashot_workspace_bytes(...) for the same
@@ -79,6 +79,11 @@ typedef struct CUstream_st *flashot_stream_t;
  * and a == b (the same pointers) without a warm start, f == g at every iteration, and the
  * solve runs one pass per iteration instead of two. */
 #define FLASHOT_SYMMETRIC   0x40
+/* Check the inputs before any work: every coordinate of X and Y finite, every weight of a
+ * and b (when given) finite and non-negative. One device pass over X, Y, a, b and a read of
+ * its result, which SYNCHRONISES `stream`; a violation returns FLASHOT_ERR_INVALID_ARG with
+ * nothing else enqueued. Accepted by every entry point that reads X and Y. */
+#define FLASHOT_VALIDATE    0x80
 
 /* ---- library information ------------------------------------------------------------ */
 int flashot_version(void);                       /* major*10000 + minor*100 + patch      */
@@ -154,8 +159,8 @@ int flashot_sinkhorn_solve(const float *X, const float *Y, const float *a, const
  *   error (-1 if none). err_hist: HOST array of max_iters / check_every doubles or NULL;
  *   entry k / check_every - 1 receives the error measured at check iteration k.
  *   loss: device double or NULL, <a, f> + <b, g> of the returned iterate.
- * flags: a precision and optionally FLASHOT_REUSE_PACK; anything else returns
- * FLASHOT_ERR_NOT_IMPLEMENTED. The error is formed from fp32 potentials, so it cannot
+ * flags: a precision and optionally FLASHOT_REUSE_PACK and FLASHOT_VALIDATE; anything else
+ * returns FLASHOT_ERR_NOT_IMPLEMENTED. The error is formed from fp32 potentials, so it cannot
  * resolve much below ~1e-6 * max|f| / eps (the fp32 spacing of f, relative to eps).
  * Returns FLASHOT_ERR_DEVICE_TIMEOUT (and stops) if a kernel gave up a bounded wait.
  */
@@ -246,7 +251,8 @@ int flashot_ot_grad_x(const float *X, const float *Y, const float *a, const floa
  *   V, out: n x d device floats (out must not alias V). f (n), g (m): device floats.
  *   cg_iters, cg_rel_residual: HOST pointers or NULL (iterations run; final residual ratio).
  *   flags: FLASHOT_PREC_AUTO or FLASHOT_PREC_FP32 (the passes run on fp32 CUDA cores),
- *   optionally FLASHOT_REUSE_PACK; anything else returns FLASHOT_ERR_NOT_IMPLEMENTED.
+ *   optionally FLASHOT_REUSE_PACK and FLASHOT_VALIDATE; anything else returns
+ *   FLASHOT_ERR_NOT_IMPLEMENTED.
  *   ws: at least flashot_hvp_workspace_bytes(n, m, d, flags) bytes.
  */
 size_t flashot_hvp_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags);

@@ -38,7 +38,7 @@ def version() -> int:
 
 
 def _flags(precision: str, warm: bool = False, reuse: bool = False,
-           schedule: str = "alternating") -> int:
+           schedule: str = "alternating", validate: bool = False) -> int:
     try:
         fl = PRECISIONS[precision]
     except KeyError:
@@ -47,6 +47,8 @@ def _flags(precision: str, warm: bool = False, reuse: bool = False,
         fl |= _binding.WARM_START
     if reuse:
         fl |= _binding.REUSE_PACK
+    if validate:
+        fl |= _binding.VALIDATE
     if schedule == "symmetric":
         fl |= _binding.SYMMETRIC
     elif schedule != "alternating":
@@ -126,11 +128,13 @@ def sinkhorn_solve(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] =
                    f_out: Optional[torch.Tensor] = None, g_out: Optional[torch.Tensor] = None,
                    loss_out: Optional[torch.Tensor] = None,
                    workspace: Optional[Workspace] = None, reuse_pack: bool = False,
-                   schedule: str = "alternating", f0: Optional[torch.Tensor] = None):
+                   schedule: str = "alternating", f0: Optional[torch.Tensor] = None,
+                   validate: bool = False):
     """Solve; ``eps`` is a float or an annealing schedule (one eps per stage). Returns
     (f, g, loss) with loss a 0-d float64 CUDA tensor. ``schedule`` is "alternating"
     (f = F(g), then g = G(f)) or "symmetric" (both averaged with the previous iterate).
-    ``g0`` warm-starts the alternating schedule; ``f0`` and ``g0`` the symmetric one."""
+    ``g0`` warm-starts the alternating schedule; ``f0`` and ``g0`` the symmetric one.
+    ``validate`` checks X, Y, a, b first (finite; weights non-negative), synchronising."""
     n, m, d = _sizes(X, Y)
     sched = [float(eps)] if isinstance(eps, (int, float)) else [float(e) for e in eps]
     lib = library()
@@ -146,7 +150,8 @@ def sinkhorn_solve(X: torch.Tensor, Y: torch.Tensor, a: Optional[torch.Tensor] =
     loss = loss_out if loss_out is not None else torch.empty((), dtype=torch.float64,
                                                              device=X.device)
     warm = g0 is not None and (schedule == "alternating" or f0 is not None)
-    flags = _flags(precision, warm=warm, reuse=reuse_pack, schedule=schedule)
+    flags = _flags(precision, warm=warm, reuse=reuse_pack, schedule=schedule,
+                   validate=validate)
     ws = _ws(workspace, workspace_bytes(n, m, d, 0, precision))
     arr = (ctypes.c_float * len(sched))(*sched)
     st = lib.flashot_sinkhorn_solve(

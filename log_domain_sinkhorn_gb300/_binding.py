@@ -35,6 +35,7 @@ PREC_TF32X3 = 0x4
 WARM_START = 0x10
 REUSE_PACK = 0x20
 SYMMETRIC = 0x40
+VALIDATE = 0x80
 
 KERNEL_LSE = 0
 KERNEL_WSUM = 1

@@ -270,6 +270,31 @@ int pack_inputs(const Ctx& c, const float* X, const float* Y, const float* a, co
   return launch_check();
 }
 
+// FLASHOT_VALIDATE: X and Y finite, a and b (when given) finite and non-negative. Reads
+// back one flag, so it synchronises the stream; returns FLASHOT_ERR_INVALID_ARG on a
+// violation, before anything else is enqueued for the call.
+int validate_inputs(const Ctx& c, int flags, const float* X, const float* Y, const float* a,
+                    const float* b) {
+  if (!(flags & FLASHOT_VALIDATE)) return FLASHOT_OK;
+  unsigned* flag = reinterpret_cast<unsigned*>(c.at<char>(c.L.loss) + 48);
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(unsigned), c.st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const Geometry& g = c.g;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    validate_kernel<<<(unsigned)std::min<int64_t>(c.sms * 8, grid1(g.n * g.d + g.m * g.d, 256)),
+                      256, 0, c.st>>>(X, X ? g.n * g.d : 0, Y, Y ? g.m * g.d : 0, a,
+                                      a ? g.n : 0, b, b ? g.m : 0, flag);
+  }
+  int rc = launch_check();
+  if (rc != FLASHOT_OK) return rc;
+  unsigned word = 0;
+  e = cudaMemcpyAsync(&word, flag, sizeof(word), cudaMemcpyDeviceToHost, c.st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word ? FLASHOT_ERR_INVALID_ARG : FLASHOT_OK;
+}
+
 // bias = (pot - norms) log2e / eps + lw2 over one side (pot == NULL: pot = 0).
 int launch_bias(const Ctx& c, const float* pot, bool x_side, float eps) {
   const Geometry& g = c.g;
@@ -681,6 +706,7 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
       !is_device_ptr(f) || !is_device_ptr(g) || !opt_device_ptr(loss))
     return FLASHOT_ERR_INVALID_ARG;
   const bool symmetric = (flags & FLASHOT_SYMMETRIC) != 0;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   // Small fp32 problems: every iteration in one launch of one thread-block cluster.
   if (!symmetric && c.g.prec == FLASHOT_PREC_FP32 && c.g.small &&
       small_solve_eligible(n, m, c.g.dpf, n_stages))
@@ -750,7 +776,8 @@ int flashot_sinkhorn_solve_tol(const float* X, const float* Y, const float* a, c
   if (!eps_ok(eps) || !std::isfinite(tol) || tol < 0.0 || max_iters < 1 || check_every < 1 ||
       iters_done == nullptr)
     return FLASHOT_ERR_INVALID_ARG;
-  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK | FLASHOT_VALIDATE))
+    return FLASHOT_ERR_NOT_IMPLEMENTED;
   Ctx c;
   int rc = begin(n, m, d, 0, flags, ws, ws_bytes, stream, &c);
   if (rc != FLASHOT_OK) return rc;
@@ -759,6 +786,7 @@ int flashot_sinkhorn_solve_tol(const float* X, const float* Y, const float* a, c
     return FLASHOT_ERR_INVALID_ARG;
   *iters_done = 0;
   if (err) *err = -1.0;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, nullptr, false, eps)) != FLASHOT_OK) return rc;
   float* err_rows = c.at<float>(c.L.lse2);
@@ -821,12 +849,13 @@ int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float
                      flashot_stream_t stream) {
   if (!eps_ok(eps) || !std::isfinite(cg_tol) || cg_tol < 0.0 || cg_max_iters < 0)
     return FLASHOT_ERR_INVALID_ARG;
-  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  if (flags & ~(FLASHOT_PREC_MASK | FLASHOT_REUSE_PACK | FLASHOT_VALIDATE))
+    return FLASHOT_ERR_NOT_IMPLEMENTED;
   {
     const int p = flags & FLASHOT_PREC_MASK;
     if (p != FLASHOT_PREC_AUTO && p != FLASHOT_PREC_FP32) return FLASHOT_ERR_NOT_IMPLEMENTED;
   }
-  const int fl = (flags & FLASHOT_REUSE_PACK) | FLASHOT_PREC_FP32;
+  const int fl = (flags & (FLASHOT_REUSE_PACK | FLASHOT_VALIDATE)) | FLASHOT_PREC_FP32;
   Ctx c;
   int rc = begin(n, m, d, d + 2, fl, ws, ws_bytes, stream, &c);
   if (rc != FLASHOT_OK) return rc;
@@ -838,6 +867,7 @@ int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float
     return FLASHOT_ERR_INVALID_ARG;
   if (cg_iters) *cg_iters = 0;
   if (cg_rel_residual) *cg_rel_residual = 0.0;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
@@ -1012,6 +1042,7 @@ int flashot_sinkhorn_step_f(const float* X, const float* Y, const float* b, cons
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(b) || !is_device_ptr(g) ||
       !is_device_ptr(f))
     return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, nullptr, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, nullptr, b)) != FLASHOT_OK)
     return rc;
   if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
@@ -1028,6 +1059,7 @@ int flashot_sinkhorn_step_g(const float* X, const float* Y, const float* a, cons
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !is_device_ptr(f) ||
       !is_device_ptr(g))
     return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, a, nullptr)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, nullptr)) != FLASHOT_OK)
     return rc;
   if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
@@ -1073,6 +1105,7 @@ int flashot_transport_apply(const float* X, const float* Y, const float* a, cons
       !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(V) || !is_device_ptr(out) ||
       (const void*)out == (const void*)V)
     return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
@@ -1090,6 +1123,7 @@ int flashot_transport_hadamard_xy(const float* X, const float* Y, const float* a
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
       !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(h))
     return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
@@ -1106,6 +1140,7 @@ int flashot_ot_grad_x(const float* X, const float* Y, const float* a, const floa
   if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
       !is_device_ptr(g) || !is_device_ptr(grad))
     return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
   if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
   if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
   // f~ = F(g); its combine writes biasG = log2 a_i - L_i, so the weighted pass below uses

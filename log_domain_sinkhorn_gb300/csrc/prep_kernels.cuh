@@ -115,6 +115,26 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
   if (out_lse2) out_lse2[i] = L;
 }
 
+// Input check (FLASHOT_VALIDATE): bit 1 of *flag if a coordinate of X or Y is not finite,
+// bit 2 if a weight is negative or not finite.
+__global__ void validate_kernel(const float* __restrict__ X, int64_t nx,
+                                const float* __restrict__ Y, int64_t ny,
+                                const float* __restrict__ a, int64_t na,
+                                const float* __restrict__ b, int64_t nb,
+                                unsigned* __restrict__ flag) {
+  unsigned bad = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nx + ny; i += stride) {
+    const float v = i < nx ? X[i] : Y[i - nx];
+    if (!isfinite(v)) bad |= 1u;
+  }
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < na + nb; i += stride) {
+    const float w = i < na ? a[i] : b[i - na];
+    if (!(w >= 0.0f) || !isfinite(w)) bad |= 2u;
+  }
+  if (bad) atomicOr(flag, bad);
+}
+
 // loss = sum_i wa_i f_i + sum_j wb_j g_j in fp64; one block, deterministic order.
 __global__ void __launch_bounds__(1024)
 dual_loss_kernel(const float* __restrict__ wa, const float* __restrict__ f, int64_t n,

@@ -89,3 +89,32 @@ def test_apply_rejects_aliasing_and_bad_k(setup):
     assert lib.flashot_transport_apply(*common, V.data_ptr(), 4, 0, out.data_ptr(), 1, wsb.ptr,
                                        wsb.nbytes, s) == B.OK
     torch.cuda.synchronize()
+
+
+def test_validate_flag_rejects_bad_inputs(setup):
+    """FLASHOT_VALIDATE: a negative or NaN weight, or a non-finite coordinate, is rejected
+    with ERR_INVALID_ARG before anything runs; valid inputs pass, on the streaming and the
+    single-launch cluster paths alike."""
+    lds, B, X, Y, f, g, ws, n, m, d, nb = setup
+    rng = np.random.default_rng(3)
+    a = to_dev((rng.exponential(size=n) / n).astype(np.float32))
+    b = to_dev((rng.exponential(size=m) / m).astype(np.float32))
+    for prec in ("fp32", "tf32"):  # n * m small: fp32 takes the cluster path
+        f_, g_, _ = lds.sinkhorn_solve(X, Y, a, b, 0.5, 5, precision=prec, validate=True)
+        assert np.isfinite(f_.cpu().numpy()).all()
+        for bad in ("neg", "nan", "xinf"):
+            a2, X2 = a.clone(), X.clone()
+            if bad == "neg":
+                a2[7] = -1e-3
+            elif bad == "nan":
+                a2[3] = float("nan")
+            else:
+                X2[5, 1] = float("inf")
+            with pytest.raises(lds.FlashotError) as ei:
+                lds.sinkhorn_solve(X2, Y, a2, b, 0.5, 5, precision=prec, validate=True)
+            assert ei.value.status == B.ERR_INVALID_ARG
+    # without the flag the call is not checked (and returns OK)
+    a3 = a.clone()
+    a3[0] = -1.0
+    lds.sinkhorn_solve(X, Y, a3, b, 0.5, 2, precision="fp32")
+    torch.cuda.synchronize()
