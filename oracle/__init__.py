@@ -23,6 +23,9 @@ Parity status of each function (what pins it, in tests/test_oracle_pins.py):
                              the gradient identity grad_i = 2(a_i x_i - (P~ Y)_i).
   hadamard_xy                h_i = <x_i, (P Y)_i> and d/dt OT(X, tY) finite difference.
   marginals                  row sums = a after F and column sums = b after G.
+  diagnostics                strong duality at convergence (primal = dual); the primal and
+                             dual objectives and the transport cost restated densely in
+                             numpy; marginal errors equal those of marginals().
   solve_symmetric            X = Y gives f == g at every iteration; same converged loss
                              as the alternating schedule.
   sinkhorn_divergence        S(a, a) = 0; S >= 0; eps -> inf limit |mean x - mean y|^2.
@@ -114,6 +117,9 @@ def _lib():
             lib.oracle_marginals.restype = None
             lib.oracle_sinkhorn_knopp.argtypes = [_dp, _i64, ctypes.c_int, ctypes.c_int, _dp]
             lib.oracle_sinkhorn_knopp.restype = None
+            lib.oracle_diagnostics.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _i64, _i64, _i64,
+                                               ctypes.c_double, _dp]
+            lib.oracle_diagnostics.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _LIB = lib
@@ -340,3 +346,16 @@ def sinkhorn_knopp(H, n_iter):
     P = np.empty_like(H)
     _lib().oracle_sinkhorn_knopp(_p(H), B, n, int(n_iter), _p(P))
     return P
+
+
+def diagnostics(X, Y, a, b, f, g, eps):
+    """Plan diagnostics at (f, g): dict with primal, dual, transport_cost, row_err, col_err
+    and mass (see oracle_diagnostics)."""
+    X, Y, a, b, f, g = map(_f64, (X, Y, a, b, f, g))
+    n, d = X.shape
+    m = Y.shape[0]
+    out = np.empty(6, dtype=np.float64)
+    _lib().oracle_diagnostics(_p(X), _p(Y), _p(a), _p(b), _p(f), _p(g), n, m, d, float(eps),
+                              _p(out))
+    keys = ("primal", "dual", "transport_cost", "row_err", "col_err", "mass")
+    return dict(zip(keys, out.tolist()))

@@ -363,3 +363,50 @@ void oracle_sinkhorn_knopp(const double *H, int64_t B, int n, int n_iter, double
         free(v);
     }
 }
+
+/*
+ * Diagnostics of the plan defined by (f, g) ([REV] "Summary": the dual potentials define
+ * the plan; the primal objective of the KL-regularised problem), all from the plain
+ * definitions with the dense cost:
+ *   out[0] primal   <C, P> + eps KL(P | a b^T),  KL = sum P log(P / (a b)) - sum P + sum a b
+ *   out[1] dual     <a, f> + <b, g> - eps (sum P - sum a sum b)
+ *   out[2] <C, P>   (transport cost)
+ *   out[3] sum_i |sum_j P_ij - a_i|   (row-marginal L1 error)
+ *   out[4] sum_j |sum_i P_ij - b_j|   (column-marginal L1 error)
+ *   out[5] sum P    (mass)
+ * Zero weights contribute nothing (their plan entries are 0).
+ */
+void oracle_diagnostics(const double *X, const double *Y, const double *a, const double *b,
+                        const double *f, const double *g, int64_t n, int64_t m, int64_t d,
+                        double eps, double *out)
+{
+    double cost = 0.0, kl = 0.0, mass = 0.0, row_err = 0.0, col_err = 0.0;
+    double suma = 0.0, sumb = 0.0, dual = 0.0;
+    double *col = (double *)calloc((size_t)(m > 0 ? m : 1), sizeof(double));
+    for (int64_t i = 0; i < n; ++i) {
+        double r = 0.0;
+        for (int64_t j = 0; j < m; ++j) {
+            const double c = sq_cost(X + i * d, Y + j * d, d);
+            const double p = plan_entry(X + i * d, Y + j * d, d, a[i], b[j], f[i], g[j], eps);
+            if (p > 0.0) {
+                cost += p * c;
+                kl += p * log(p / (a[i] * b[j]));
+            }
+            r += p;
+            col[j] += p;
+        }
+        mass += r;
+        row_err += fabs(r - a[i]);
+    }
+    for (int64_t j = 0; j < m; ++j) col_err += fabs(col[j] - b[j]);
+    for (int64_t i = 0; i < n; ++i) { suma += a[i]; dual += a[i] * f[i]; }
+    for (int64_t j = 0; j < m; ++j) { sumb += b[j]; dual += b[j] * g[j]; }
+    kl += -mass + suma * sumb;
+    out[0] = cost + eps * kl;
+    out[1] = dual - eps * (mass - suma * sumb);
+    out[2] = cost;
+    out[3] = row_err;
+    out[4] = col_err;
+    out[5] = mass;
+    free(col);
+}

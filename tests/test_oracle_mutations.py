@@ -37,6 +37,7 @@ MUTATIONS = {
     "sk_row_uses_transpose": ("s += M[i * n + j] * v[j];", "s += M[j * n + i] * v[j];"),
     "sk_missing_exp": ("M[k] = exp(h[k]);", "M[k] = h[k] * h[k] + 1.0;"),
     "sk_output_drops_u": ("p[i * n + j] = u[i] * M[i * n + j] * v[j];", "p[i * n + j] = M[i * n + j] * v[j];"),
+    "diag_kl_drops_mass_terms": ("kl += -mass + suma * sumb;", "kl += 0.0;"),
     "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
 }
 

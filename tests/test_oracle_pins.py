@@ -635,3 +635,28 @@ def test_sinkhorn_knopp_rank_one_and_invariances():
     pr, pc = rng.permutation(4), rng.permutation(4)
     Pp = oracle.sinkhorn_knopp(H[:, pr][:, :, pc], 20)
     np.testing.assert_allclose(Pp, P[:, pr][:, :, pc], rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------------
+# Plan diagnostics
+# ---------------------------------------------------------------------------------
+
+def test_diagnostics_match_dense_definitions_and_strong_duality():
+    """Primal and dual objectives restated densely here (primal_objective, dual_objective),
+    marginal errors from marginals(), and primal = dual at convergence."""
+    X, Y, a, b, f, g = _random_instance(seed=95, n=17, m=13, d=3)
+    eps = 0.4
+    dg = oracle.diagnostics(X, Y, a, b, f, g, eps)
+    assert dg["primal"] == pytest.approx(primal_objective(X, Y, a, b, f, g, eps), rel=1e-11)
+    assert dg["dual"] == pytest.approx(dual_objective(X, Y, a, b, f, g, eps), rel=1e-11)
+    P = plan(X, Y, a, b, f, g, eps)
+    assert dg["transport_cost"] == pytest.approx(float((P * dense_cost(X, Y)).sum()), rel=1e-11)
+    assert dg["mass"] == pytest.approx(float(P.sum()), rel=1e-12)
+    r, c = oracle.marginals(X, Y, a, b, f, g, eps)
+    assert dg["row_err"] == pytest.approx(float(np.abs(r - a).sum()), rel=1e-11)
+    assert dg["col_err"] == pytest.approx(float(np.abs(c - b).sum()), rel=1e-11)
+    a1, b1 = a / a.sum(), b / b.sum()
+    fc, gc = _converged(X, Y, a1, b1, eps)
+    dc = oracle.diagnostics(X, Y, a1, b1, fc, gc, eps)
+    assert dc["primal"] == pytest.approx(dc["dual"], rel=1e-10)
+    assert dc["row_err"] < 1e-12 and dc["col_err"] < 1e-12
