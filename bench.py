@@ -60,6 +60,10 @@ def parse_args():
                    help="supplementary lines: iteration schedule of the solves")
     p.add_argument("--divergence", action="store_true",
                    help="supplementary line: debiased Sinkhorn divergence (three solves)")
+    p.add_argument("--diagnostics", action="store_true",
+                   help="supplementary line: plan diagnostics (primal/dual objectives, "
+                        "transport cost, marginal errors) of --workload at its solved "
+                        "potentials; three streaming passes per step")
     p.add_argument("--tol", type=float, default=None,
                    help="supplementary line: convergence-driven solve of --workload to this "
                         "L1 marginal error (with --eps, --max-iters, --check-every)")
@@ -322,7 +326,22 @@ def run_other_workload(args):
     g = torch.empty(m, device=dev)
     loss = torch.empty((), dtype=torch.float64, device=dev)
     nm = float(n) * float(m)
-    if idx == 5:
+    if args.diagnostics:
+        lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
+                           g_out=g, loss_out=loss, workspace=ws)
+        res = torch.empty(6, dtype=torch.float64, device=dev)
+        dws = lds.Workspace(int(lds.library().flashot_diagnostics_workspace_bytes(
+            n, m, d, lds._flags(prec))))
+        eps = sched[-1]
+
+        def step():
+            lds.plan_diagnostics(X, Y, f, g, eps, a, b, precision=prec, out=res, workspace=dws,
+                                 as_dict=False)
+        # r = P 1, c = P^T 1 and the Hadamard sums: three streaming passes over the n x m
+        # scores (plus O(n + m) packing and the fp64 reduction)
+        units_per_step, unit, scores_per_step = 1, "plan diagnostics/s", 3 * nm
+        hot = lds.KernelTimer.WSUM
+    elif idx == 5:
         lds.sinkhorn_solve(X, Y, a, b, sched, pr.iters_per_stage, precision=prec, f_out=f,
                            g_out=g, loss_out=loss, workspace=ws)
         V = torch.from_numpy(pr.V).to(dev)
@@ -409,7 +428,7 @@ def run_other_workload(args):
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
     graph = None
-    if args.graph and idx != 5 and not args.divergence:
+    if args.graph and idx != 5 and not args.divergence and not args.diagnostics:
         # The same solve captured once into a CUDA graph (torch's capture stream is the
         # current stream the binding passes) and replayed: no per-launch host work.
         cg = torch.cuda.CUDAGraph()
@@ -439,6 +458,7 @@ def run_other_workload(args):
                  "speedup_vs_direct": ms / gms}
     line = {"metric": f"workload {idx} ({pr.name}) throughput"
                       + (" [debiased divergence]" if args.divergence else "")
+                      + (" [plan diagnostics]" if args.diagnostics else "")
                       + (" [symmetric schedule]" if args.schedule == "symmetric" else ""),
             "supplementary": True,
             "value": units_per_step * args.steps / (ms / 1e3), "unit": unit,
@@ -450,6 +470,11 @@ def run_other_workload(args):
             "roofline": roof, "gpu_launches": int(launches)}
     if graph is not None:
         line["cuda_graph"] = graph
+    if args.diagnostics:
+        if lds.workspace_status(dws) != 0:
+            raise RuntimeError("device timeout reported")
+        line["diagnostics"] = dict(zip(("primal", "dual", "transport_cost", "row_err",
+                                        "col_err", "mass"), res.cpu().tolist()))
     print(json.dumps(line), flush=True)
 
 
@@ -1000,7 +1025,8 @@ def main():
         run_sk(args)
     elif args.tol is not None:
         run_convergence(args)
-    elif args.workload != WORKLOAD_IDX or args.divergence or args.schedule != "alternating":
+    elif (args.workload != WORKLOAD_IDX or args.divergence or args.diagnostics
+          or args.schedule != "alternating"):
         run_other_workload(args)
     else:
         if args.precision is None:

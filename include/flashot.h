@@ -281,6 +281,27 @@ int flashot_ot_hvp_x(const float *X, const float *Y, const float *a, const float
 int flashot_sinkhorn_knopp_batched(const float *H, int64_t B, int n, int n_iter, float *P,
                                    flashot_stream_t stream);
 
+/*
+ * Diagnostics of the plan defined by (f, g) (the review's "Summary": the dual potentials
+ * define the plan P_ij = a_i b_j exp((f_i + g_j - C_ij)/eps)), from three streaming passes
+ * (P 1, P^T 1 and the Hadamard sums h_i = sum_j P_ij <x_i, y_j>) and one fp64 reduction:
+ *   out[0] primal objective <C, P> + eps KL(P | a b^T)  (KL with the -sum P + sum a b terms)
+ *   out[1] dual objective   <a, f> + <b, g> - eps (sum P - sum a sum b)
+ *   out[2] transport cost   <C, P> = sum_i r_i |x_i|^2 + sum_j c_j |y_j|^2 - 2 sum_i h_i
+ *   out[3] row-marginal L1 error    sum_i |r_i - a_i|,  r = P 1
+ *   out[4] column-marginal L1 error sum_j |c_j - b_j|,  c = P^T 1
+ *   out[5] mass sum P
+ * At optimal potentials primal = dual and both errors vanish. out: SIX device doubles.
+ * The passes run in the precision of flags (the fp32 path gives fp32-accurate sums; the
+ * transport cost is a difference of larger terms). ws: at least
+ * flashot_diagnostics_workspace_bytes(n, m, d, flags) bytes.
+ */
+size_t flashot_diagnostics_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags);
+int flashot_plan_diagnostics(const float *X, const float *Y, const float *a, const float *b,
+                             const float *f, const float *g, int64_t n, int64_t m, int64_t d,
+                             float eps, int flags, double *out, void *ws, size_t ws_bytes,
+                             flashot_stream_t stream);
+
 /* ---- allocation-free variant -------------------------------------------------------- */
 /*
  * The paper has no counterpart to this entry point; it exists for callers that cannot give

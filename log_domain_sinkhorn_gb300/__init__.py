@@ -25,6 +25,7 @@ __all__ = [
     "dual_loss", "transport_apply", "transport_hadamard_xy", "ot_grad_x", "workspace_status",
     "FlashotError", "library", "version", "launch_count", "KernelTimer",
     "sinkhorn_divergence", "sinkhorn_solve_tol", "ot_hvp_x", "sinkhorn_knopp_batched",
+    "plan_diagnostics",
 ]
 
 
@@ -338,6 +339,31 @@ def sinkhorn_knopp_batched(H: torch.Tensor, n_iter: int = 20, *, out=None):
         _stream())
     _binding.check(st, "flashot_sinkhorn_knopp_batched")
     return P
+
+
+def plan_diagnostics(X, Y, f, g, eps: float, a=None, b=None, *, precision="auto",
+                     out=None, workspace=None, reuse_pack=False, as_dict=True):
+    """Primal and dual objectives, transport cost, marginal L1 errors and mass of the plan
+    defined by (f, g), as a dict of floats (the six device doubles are in ``out``); with
+    ``as_dict=False`` the device tensor is returned and nothing is read back."""
+    n, m, d = _sizes(X, Y)
+    lib = library()
+    nb = int(lib.flashot_diagnostics_workspace_bytes(n, m, d, _flags(precision)))
+    if nb == 0:
+        raise ValueError(f"invalid sizes n={n} m={m} d={d}")
+    ws = _ws(workspace, nb)
+    res = out if out is not None else torch.empty(6, dtype=torch.float64, device=X.device)
+    st = lib.flashot_plan_diagnostics(
+        _dev_ptr(X, "X", (n, d)), _dev_ptr(Y, "Y", (m, d)),
+        _dev_ptr(a, "a", (n,), optional=True), _dev_ptr(b, "b", (m,), optional=True),
+        _dev_ptr(f, "f", (n,)), _dev_ptr(g, "g", (m,)), n, m, d, float(eps),
+        _flags(precision, reuse=reuse_pack), _dev_ptr(res, "out", (6,), dtype=torch.float64),
+        ws.ptr, ws.nbytes, _stream())
+    _binding.check(st, "flashot_plan_diagnostics")
+    if not as_dict:
+        return res
+    v = res.cpu().tolist()
+    return dict(zip(("primal", "dual", "transport_cost", "row_err", "col_err", "mass"), v))
 
 
 def workspace_status(workspace: Workspace) -> int:

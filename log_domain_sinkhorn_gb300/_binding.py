@@ -91,6 +91,11 @@ SIGNATURES = {
         ctypes.POINTER(ctypes.c_double), _vp, ctypes.c_size_t, _vp]),
     "flashot_sinkhorn_knopp_batched": (ctypes.c_int, [_vp, _c_i64, ctypes.c_int, ctypes.c_int,
                                                       _vp, _vp]),
+    "flashot_diagnostics_workspace_bytes": (ctypes.c_size_t, [_c_i64, _c_i64, _c_i64,
+                                                              ctypes.c_int]),
+    "flashot_plan_diagnostics": (ctypes.c_int, [
+        _vp, _vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int,
+        _vp, _vp, ctypes.c_size_t, _vp]),
     "flashot_sinkhorn_step_f_noalloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int, _vp, _vp]),
     "flashot_ot_grad_x": (ctypes.c_int, [

@@ -979,6 +979,58 @@ int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float
   return launch_check();
 }
 
+size_t flashot_diagnostics_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags) {
+  Geometry g;
+  if (!make_geometry(n, m, d, 1, flags, &g)) return 0;
+  // r (n), c (m), h (n) and a vector of ones (max(n, m)), each 256-byte aligned
+  const size_t mx = (size_t)std::max(g.n_pad, g.m_pad);
+  return make_layout(g).total + 4 * (mx * 4 + 256);
+}
+
+int flashot_plan_diagnostics(const float* X, const float* Y, const float* a, const float* b,
+                             const float* f, const float* g, int64_t n, int64_t m, int64_t d,
+                             float eps, int flags, double* out, void* ws, size_t ws_bytes,
+                             flashot_stream_t stream) {
+  if (!eps_ok(eps)) return FLASHOT_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = begin(n, m, d, 1, flags, ws, ws_bytes, stream, &c);
+  if (rc != FLASHOT_OK) return rc;
+  if (ws_bytes < flashot_diagnostics_workspace_bytes(n, m, d, flags))
+    return FLASHOT_ERR_WORKSPACE_TOO_SMALL;
+  if (!is_device_ptr(X) || !is_device_ptr(Y) || !opt_device_ptr(a) || !opt_device_ptr(b) ||
+      !is_device_ptr(f) || !is_device_ptr(g) || !is_device_ptr(out))
+    return FLASHOT_ERR_INVALID_ARG;
+  if ((rc = validate_inputs(c, flags, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if (!(flags & FLASHOT_REUSE_PACK) && (rc = pack_inputs(c, X, Y, a, b)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, g, false, eps)) != FLASHOT_OK) return rc;
+  if ((rc = launch_bias(c, f, true, eps)) != FLASHOT_OK) return rc;
+  const size_t mx = (size_t)std::max(c.g.n_pad, c.g.m_pad);
+  const size_t slot = (mx * 4 + 255) / 256 * 256;
+  float* r_ = reinterpret_cast<float*>(c.ws + c.L.total);
+  float* c_ = reinterpret_cast<float*>(c.ws + c.L.total + slot);
+  float* h_ = reinterpret_cast<float*>(c.ws + c.L.total + 2 * slot);
+  float* ones = reinterpret_cast<float*>(c.ws + c.L.total + 3 * slot);
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    fill_kernel<<<grid1((int64_t)mx, 256), 256, 0, c.st>>>(ones, (int64_t)mx, 1.0f);
+  }
+  if ((rc = launch_check()) != FLASHOT_OK) return rc;
+  if ((rc = run_wsum_pass(c, kWsumApply, false, eps, ones, 1, 1, X, Y, r_, 1)) != FLASHOT_OK)
+    return rc;
+  if ((rc = run_wsum_pass(c, kWsumApply, true, eps, ones, 1, 1, X, Y, c_, 1)) != FLASHOT_OK)
+    return rc;
+  if ((rc = run_wsum_pass(c, kWsumHadamard, false, eps, nullptr, 0, 1, X, Y, h_, 1)) !=
+      FLASHOT_OK)
+    return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+    diagnostics_kernel<<<1, 1024, 0, c.st>>>(r_, c_, h_, c.at<float>(c.L.alpha),
+                                             c.at<float>(c.L.beta), c.at<float>(c.L.wa),
+                                             c.at<float>(c.L.wb), f, g, n, m, (double)eps, out);
+  }
+  return launch_check();
+}
+
 size_t flashot_divergence_workspace_bytes(int64_t n, int64_t m, int64_t d, int flags) {
   const size_t w1 = flashot_workspace_bytes(n, m, d, 0, flags);
   const size_t w2 = flashot_workspace_bytes(n, n, d, 0, flags);

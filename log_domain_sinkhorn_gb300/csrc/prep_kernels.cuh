@@ -135,6 +135,71 @@ __global__ void validate_kernel(const float* __restrict__ X, int64_t nx,
   if (bad) atomicOr(flag, bad);
 }
 
+// Plan diagnostics from the marginals r = P 1, c = P^T 1 and the Hadamard sums
+// h_i = sum_j P_ij <x_i, y_j> (one block, fp64, fixed order). With <C, P> = sum r alpha +
+// sum c beta - 2 sum h and sum P log(P / (a b)) = (sum r f + sum c g - <C, P>) / eps:
+//   out = {primal = sum r f + sum c g - eps (sum P - sum a sum b),
+//          dual = sum a f + sum b g - eps (sum P - sum a sum b),
+//          <C, P>, sum |r - a|, sum |c - b|, sum P}.
+__global__ void __launch_bounds__(1024)
+diagnostics_kernel(const float* __restrict__ r, const float* __restrict__ c,
+                   const float* __restrict__ h, const float* __restrict__ alpha,
+                   const float* __restrict__ beta, const float* __restrict__ wa,
+                   const float* __restrict__ wb, const float* __restrict__ f,
+                   const float* __restrict__ g, int64_t n, int64_t m, double eps,
+                   double* __restrict__ out) {
+  __shared__ double red[8][33];
+  double v[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // rf+cg, af+bg, cost, row_err, col_err, mass, suma, sumb
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const double ri = r[i], ai = wa[i];
+    v[0] += ri == 0.0 ? 0.0 : ri * (double)f[i];
+    v[1] += ai == 0.0 ? 0.0 : ai * (double)f[i];
+    v[2] += ri * (double)alpha[i] - 2.0 * (double)h[i];
+    v[3] += fabs(ri - ai);
+    v[5] += ri;
+    v[6] += ai;
+  }
+  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+    const double cj = c[j], bj = wb[j];
+    v[0] += cj == 0.0 ? 0.0 : cj * (double)g[j];
+    v[1] += bj == 0.0 ? 0.0 : bj * (double)g[j];
+    v[2] += cj * (double)beta[j];
+    v[4] += fabs(cj - bj);
+    v[7] += bj;
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
+    if ((threadIdx.x & 31) == 0) red[k][threadIdx.x >> 5] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    double t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      t[k] = (threadIdx.x < (blockDim.x >> 5)) ? red[k][threadIdx.x] : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t[k] += __shfl_xor_sync(0xffffffffu, t[k], o);
+    }
+    if (threadIdx.x == 0) {
+      const double excess = t[5] - t[6] * t[7];
+      out[0] = t[0] - eps * excess;
+      out[1] = t[1] - eps * excess;
+      out[2] = t[2];
+      out[3] = t[3];
+      out[4] = t[4];
+      out[5] = t[5];
+    }
+  }
+}
+
+__global__ void fill_kernel(float* __restrict__ p, int64_t count, float v) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
 // loss = sum_i wa_i f_i + sum_j wb_j g_j in fp64; one block, deterministic order.
 __global__ void __launch_bounds__(1024)
 dual_loss_kernel(const float* __restrict__ wa, const float* __restrict__ f, int64_t n,
