@@ -5,9 +5,11 @@
 // For every (row tile i, column tile j) of 128 x 256:
 //   S   = rows * cols^T                               tcgen05.mma M=128 N=256 -> TMEM[0:256)
 //   w_ij = exp2(kappa S_ij + colBias_j + rowBias_i)   8 epilogue warps, fp32 + SFU ex2
-//   O  += W * V^T-tile                                tcgen05.mma M=128 N=kKV -> TMEM[256:)
-// W is written by the epilogue into shared memory in the 128-byte-swizzled K-major layout
-// the MMA reads; V^T is loaded by TMA. The S MMA of tile j+1 overlaps the epilogue of tile j.
+//   O  += W * V^T-tile                                tcgen05.mma M=128 N=kKV -> TMEM[384:)
+// W is written by the epilogue as bf16 into tensor memory (TMEM[256:384), two weights per
+// 32-bit column) and is the A operand of the second MMA, read from there; V^T is loaded by
+// TMA. Keeping W out of shared memory leaves room for four operand stages instead of two.
+// The S MMA of tile j+1 overlaps the epilogue of tile j.
 // The weights are plan entries (or a_i times softmax weights), all <= 1, so no running max.
 //
 // Work split: the (output-column group, row tile, column tile) triples are cut into
@@ -69,16 +71,15 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
   constexpr bool kHad = (kKV == 0);
   constexpr uint32_t kBChunk = 2u * kChunk;            // 256 rows x 128 B
   constexpr uint32_t kStage = kChunk + kBChunk;        // A chunk + B chunk
-  constexpr uint32_t kWBytes = kHad ? 0u : 4u * kChunk;  // 128 x 256 bf16, 4 K-chunks of 64
   constexpr uint32_t kVChunk = (uint32_t)(kHad ? 1 : kKV) * 128u;  // kKV rows x 128 B
   constexpr uint32_t kVBytes = kHad ? 0u : 4u * kVChunk;
-  constexpr uint32_t kTmemCols = 512;                  // S at [0, 256), O at [256, 256 + kKV)
+  constexpr uint32_t kTmemCols = 512;  // S at [0, 256), W at [256, 384), O at [384, 384 + kKV)
+  constexpr uint32_t kTmemW = 256, kTmemO = 384;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = ptx::smem_u32(dyn_smem);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = dyn_smem + (base - raw);
-  const uint32_t w_base = (uint32_t)n_st * kStage;
-  const uint32_t v_base = w_base + kWBytes;
+  const uint32_t v_base = (uint32_t)n_st * kStage;
   const int64_t G = gridDim.x, cta = blockIdx.x;
   const int64_t t_begin = sk_begin(cta, T, G), t_end = sk_begin(cta + 1, T, G);
 
@@ -188,15 +189,16 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
               if (!ptx::mbar_wait(&ctl.w_full, par(w_uses))) { ok = false; break; }
               if (!ptx::mbar_wait(&ctl.v_full, par(w_uses))) { ok = false; break; }
               ptx::tc_fence_after();
-              const uint64_t w_desc = ptx::sdesc_k128(base + w_base);
               const uint64_t v_desc = ptx::sdesc_k128(base + v_base);
+              // K = 256 in steps of 16: W columns advance by 8 (two bf16 per column), the V
+              // descriptor by 32 bytes inside each 64-element swizzled chunk.
 #pragma unroll
               for (int vc = 0; vc < 4; ++vc) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  ptx::umma<true>(tmem + 256, w_desc + (uint64_t)(vc * (kChunk >> 4) + 2 * kk),
-                                  v_desc + (uint64_t)(vc * (kVChunk >> 4) + 2 * kk), idesc_o,
-                                  (u > 1 || vc > 0 || kk > 0) ? 1u : 0u);
+                  ptx::umma_ts_bf16(tmem + kTmemO, tmem + kTmemW + (uint32_t)(vc * 4 + kk) * 8u,
+                                    v_desc + (uint64_t)(vc * (kVChunk >> 4) + 2 * kk), idesc_o,
+                                    (u > 1 || vc > 0 || kk > 0) ? 1u : 0u);
               }
               ptx::umma_commit(&ctl.w_empty);
               ptx::umma_commit(&ctl.v_empty);
@@ -265,25 +267,18 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
           v[j + 3] = w3;
         }
         if constexpr (!kHad) {
-          if (!ptx::mbar_wait(&ctl.w_empty, par(w_uses) ^ 1u)) { ok = false; break; }
-          // This warp's 128 weights are K-chunks 2h and 2h+1 (64 bf16 each) of the W row.
-          const uint32_t wrow = base + w_base + (uint32_t)rloc * 128u;
+          // This warp's 128 weights are W row rloc, K = 128h .. 128h + 127: 64 columns of
+          // bf16 pairs at TMEM column 256 + 64h.
+          uint32_t wp[64];
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-#pragma unroll
-            for (int u8 = 0; u8 < 8; ++u8) {
-              const int j = c * 64 + u8 * 8;
-              __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j + 0], v[j + 1]);
-              __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
-              __nv_bfloat162 h3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
-              ptx::st_shared_v4(wrow + (uint32_t)(2 * h + c) * kChunk +
-                                    (uint32_t)((u8 ^ (rloc & 7)) << 4),
-                                *reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1),
-                                *reinterpret_cast<uint32_t*>(&h2), *reinterpret_cast<uint32_t*>(&h3));
-            }
+          for (int c = 0; c < 64; ++c) {
+            __nv_bfloat162 hp = __floats2bfloat162_rn(v[2 * c], v[2 * c + 1]);
+            wp[c] = *reinterpret_cast<uint32_t*>(&hp);
           }
-          ptx::fence_proxy_async_smem();
+          if (!ptx::mbar_wait(&ctl.w_empty, par(w_uses) ^ 1u)) { ok = false; break; }
+          ptx::tc_fence_after();
+          ptx::tmem_st_x64_sync(tmem + lane_base + kTmemW + (uint32_t)h * 64u, wp);
+          ptx::tc_fence_before();
           ptx::mbar_arrive(&ctl.w_full);
           ++w_uses;
         }
@@ -298,7 +293,7 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
 #pragma unroll 1
         for (int c = 0; c < kKV / 64; ++c) {
           float o[32];
-          ptx::tmem_ld_x32_sync(tmem + lane_base + 256 + h * (kKV / 2) + c * 32, o);
+          ptx::tmem_ld_x32_sync(tmem + lane_base + kTmemO + h * (kKV / 2) + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + c * 32 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
@@ -367,7 +362,7 @@ static int launch(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMa
                   const float* colBias, const float* rowBias, int64_t n_rows, int64_t row_tiles,
                   int64_t NT, int64_t T, int64_t G, int kc, float kappa, float* pO, float2* pW,
                   int64_t ldp, unsigned* status, cudaStream_t st) {
-  const int fixed = (kKV == 0) ? 0 : 4 * kChunk + 4 * kKV * 128;
+  const int fixed = (kKV == 0) ? 0 : 4 * kKV * 128;  // the V^T tile
   const int budget = kSmemLimit - (int)sizeof(W2Ctrl) - 1024 - fixed;
   const int n_st = std::min(kMaxStages, budget / (3 * kChunk));
   if (n_st < 2) return FLASHOT_ERR_INVALID_ARG;
