@@ -54,7 +54,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-passes", type=int, default=0, metavar="P",
                    help="profiling driver: pack once, run P f-updates and P g-updates of the "
-                        "workload (no timing, no JSON line) and exit; for ncu captures")
+                        "workload (no timing, no JSON line) and exit; for ncu captures. With "
+                        "--diagnostics, then P plan diagnostics and P transport applications "
+                        "(k = 128) at those potentials")
     p.add_argument("--n", type=int, default=None, help="override n = m (profiling driver)")
     p.add_argument("--schedule", choices=["alternating", "symmetric"], default="alternating",
                    help="supplementary lines: iteration schedule of the solves")
@@ -1000,11 +1002,29 @@ def run_profile_driver(args):
                             reuse_pack=True)
         lds.sinkhorn_step_f(X, Y, g, eps, precision=args.precision, out=f, workspace=ws,
                             reuse_pack=True)
+    extra = ""
+    if args.diagnostics:
+        # then the weighted-sum passes at those potentials: per round one plan diagnostics
+        # (P 1, P^T 1, Hadamard) and one P V with k = 128
+        dws = lds.Workspace(int(lds.library().flashot_diagnostics_workspace_bytes(
+            pr.n, pr.m, pr.d, lds._flags(args.precision))))
+        aws = lds.Workspace(lds.workspace_bytes(pr.n, pr.m, pr.d, 128, args.precision))
+        V = torch.randn(pr.m, 128, device="cuda")
+        PV = torch.empty(pr.n, 128, device="cuda")
+        for _ in range(args.profile_passes):
+            lds.plan_diagnostics(X, Y, f, g, eps, precision=args.precision, workspace=dws,
+                                 as_dict=False)
+            lds.transport_apply(X, Y, f, g, eps, V, precision=args.precision, out=PV,
+                                workspace=aws)
+        torch.cuda.synchronize()
+        if lds.workspace_status(dws) != 0 or lds.workspace_status(aws) != 0:
+            raise RuntimeError("device timeout reported")
+        extra = f", then {args.profile_passes} x (diagnostics + P V k=128)"
     torch.cuda.synchronize()
     if lds.workspace_status(ws) != 0:
         raise RuntimeError("device timeout reported")
     print(f"profile driver: n=m={pr.n} d={pr.d} {args.precision}: "
-          f"{2 * args.profile_passes + 1} LSE passes, f[0]={float(f[0]):.6f}")
+          f"{2 * args.profile_passes + 1} LSE passes{extra}, f[0]={float(f[0]):.6f}")
 
 
 def main():

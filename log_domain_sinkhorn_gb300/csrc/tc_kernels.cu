@@ -66,24 +66,28 @@ __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
 }
 
 // 64 columns of one S-tile row: scores s2 = kappa * dot + bias, then the online base-2
-// (max, sum) update (rescaled only when the chunk raises the running max). One FFMA, half a
-// 3-input max, one FADD, one SFU ex2 and one FADD per score.
+// (max, sum) update (rescaled only when the chunk raises the running max). Pairs of scores
+// go through packed fp32x2 instructions: per score half an FFMA2, half a 3-input max, half
+// an FADD2, one SFU ex2 and half an FADD2. kLdg: read the biases through the read-only
+// path (global memory) rather than as plain loads (biases staged in shared memory).
+template <bool kLdg>
 __device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __restrict__ cb,
                                             float kappa, float& M, float& S) {
-  // Four independent running maxima / eight sums keep the dependency chains short.
+  const uint64_t k2 = ptx::pack2(kappa, kappa);
+  // Four independent running maxima / four packed sums keep the dependency chains short.
   float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
 #pragma unroll
   for (int j = 0; j < 64; j += 8) {
-    const float4 b4 = __ldg(cb + j / 4);
-    const float4 b5 = __ldg(cb + j / 4 + 1);
-    v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
-    v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
-    v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
-    v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
-    v[j + 4] = fmaf(kappa, v[j + 4], b5.x);
-    v[j + 5] = fmaf(kappa, v[j + 5], b5.y);
-    v[j + 6] = fmaf(kappa, v[j + 6], b5.z);
-    v[j + 7] = fmaf(kappa, v[j + 7], b5.w);
+    const float4 b4 = kLdg ? __ldg(cb + j / 4) : cb[j / 4];
+    const float4 b5 = kLdg ? __ldg(cb + j / 4 + 1) : cb[j / 4 + 1];
+    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 0], v[j + 1]), ptx::pack2(b4.x, b4.y)),
+                 v[j + 0], v[j + 1]);
+    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 2], v[j + 3]), ptx::pack2(b4.z, b4.w)),
+                 v[j + 2], v[j + 3]);
+    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 4], v[j + 5]), ptx::pack2(b5.x, b5.y)),
+                 v[j + 4], v[j + 5]);
+    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 6], v[j + 7]), ptx::pack2(b5.z, b5.w)),
+                 v[j + 6], v[j + 7]);
     m0 = ptx::max3(m0, v[j + 0], v[j + 1]);
     m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
     m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
@@ -94,48 +98,21 @@ __device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __rest
     S *= ex2(M - mx);
     M = mx;
   }
-  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint64_t nm2 = ptx::pack2(-M, -M);
+  uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int j = 0; j < 64; j += 8) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) s[u] += ex2(v[j + u] - M);
+    for (int u = 0; u < 4; ++u) {
+      float d0, d1;
+      ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2 * u], v[j + 2 * u + 1]), nm2), d0, d1);
+      s2[u] = ptx::add2(s2[u], ptx::pack2(ex2(d0), ex2(d1)));
+    }
   }
-  S += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-}
-
-// The same for biases staged in shared memory (plain loads).
-__device__ __forceinline__ void lse_chunk64_sb(float (&v)[64], const float4* cb, float kappa,
-                                               float& M, float& S) {
-  float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
-#pragma unroll
-  for (int j = 0; j < 64; j += 8) {
-    const float4 b4 = cb[j / 4];
-    const float4 b5 = cb[j / 4 + 1];
-    v[j + 0] = fmaf(kappa, v[j + 0], b4.x);
-    v[j + 1] = fmaf(kappa, v[j + 1], b4.y);
-    v[j + 2] = fmaf(kappa, v[j + 2], b4.z);
-    v[j + 3] = fmaf(kappa, v[j + 3], b4.w);
-    v[j + 4] = fmaf(kappa, v[j + 4], b5.x);
-    v[j + 5] = fmaf(kappa, v[j + 5], b5.y);
-    v[j + 6] = fmaf(kappa, v[j + 6], b5.z);
-    v[j + 7] = fmaf(kappa, v[j + 7], b5.w);
-    m0 = ptx::max3(m0, v[j + 0], v[j + 1]);
-    m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
-    m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
-    m3 = ptx::max3(m3, v[j + 6], v[j + 7]);
-  }
-  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
-  if (mx > M) {
-    S *= ex2(M - mx);
-    M = mx;
-  }
-  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 64; j += 8) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) s[u] += ex2(v[j + u] - M);
-  }
-  S += ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+  const uint64_t t2 = ptx::add2(ptx::add2(s2[0], s2[1]), ptx::add2(s2[2], s2[3]));
+  float t0, t1;
+  ptx::unpack2(t2, t0, t1);
+  S += t0 + t1;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -334,12 +311,12 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
         float v[64];
         ptx::tmem_ld_x64_sync(taddr, v);
-        lse_chunk64_sb(v, cb, kappa, M, S);
+        lse_chunk64<false>(v, cb, kappa, M, S);
         ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_chunk64_sb(v, cb + 16, kappa, M, S);
+        lse_chunk64<false>(v, cb + 16, kappa, M, S);
         __syncwarp();  // every lane is done with bslot[bs] before it is refilled
         bs ^= 1;
       }
@@ -370,12 +347,12 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
         float v[64];
         ptx::tmem_ld_x64_sync(taddr, v);
-        lse_chunk64(v, cb, kappa, M, S);
+        lse_chunk64<true>(v, cb, kappa, M, S);
         ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_chunk64(v, cb + 16, kappa, M, S);
+        lse_chunk64<true>(v, cb + 16, kappa, M, S);
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
