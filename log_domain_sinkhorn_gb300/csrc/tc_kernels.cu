@@ -65,19 +65,29 @@ __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
   ctl.abort_flag = 1;
 }
 
-// 64 columns of one S-tile row: scores s2 = kappa * dot + bias, then the online base-2
-// (max, sum) update (rescaled only when the chunk raises the running max). Pairs of scores
-// go through packed fp32x2 instructions: per score half an FFMA2, half a 3-input max, half
-// an FADD2, one SFU ex2 and half an FADD2. kLdg: read the biases through the read-only
-// path (global memory) rather than as plain loads (biases staged in shared memory).
-template <bool kLdg>
-__device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __restrict__ cb,
-                                            float kappa, float& M, float& S) {
+// Lazy rescaling of the online (max, sum): a chunk is exponentiated against the running max
+// M of the earlier chunks in the same pass that finds its own max, so the ex2 work does not
+// wait for the chunk's max. M is raised only when the chunk's max exceeds it by more than
+// kLazyRescale (then the chunk's sums are taken again against the new max); otherwise the
+// terms are at most 2^kLazyRescale, far inside fp32 range. The first chunk of a row
+// segment (M at its floor) always takes the second pass.
+constexpr float kLazyRescale = 8.0f;
+
+// kN (a multiple of 8) columns of one S-tile row: scores s2 = kappa * dot + bias and the online
+// base-2 (max, sum) update. Pairs of scores go through packed fp32x2 instructions: per
+// score half an FFMA2, half a 3-input max, half an FADD2, one SFU ex2 and half an FADD2.
+// kLdg: read the biases through the read-only path (global memory) rather than as plain
+// loads (biases staged in shared memory).
+template <int kN, bool kLdg>
+__device__ __forceinline__ void lse_chunk(float (&v)[kN], const float4* __restrict__ cb,
+                                          float kappa, float& M, float& S) {
   const uint64_t k2 = ptx::pack2(kappa, kappa);
+  uint64_t nm2 = ptx::pack2(-M, -M);
   // Four independent running maxima / four packed sums keep the dependency chains short.
   float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
+  uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int j = 0; j < 64; j += 8) {
+  for (int j = 0; j < kN; j += 8) {
     const float4 b4 = kLdg ? __ldg(cb + j / 4) : cb[j / 4];
     const float4 b5 = kLdg ? __ldg(cb + j / 4 + 1) : cb[j / 4 + 1];
     ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 0], v[j + 1]), ptx::pack2(b4.x, b4.y)),
@@ -92,21 +102,28 @@ __device__ __forceinline__ void lse_chunk64(float (&v)[64], const float4* __rest
     m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
     m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
     m3 = ptx::max3(m3, v[j + 6], v[j + 7]);
-  }
-  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
-  if (mx > M) {
-    S *= ex2(M - mx);
-    M = mx;
-  }
-  const uint64_t nm2 = ptx::pack2(-M, -M);
-  uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-  for (int j = 0; j < 64; j += 8) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       float d0, d1;
       ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2 * u], v[j + 2 * u + 1]), nm2), d0, d1);
       s2[u] = ptx::add2(s2[u], ptx::pack2(ex2(d0), ex2(d1)));
+    }
+  }
+  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
+  if (mx > M + kLazyRescale) {  // rare: raise the max and take the sums again
+    S *= ex2(M - mx);
+    M = mx;
+    nm2 = ptx::pack2(-M, -M);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) s2[u] = 0ull;
+#pragma unroll
+    for (int j = 0; j < kN; j += 8) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float d0, d1;
+        ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2 * u], v[j + 2 * u + 1]), nm2), d0, d1);
+        s2[u] = ptx::add2(s2[u], ptx::pack2(ex2(d0), ex2(d1)));
+      }
     }
   }
   const uint64_t t2 = ptx::add2(ptx::add2(s2[0], s2[1]), ptx::add2(s2[2], s2[3]));
@@ -135,9 +152,11 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
               unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
+  constexpr int kGroups = 2;               // column halves per tile (one warp per lane quarter)
+  constexpr int kCols = kLseBN / kGroups;  // columns of a tile per epilogue warp
   // Column biases of the current and the next tile, per epilogue warp (its 128 columns).
   __shared__ __align__(16) float bias_s[kStageBias ? kLseEpiThreads / 32 : 1][2]
-                                       [kStageBias ? 128 : 4];
+                                       [kStageBias ? kCols : 4];
   constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
   constexpr uint32_t kBChunk = 2u * kChunk;  // 256 rows x 128 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -281,9 +300,9 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     bool ok = true;
     // The warp's 128 biases of a tile (512 B, 16 per lane) are copied global -> shared with
     // cp.async one tile ahead into one of two slots.
-    float (*bslot)[kStageBias ? 128 : 4] = bias_s[kStageBias ? warp - 2 : 0];
+    float (*bslot)[kStageBias ? kCols : 4] = bias_s[kStageBias ? warp - 2 : 0];
     auto stage_bias = [&](int64_t tile, int slot) {
-      const float* src = colBias + (tile % NT) * kLseBN + h * 128 + lane * 4;
+      const float* src = colBias + (tile % NT) * kLseBN + h * kCols + lane * 4;
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                        ptx::smem_u32(&bslot[slot][lane * 4])),
                    "l"(src)
@@ -308,21 +327,23 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const float4* cb = reinterpret_cast<const float4*>(bslot[bs]);
         if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
+        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * kCols;
+        // Two halves of the warp's columns; the accumulator is released after the second
+        // load, so the MMA may refill it while the second half is reduced.
         float v[64];
         ptx::tmem_ld_x64_sync(taddr, v);
-        lse_chunk64<false>(v, cb, kappa, M, S);
+        lse_chunk<64, false>(v, cb, kappa, M, S);
         ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_chunk64<false>(v, cb + 16, kappa, M, S);
+        lse_chunk<64, false>(v, cb + 16, kappa, M, S);
         __syncwarp();  // every lane is done with bslot[bs] before it is refilled
         bs ^= 1;
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
-      const int64_t slot = 2 * (cta - sk_owner(rt * NT, T, G)) + h;
+      const int64_t slot = kGroups * (cta - sk_owner(rt * NT, T, G)) + h;
       if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
       t = seg_end;
     }
@@ -347,16 +368,16 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
         float v[64];
         ptx::tmem_ld_x64_sync(taddr, v);
-        lse_chunk64<true>(v, cb, kappa, M, S);
+        lse_chunk<64, true>(v, cb, kappa, M, S);
         ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
         ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_chunk64<true>(v, cb + 16, kappa, M, S);
+        lse_chunk<64, true>(v, cb + 16, kappa, M, S);
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
-      const int64_t slot = 2 * (cta - sk_owner(rt * NT, T, G)) + h;
+      const int64_t slot = kGroups * (cta - sk_owner(rt * NT, T, G)) + h;
       if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
       t = seg_end;
     }

@@ -230,6 +230,7 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
       const int64_t grp = vr / row_tiles, rt = vr - grp * row_tiles;
       const int64_t row = rt * kBM + rloc;
       const float rb = row < n_rows ? rowBias[row] : neg_inf();
+      const uint64_t rb2 = ptx::pack2(rb, rb), k2 = ptx::pack2(kappa, kappa);
       float sumw = 0.0f, had = 0.0f;
       for (int64_t tt = t; tt < seg_end; ++tt) {
         const int jt = (int)(tt - vr * NT);
@@ -247,34 +248,47 @@ wsum2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ C
         ptx::tc_fence_before();
         ptx::mbar_arrive(&ctl.s_empty);   // S may now be overwritten by the next tile
         ++s_uses;
+        // Pairs of scores through packed fp32x2 instructions: w = 2^((kappa S + b_j) + b_i).
+        // For the second MMA each pair is rounded to bf16 at once (wp[c] holds the weights
+        // of K = 128h + 2c, 2c + 1), so the fp32 scores die as they are consumed.
+        uint64_t sw2 = 0ull, hd2 = 0ull;
+        uint32_t wp[kHad ? 1 : 64];
 #pragma unroll
         for (int j = 0; j < 128; j += 4) {
           const float4 b4 = __ldg(cb + j / 4);
-          const float w0 = ex2(fmaf(kappa, v[j + 0], b4.x) + rb);
-          const float w1 = ex2(fmaf(kappa, v[j + 1], b4.y) + rb);
-          const float w2 = ex2(fmaf(kappa, v[j + 2], b4.z) + rb);
-          const float w3 = ex2(fmaf(kappa, v[j + 3], b4.w) + rb);
+          const uint64_t e01 = ptx::add2(ptx::fma2(k2, ptx::pack2(v[j + 0], v[j + 1]),
+                                                   ptx::pack2(b4.x, b4.y)), rb2);
+          const uint64_t e23 = ptx::add2(ptx::fma2(k2, ptx::pack2(v[j + 2], v[j + 3]),
+                                                   ptx::pack2(b4.z, b4.w)), rb2);
+          float x0, x1, x2, x3;
+          ptx::unpack2(e01, x0, x1);
+          ptx::unpack2(e23, x2, x3);
+          const float w0 = ex2(x0), w1 = ex2(x1), w2 = ex2(x2), w3 = ex2(x3);
+          const uint64_t w01 = ptx::pack2(w0, w1);
+          const uint64_t w23 = ptx::pack2(w2, w3);
           if constexpr (kHad) {
-            had = fmaf(w0, v[j + 0], had);
-            had = fmaf(w1, v[j + 1], had);
-            had = fmaf(w2, v[j + 2], had);
-            had = fmaf(w3, v[j + 3], had);
+            hd2 = ptx::fma2(w01, ptx::pack2(v[j + 0], v[j + 1]), hd2);
+            hd2 = ptx::fma2(w23, ptx::pack2(v[j + 2], v[j + 3]), hd2);
+          } else {
+            __nv_bfloat162 h01 = __floats2bfloat162_rn(w0, w1);
+            __nv_bfloat162 h23 = __floats2bfloat162_rn(w2, w3);
+            wp[j / 2] = *reinterpret_cast<uint32_t*>(&h01);
+            wp[j / 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
           }
-          sumw += (w0 + w1) + (w2 + w3);
-          v[j + 0] = w0;
-          v[j + 1] = w1;
-          v[j + 2] = w2;
-          v[j + 3] = w3;
+          sw2 = ptx::add2(sw2, ptx::add2(w01, w23));
+        }
+        {
+          float a0, a1;
+          ptx::unpack2(sw2, a0, a1);
+          sumw += a0 + a1;
+          if constexpr (kHad) {
+            ptx::unpack2(hd2, a0, a1);
+            had += a0 + a1;
+          }
         }
         if constexpr (!kHad) {
           // This warp's 128 weights are W row rloc, K = 128h .. 128h + 127: 64 columns of
           // bf16 pairs at TMEM column 256 + 64h.
-          uint32_t wp[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            __nv_bfloat162 hp = __floats2bfloat162_rn(v[2 * c], v[2 * c + 1]);
-            wp[c] = *reinterpret_cast<uint32_t*>(&hp);
-          }
           if (!ptx::mbar_wait(&ctl.w_empty, par(w_uses) ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
           ptx::tmem_st_x64_sync(tmem + lane_base + kTmemW + (uint32_t)h * 64u, wp);
