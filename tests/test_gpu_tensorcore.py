@@ -239,6 +239,55 @@ def test_apply_grad_hadamard_workload5_scaled(cuda_lib, precision):
     assert scaled_linf(grad, oracle.grad_x(pr.X, pr.Y, pr.a, pr.b, g32, eps)) <= tol
 
 
+@pytest.mark.parametrize("precision", TC_PRECS)
+def test_full_size_workload5_apply_sampled(cuda_lib, precision):
+    """Transport application at full size (n = m = 20000, d = 1024, k = 128, eps = 0.1) in
+    the benchmark's launch configuration. The GPU's own 100-iteration solve gives the
+    potentials; P V, P^T U and the Hadamard sums are compared on sampled rows (columns for
+    P^T U) with the oracle evaluated at those fp32 potentials, each sampled output computed
+    against every point of the other cloud."""
+    from gpu_helpers import OUT_TOL
+    lds = cuda_lib
+    pr = workload(5)
+    X, Y, a, b = problem_tensors(pr)
+    eps = float(pr.eps_schedule[0])
+    f, g, _ = lds.sinkhorn_solve(X, Y, a, b, list(pr.eps_schedule), pr.iters_per_stage,
+                                 precision=precision)
+    PV = lds.transport_apply(X, Y, f, g, eps, to_dev(pr.V), a, b,
+                             precision=precision).cpu().numpy()
+    PtU = lds.transport_apply(X, Y, f, g, eps, to_dev(pr.U), a, b, transpose=True,
+                              precision=precision).cpu().numpy()
+    h = lds.transport_hadamard_xy(X, Y, f, g, eps, a, b, precision=precision).cpu().numpy()
+    f_np, g_np = f.cpu().numpy(), g.cpu().numpy()
+    rows, cols = _sample(pr.n, 21), _sample(pr.m, 22)
+    tol = OUT_TOL[precision]
+    ref = oracle.transport_apply(pr.X, pr.Y, pr.a, pr.b, f_np, g_np, eps, pr.V, rows=rows)
+    assert scaled_linf(PV[rows], ref) <= tol
+    ref = oracle.transport_apply(pr.X, pr.Y, pr.a, pr.b, f_np, g_np, eps, pr.U,
+                                 transpose=True, rows=cols)
+    assert scaled_linf(PtU[cols], ref) <= tol
+    ref = oracle.hadamard_xy(pr.X, pr.Y, pr.a, pr.b, f_np, g_np, eps, rows=rows)
+    assert scaled_linf(h[rows], ref) <= tol
+
+
+@pytest.mark.parametrize("precision", TC_PRECS)
+def test_full_size_workload3_grad_sampled(cuda_lib, precision):
+    """The benchmark step's gradient at full size (n = m = 50000, d = 512, eps = 0.1, after
+    the 100-iteration solve): grad_i = 2 a_i (x_i - yhat_i) on sampled rows against the
+    oracle at the GPU's final g."""
+    from gpu_helpers import OUT_TOL
+    lds = cuda_lib
+    pr = workload(3)
+    X, Y, a, b = problem_tensors(pr)
+    eps = float(pr.eps_schedule[0])
+    _, g, _ = lds.sinkhorn_solve(X, Y, a, b, list(pr.eps_schedule), pr.iters_per_stage,
+                                 precision=precision)
+    grad = lds.ot_grad_x(X, Y, g, eps, a, b, precision=precision).cpu().numpy()
+    rows = _sample(pr.n, 31)
+    ref = oracle.grad_x(pr.X, pr.Y, pr.a, pr.b, g.cpu().numpy(), eps, rows=rows)
+    assert scaled_linf(grad[rows], ref) <= OUT_TOL[precision]
+
+
 def test_split_tf32_anneal_rect_d16_scaled(cuda_lib):
     """The split-tf32 mode on the low-eps rectangular d = 16 workload (Dirichlet weights,
     eps 1.0 -> 0.01 over 10 stages; scaled to n = 600, m = 2400, 20 iterations per stage),
