@@ -152,11 +152,11 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
               unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
-  constexpr int kGroups = 2;               // column halves per tile (one warp per lane quarter)
-  constexpr int kCols = kLseBN / kGroups;  // columns of a tile per epilogue warp
-  // Column biases of the current and the next tile, per epilogue warp (its 128 columns).
+  constexpr int kGroups = 2;               // partial slots per CTA and row tile
+  constexpr int kCols = kLseBN / kGroups;  // columns of a tile per epilogue warp (direct biases)
+  // kStageBias: column biases of the warp's current and next tile (all 256 columns).
   __shared__ __align__(16) float bias_s[kStageBias ? kLseEpiThreads / 32 : 1][2]
-                                       [kStageBias ? kCols : 4];
+                                       [kStageBias ? kLseBN : 4];
   constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
   constexpr uint32_t kBChunk = 2u * kChunk;  // 256 rows x 128 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,7 +176,8 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.acc_full[b], 1);
-      ptx::mbar_init(&ctl.acc_empty[b], kLseEpiThreads);
+      // staged biases: the four warps of one tile parity read a tile; otherwise all eight
+      ptx::mbar_init(&ctl.acc_empty[b], kStageBias ? kLseEpiThreads / 2 : kLseEpiThreads);
     }
     ptx::mbar_init(&ctl.a_full, 1);
     ptx::mbar_init(&ctl.a_empty, 1);
@@ -296,54 +297,66 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
     const int h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     if constexpr (kStageBias) {
-    uint32_t ab = 0, acc_ph = 0;
+    // Short contractions: the two warps of a sub-partition take alternate tiles (warp of
+    // parity p = h reads every tile k = p, p + 2, ... of the CTA's range, all 256 columns,
+    // from accumulator p), so their SFU bursts and their loads and max phases interleave
+    // instead of coinciding. Each (row, parity) keeps its own online (max, sum) and becomes
+    // its own partial slot.
+    const int par = h;
+    uint32_t acc_ph = 0;
     bool ok = true;
-    // The warp's 128 biases of a tile (512 B, 16 per lane) are copied global -> shared with
-    // cp.async one tile ahead into one of two slots.
-    float (*bslot)[kStageBias ? kCols : 4] = bias_s[kStageBias ? warp - 2 : 0];
+    // The warp's 256 biases of a tile (1 KB, 32 per lane) are copied global -> shared with
+    // cp.async one own tile ahead into one of two slots.
+    float (*bslot)[kStageBias ? kLseBN : 4] = bias_s[kStageBias ? warp - 2 : 0];
     auto stage_bias = [&](int64_t tile, int slot) {
-      const float* src = colBias + (tile % NT) * kLseBN + h * kCols + lane * 4;
+      const float* src = colBias + (tile % NT) * kLseBN + lane * 4;
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                        ptx::smem_u32(&bslot[slot][lane * 4])),
                    "l"(src)
+                   : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       ptx::smem_u32(&bslot[slot][128 + lane * 4])),
+                   "l"(src + 128)
                    : "memory");
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
     int bs = 0;
     griddep_wait();  // the biases (and the partial buffer) belong to the previous kernel
-    if (t_begin < t_end) stage_bias(t_begin, 0);
+    if (t_begin + par < t_end) stage_bias(t_begin + par, 0);
     for (int64_t t = t_begin; ok && t < t_end;) {
       const int64_t rt = t / NT;
       const int64_t seg_end = min(t_end, (rt + 1) * NT);
       float M = kNegBig, S = 0.0f;
-      for (int64_t tt = t; tt < seg_end; ++tt) {
-        if (tt + 1 < t_end) {
-          stage_bias(tt + 1, bs ^ 1);
+      // this warp's first tile of the segment: (tt - t_begin) % 2 == par
+      for (int64_t tt = t + (((t - t_begin) & 1) != par ? 1 : 0); tt < seg_end; tt += 2) {
+        if (tt + 2 < t_end) {
+          stage_bias(tt + 2, bs ^ 1);
           asm volatile("cp.async.wait_group 1;" ::: "memory");
         } else {
           asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
         __syncwarp();
         const float4* cb = reinterpret_cast<const float4*>(bslot[bs]);
-        if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
+        if (!ptx::mbar_wait(&ctl.acc_full[par], acc_ph)) { ok = false; break; }
         ptx::tc_fence_after();
-        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * kCols;
-        // Two halves of the warp's columns; the accumulator is released after the second
-        // load, so the MMA may refill it while the second half is reduced.
+        const uint32_t taddr = tmem + lane_base + (uint32_t)par * kLseBN;
         float v[64];
-        ptx::tmem_ld_x64_sync(taddr, v);
-        lse_chunk<64, false>(v, cb, kappa, M, S);
-        ptx::tmem_ld_x64_sync(taddr + 64, v);
+#pragma unroll 1
+        for (int c = 0; c < 3; ++c) {
+          ptx::tmem_ld_x64_sync(taddr + c * 64, v);
+          lse_chunk<64, false>(v, cb + c * 16, kappa, M, S);
+        }
+        ptx::tmem_ld_x64_sync(taddr + 192, v);
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl.acc_empty[ab]);   // this warp's part of the tile is read
-        if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
-        lse_chunk<64, false>(v, cb + 16, kappa, M, S);
+        ptx::mbar_arrive(&ctl.acc_empty[par]);   // this warp's part of the tile is read
+        acc_ph ^= 1u;
+        lse_chunk<64, false>(v, cb + 48, kappa, M, S);
         __syncwarp();  // every lane is done with bslot[bs] before it is refilled
         bs ^= 1;
       }
       if (!ok) break;
       const int64_t row = rt * kBM + q * 32 + lane;
-      const int64_t slot = kGroups * (cta - sk_owner(rt * NT, T, G)) + h;
+      const int64_t slot = kGroups * (cta - sk_owner(rt * NT, T, G)) + par;
       if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
       t = seg_end;
     }
@@ -756,7 +769,7 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
                       float2* partial, int64_t ld, unsigned* status, cudaStream_t st) {
   // Static shared memory: the control block and the staged column biases.
   const int ctrl = (int)sizeof(Ctrl) +
-                   (kStageBias ? kLseEpiThreads / 32 * 2 * 128 : 2 * 4) * (int)sizeof(float);
+                   (kStageBias ? kLseEpiThreads / 32 * 2 * kLseBN : 2 * 4) * (int)sizeof(float);
   const int a_bytes = kARes ? kc * kChunk : 0;
   const int stage_bytes = kARes ? 2 * kChunk : 3 * kChunk;
   const int budget = kSmemLimit - ctrl - 1024 - a_bytes;
