@@ -477,11 +477,15 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
   wsum_fma_small_kernel<DPV, MODEV, KOV, RV><<<grid, kFmaThreads, 0, c.st>>>(                \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
       out, ldo, rowU, tps, part, rows_pad, kp)
+#define FLASHOT_WSUM_PAIR(DPV, MODEV, KOV, RV)                                               \
+  wsum_fma_pair_kernel<DPV, MODEV, KOV, RV><<<grid, kFmaThreads, 0, c.st>>>(                 \
+      rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
+      out, ldo, rowU, tps, part, rows_pad, kp)
 #define FLASHOT_WSUM_MODES(DPV)                                                     \
   case DPV:                                                                         \
-    if (narrow) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 1, ((DPV) <= 16 ? 4 : 2));      \
-    else if (mid && mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 8, 2);  \
-    else if (mid) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 8, 2);                        \
+    if (narrow) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 1, ((DPV) <= 16 ? 4 : 2));       \
+    else if (mid && mode == kWsumApply) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 8, 2);   \
+    else if (mid) FLASHOT_WSUM_PAIR(DPV, kWsumHessT, 8, 2);                         \
     else if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 32, 1);        \
     else if (mode == kWsumGrad) FLASHOT_WSUM_SMALL(DPV, kWsumGrad, 32, 1);          \
     else if (mode == kWsumHessT) FLASHOT_WSUM_SMALL(DPV, kWsumHessT, 32, 1);        \
@@ -499,6 +503,7 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
       default: return FLASHOT_ERR_INVALID_ARG;
     }
 #undef FLASHOT_WSUM_MODES
+#undef FLASHOT_WSUM_PAIR
 #undef FLASHOT_WSUM_SMALL
   } else {
 #define FLASHOT_WSUM_GENERIC(MODEV, KOV)                                                      \

@@ -17,6 +17,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace flashot {
 
@@ -47,8 +48,53 @@ __device__ __forceinline__ void lse_chunk(const float (&s)[J], float& M, float& 
   S += acc;
 }
 
+// Online base-2 LSE update of two rows at once, (M0, S0) and (M1, S1), with a chunk of J
+// score pairs s2[j] = (row 0's score, row 1's score) (packed fp32x2): per-row maxima, then
+// the shift, the sum of exponentials and its accumulation on packed instructions.
+template <int J>
+__device__ __forceinline__ void lse_chunk_pair(const uint64_t (&s2)[J], float& M0, float& S0,
+                                               float& M1, float& S1) {
+  float a[J], b[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) ptx::unpack2(s2[j], a[j], b[j]);
+  float mx0 = a[0], mx1 = b[0];
+#pragma unroll
+  for (int j = 1; j + 1 < J; j += 2) {
+    mx0 = ptx::max3(mx0, a[j], a[j + 1]);
+    mx1 = ptx::max3(mx1, b[j], b[j + 1]);
+  }
+  if constexpr (J % 2 == 0) {
+    mx0 = fmaxf(mx0, a[J - 1]);
+    mx1 = fmaxf(mx1, b[J - 1]);
+  }
+  if (mx0 > M0) {
+    S0 *= ex2(M0 - mx0);
+    M0 = mx0;
+  }
+  if (mx1 > M1) {
+    S1 *= ex2(M1 - mx1);
+    M1 = mx1;
+  }
+  const uint64_t nm2 = ptx::pack2(-M0, -M1);
+  uint64_t acc2 = 0ull;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    float d0, d1;
+    ptx::unpack2(ptx::add2(s2[j], nm2), d0, d1);
+    acc2 = ptx::add2(acc2, ptx::pack2(ex2(d0), ex2(d1)));
+  }
+  float t0, t1;
+  ptx::unpack2(acc2, t0, t1);
+  S0 += t0;
+  S1 += t1;
+}
+
 // ---------------------------------------------------------------------------------------
-// LSE pass, d_pad = DP <= 32 (multiple of 4): each thread owns R rows, x in registers.
+// LSE pass, d_pad = DP <= 32 (multiple of 4): each thread owns R rows (R even), x in
+// registers as row pairs: x2[p][k] = (x_{2p,k}, x_{2p+1,k}). The staged column tile keeps
+// every coordinate and bias duplicated, (y_k, y_k), so one packed FMA (fma.rn.f32x2)
+// advances the dot products of two rows: half the issue slots of scalar FMAs for the same
+// FMA-pipe work.
 // rowP: n_rows x DP, colP: (n_col_tiles*kFmaBN) x DP, packed fp32 (zero padded).
 // Grid: (row blocks, splits). Split s covers column tiles [s*tps, (s+1)*tps).
 // ---------------------------------------------------------------------------------------
@@ -59,20 +105,30 @@ lse_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ c
                      int tiles_per_split, float kappa, float2* __restrict__ partial,
                      int64_t ld) {
   static_assert(DP % 4 == 0 && DP <= 32, "DP must be a multiple of 4, at most 32");
+  static_assert(R % 2 == 0, "rows are processed in pairs");
   static_assert(kFmaBN == kFmaThreads, "one bias entry per thread");
   constexpr int Q = DP / 4;
-  __shared__ float4 ys[kFmaBN * Q];
-  __shared__ float cs[kFmaBN];
+  constexpr int P = R / 2;
+  __shared__ __align__(16) float2 ys2[kFmaBN * DP];  // (y_k, y_k) per column and coordinate
+  __shared__ __align__(16) float2 cs2[kFmaBN];
   const int tid = threadIdx.x;
   const int64_t row0 = (int64_t)blockIdx.x * (kFmaThreads * R) + tid;
 
-  float4 x[R][Q];
+  uint64_t x2[P][DP];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int64_t row = row0 + (int64_t)r * kFmaThreads;
-    const float4* src = reinterpret_cast<const float4*>(rowP + (row < n_rows ? row : 0) * DP);
+  for (int p = 0; p < P; ++p) {
+    const int64_t ra = row0 + (int64_t)(2 * p) * kFmaThreads;
+    const int64_t rb = ra + kFmaThreads;
+    const float4* sa = reinterpret_cast<const float4*>(rowP + (ra < n_rows ? ra : 0) * DP);
+    const float4* sb = reinterpret_cast<const float4*>(rowP + (rb < n_rows ? rb : 0) * DP);
 #pragma unroll
-    for (int q = 0; q < Q; ++q) x[r][q] = src[q];
+    for (int q = 0; q < Q; ++q) {
+      const float4 a = sa[q], b = sb[q];
+      x2[p][4 * q + 0] = ptx::pack2(a.x, b.x);
+      x2[p][4 * q + 1] = ptx::pack2(a.y, b.y);
+      x2[p][4 * q + 2] = ptx::pack2(a.z, b.z);
+      x2[p][4 * q + 3] = ptx::pack2(a.w, b.w);
+    }
   }
   float M[R], S[R];
 #pragma unroll
@@ -80,35 +136,44 @@ lse_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ c
     M[r] = kNegBig;
     S[r] = 0.0f;
   }
+  const uint64_t k2 = ptx::pack2(kappa, kappa);
 
   const int t0 = blockIdx.y * tiles_per_split;
   const int t1 = min(t0 + tiles_per_split, n_col_tiles);
   for (int t = t0; t < t1; ++t) {
     __syncthreads();
-    const float4* src = reinterpret_cast<const float4*>(colP + (int64_t)t * kFmaBN * DP);
-    for (int e = tid; e < kFmaBN * Q; e += kFmaThreads) ys[e] = src[e];
-    cs[tid] = colBias[(int64_t)t * kFmaBN + tid];
+    const float* src = colP + (int64_t)t * kFmaBN * DP;
+    for (int e = tid; e < kFmaBN * DP; e += kFmaThreads) {
+      const float v = src[e];
+      ys2[e] = make_float2(v, v);
+    }
+    const float cb = colBias[(int64_t)t * kFmaBN + tid];
+    cs2[tid] = make_float2(cb, cb);
     __syncthreads();
+    const uint64_t* ysp = reinterpret_cast<const uint64_t*>(ys2);
+    const uint64_t* csp = reinterpret_cast<const uint64_t*>(cs2);
 #pragma unroll 1
     for (int jc = 0; jc < kFmaBN; jc += kFmaJ) {
-      float s[R][kFmaJ];
+      uint64_t s2[P][kFmaJ];
 #pragma unroll
       for (int jj = 0; jj < kFmaJ; ++jj) {
-        float acc[R];
+        const uint64_t* y2 = ysp + (jc + jj) * DP;
+        uint64_t acc[P];
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[r] = 0.0f;
+        for (int p = 0; p < P; ++p) acc[p] = 0ull;
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-          const float4 y = ys[(jc + jj) * Q + q];
+        for (int k = 0; k < DP; ++k) {
+          const uint64_t yk = y2[k];
 #pragma unroll
-          for (int r = 0; r < R; ++r) acc[r] = dot4(x[r][q], y, acc[r]);
+          for (int p = 0; p < P; ++p) acc[p] = ptx::fma2(x2[p][k], yk, acc[p]);
         }
-        const float c = cs[jc + jj];
+        const uint64_t c2 = csp[jc + jj];
 #pragma unroll
-        for (int r = 0; r < R; ++r) s[r][jj] = fmaf(kappa, acc[r], c);
+        for (int p = 0; p < P; ++p) s2[p][jj] = ptx::fma2(k2, acc[p], c2);
       }
 #pragma unroll
-      for (int r = 0; r < R; ++r) lse_chunk<kFmaJ>(s[r], M[r], S[r]);
+      for (int p = 0; p < P; ++p)
+        lse_chunk_pair<kFmaJ>(s2[p], M[2 * p], S[2 * p], M[2 * p + 1], S[2 * p + 1]);
     }
   }
 #pragma unroll
@@ -330,6 +395,173 @@ wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ 
       if (blockIdx.y == 0) pr[kp - 1] = (MODE == kWsumHadamard) ? had[r] : sumw[r];
     } else {
       wsum_store<MODE, KO>(acc[r], sumw[r], had[r], row, o0, k, rowW, Xrow, d, out, ldo);
+    }
+  }
+}
+
+// The same weighted sums with R (even) rows per thread processed as row pairs on packed
+// fp32x2 instructions, as in lse_fma_small_kernel: the row points (and the u_i of HessT) are
+// held as pairs x2[p][k] = (x_{2p,k}, x_{2p+1,k}); the staged column coordinates, biases and
+// values of V are duplicated, (v, v), so every packed operand is one shared-memory load.
+// Same arguments, grid and outputs as wsum_fma_small_kernel.
+template <int DP, int MODE, int KO, int R>
+__global__ void __launch_bounds__(kFmaThreads)
+wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
+                     const float* __restrict__ colBias, const float* __restrict__ rowBias,
+                     int64_t n_rows, int64_t n_cols, int n_col_tiles, float kappa,
+                     const float* __restrict__ V, int64_t ldv, int64_t k,
+                     const float* __restrict__ rowW, const float* __restrict__ Xrow,
+                     int64_t d, float* __restrict__ out, int64_t ldo,
+                     const float* __restrict__ rowU, int tiles_per_split = 0,
+                     float* __restrict__ part = nullptr, int64_t rows_pad = 0, int kp = 0) {
+  static_assert(R % 2 == 0, "rows are processed in pairs");
+  constexpr int Q = DP / 4;
+  constexpr int P = R / 2;
+  constexpr bool kHess = (MODE == kWsumHessT);
+  constexpr bool kHad = (MODE == kWsumHadamard);
+  constexpr int KV = kHad ? 1 : KO;
+  __shared__ __align__(16) float2 ys2[32 * DP];
+  __shared__ __align__(16) float2 cs2[32];
+  __shared__ __align__(16) float2 vs2[32][KV];
+  const int tid = threadIdx.x;
+  const int64_t row0 = (int64_t)blockIdx.x * kFmaThreads * R + tid;
+  const int64_t o0 = (int64_t)blockIdx.y * KO;
+  uint64_t x2[P][DP], u2[P][kHess ? DP : 1], rb2[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    const int64_t ra = row0 + (int64_t)(2 * p) * kFmaThreads;
+    const int64_t rb = ra + kFmaThreads;
+    const int64_t qa = ra < n_rows ? ra : 0, qb = rb < n_rows ? rb : 0;
+    const float4* xa = reinterpret_cast<const float4*>(rowP + qa * DP);
+    const float4* xb = reinterpret_cast<const float4*>(rowP + qb * DP);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const float4 a = xa[q], b = xb[q];
+      x2[p][4 * q + 0] = ptx::pack2(a.x, b.x);
+      x2[p][4 * q + 1] = ptx::pack2(a.y, b.y);
+      x2[p][4 * q + 2] = ptx::pack2(a.z, b.z);
+      x2[p][4 * q + 3] = ptx::pack2(a.w, b.w);
+    }
+    if constexpr (kHess) {
+      const float4* ua = reinterpret_cast<const float4*>(rowU + qa * DP);
+      const float4* ub = reinterpret_cast<const float4*>(rowU + qb * DP);
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const float4 a = ua[q], b = ub[q];
+        u2[p][4 * q + 0] = ptx::pack2(a.x, b.x);
+        u2[p][4 * q + 1] = ptx::pack2(a.y, b.y);
+        u2[p][4 * q + 2] = ptx::pack2(a.z, b.z);
+        u2[p][4 * q + 3] = ptx::pack2(a.w, b.w);
+      }
+    }
+    rb2[p] = ptx::pack2(ra < n_rows ? rowBias[ra] : neg_inf(),
+                        rb < n_rows ? rowBias[rb] : neg_inf());
+  }
+  uint64_t acc2[P][KV], sw2[P], hd2[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    sw2[p] = 0ull;
+    hd2[p] = 0ull;
+#pragma unroll
+    for (int o = 0; o < KV; ++o) acc2[p][o] = 0ull;
+  }
+  const uint64_t k2 = ptx::pack2(kappa, kappa);
+  int t_begin = 0, t_end = n_col_tiles;
+  if (part != nullptr) {
+    t_begin = (int)blockIdx.z * tiles_per_split;
+    t_end = min(n_col_tiles, t_begin + tiles_per_split);
+  }
+  for (int t = t_begin; t < t_end; ++t) {
+    __syncthreads();
+    const float* src = colP + (int64_t)t * 32 * DP;
+    for (int e = tid; e < 32 * DP; e += kFmaThreads) {
+      const float v = src[e];
+      ys2[e] = make_float2(v, v);
+    }
+    if (tid < 32) {
+      const float cb = colBias[(int64_t)t * 32 + tid];
+      cs2[tid] = make_float2(cb, cb);
+    }
+    if constexpr (!kHad) {
+      for (int e = tid; e < 32 * KO; e += kFmaThreads) {
+        const int c = e / KO, o = e % KO;
+        const int64_t j = (int64_t)t * 32 + c, oo = o0 + o;
+        const float v = (j < n_cols && oo < k) ? V[j * ldv + oo] : 0.0f;
+        vs2[c][o] = make_float2(v, v);
+      }
+    }
+    __syncthreads();
+    const uint64_t* ysp = reinterpret_cast<const uint64_t*>(ys2);
+    const uint64_t* csp = reinterpret_cast<const uint64_t*>(cs2);
+#pragma unroll 2
+    for (int c = 0; c < 32; ++c) {
+      const uint64_t* y2 = ysp + c * DP;
+      const uint64_t c2 = csp[c];
+      uint64_t vv[KV];
+      if constexpr (!kHad) {
+        const uint64_t* vp = reinterpret_cast<const uint64_t*>(vs2[c]);
+#pragma unroll
+        for (int o = 0; o < KV; ++o) vv[o] = vp[o];
+      }
+      uint64_t dot[P], tu[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        dot[p] = 0ull;
+        tu[p] = 0ull;
+      }
+#pragma unroll
+      for (int kk = 0; kk < DP; ++kk) {
+        const uint64_t yk = y2[kk];
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          dot[p] = ptx::fma2(x2[p][kk], yk, dot[p]);
+          if constexpr (kHess) tu[p] = ptx::fma2(u2[p][kk], yk, tu[p]);
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        float e0, e1;
+        ptx::unpack2(ptx::add2(ptx::fma2(k2, dot[p], c2), rb2[p]), e0, e1);
+        uint64_t w2 = ptx::pack2(ex2(e0), ex2(e1));
+        if constexpr (kHad) {
+          hd2[p] = ptx::fma2(w2, dot[p], hd2[p]);
+        } else {
+          if constexpr (kHess) w2 = ptx::mul2(w2, tu[p]);
+#pragma unroll
+          for (int o = 0; o < KV; ++o) acc2[p][o] = ptx::fma2(w2, vv[o], acc2[p][o]);
+          if constexpr (MODE == kWsumGrad) sw2[p] = ptx::add2(sw2[p], w2);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    float accA[KV], accB[KV];
+#pragma unroll
+    for (int o = 0; o < KV; ++o) ptx::unpack2(acc2[p][o], accA[o], accB[o]);
+    float swA, swB, hdA, hdB;
+    ptx::unpack2(sw2[p], swA, swB);
+    ptx::unpack2(hd2[p], hdA, hdB);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t row = row0 + (int64_t)(2 * p + h) * kFmaThreads;
+      if (row >= n_rows) continue;
+      // h is a compile-time constant in each unrolled copy: the selections stay in registers
+      float acc[KO];
+#pragma unroll
+      for (int o = 0; o < KO; ++o) acc[o] = kHad ? 0.0f : (h ? accB[o < KV ? o : 0] : accA[o < KV ? o : 0]);
+      const float sumw = h ? swB : swA, had = h ? hdB : hdA;
+      if (part != nullptr) {
+        float* pr = part + ((int64_t)blockIdx.z * rows_pad + row) * kp;
+        if constexpr (!kHad) {
+#pragma unroll
+          for (int o = 0; o < KO; ++o)
+            if (o0 + o < kp - 1) pr[o0 + o] = acc[o];
+        }
+        if (blockIdx.y == 0) pr[kp - 1] = kHad ? had : sumw;
+      } else {
+        wsum_store<MODE, KO>(acc, sumw, had, row, o0, k, rowW, Xrow, d, out, ldo);
+      }
     }
   }
 }
