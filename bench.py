@@ -427,6 +427,13 @@ def run_other_workload(args):
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["sfu_frac"] = (per_launch_scores / avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk)
+    if prec == "fp32" and d <= 32:
+        # FMA-pipe work per score of the small-d CUDA-core LSE: the padded dot product
+        # (d_pad lanes), kappa * dot + bias, the max shift and the sum (the max itself runs
+        # on the ALU pipe): d_pad + 3 lane operations against 128 lanes per SM per clock.
+        d_pad = (d + 3) // 4 * 4
+        roof["fma_pipe_frac"] = ((per_launch_scores / avg) * (d_pad + 3)
+                                 / (N_SMS * FP32_LANES_PER_SM * clk))
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
     graph = None
@@ -665,16 +672,30 @@ def run_hvp(args):
     nm = float(n) * float(n)
     passes = 2 * cg_iters + 5  # CG: P p and P^T t; plus [PY|r], [P^T V|P^T s|c], T, rhs, final
     pass_avg = ms_ws / max(n_ws, 1) / 1e3
+    # FMA-pipe lane operations per score of each streaming pass (d = 3, padded to 4): the
+    # dot product (4), kappa * dot + c_j and + r_i (2), then the weighted sums: one output
+    # column for P t / P^T t (1 + 2 per CG iteration), 8 (the kernel's padded output width)
+    # for [PY | r], [P^T V | P^T s | c] and [P diag(z) Y | P z], and for the curvature pass
+    # T also the dot <u_i, y_j> (4) and its product with the weight (1). The ex2 (one per
+    # score) runs on the SFU at 32 per clock per SM, never the limit here.
+    d_pad = 4
+    lane_ops = nm * ((d_pad + 3) * (1 + 2 * cg_iters) + (d_pad + 2 + 8) * 3
+                     + (d_pad + 2 + 8 + d_pad + 1))
+    passes_s = ms_ws / args.steps / 1e3
     line = {"metric": "Hessian-vector products of the OT loss w.r.t. X", "supplementary": True,
             "value": 1e3 / ms, "unit": "HVPs/s", "ms_per_hvp": ms, "cg_iterations": cg_iters,
             "cg_rel_residual": rel, "streaming_passes_per_hvp": passes,
             "ms_per_cg_iteration": ms / max(cg_iters, 1),
             "kernels_ms_per_hvp": {"streaming_passes": ms_ws / args.steps,
                                    "other": ms_ot / args.steps},
-            "roofline": {"bound": "alu (SFU ex2)", "kernel": "wsum_fma_small (streaming pass)",
-                         "achieved": nm / pass_avg / 1e9,
-                         "peak": N_SMS * SFU_EX2_PER_SM_CLK * clk / 1e9,
-                         "unit": "G ex2/s", "avg_pass_ms": pass_avg * 1e3},
+            "roofline": {"bound": "alu (fp32 FMA pipe)",
+                         "kernel": "wsum_fma_pair (streaming passes)",
+                         "achieved": lane_ops / passes_s / 1e12,
+                         "peak": N_SMS * FP32_LANES_PER_SM * clk / 1e12,
+                         "unit": "T FMA-pipe lane-ops/s",
+                         "lane_ops_per_hvp": lane_ops,
+                         "sfu_frac": (nm / pass_avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk),
+                         "avg_pass_ms": pass_avg * 1e3},
             "steps": args.steps, "warmup": args.warmup, "dtype": "fp32",
             "gpu_launches": int(launches),
             "config": {"workload": "hvp50k_d3: n=m=%d, d=3, Uniform[0,1]^3, uniform weights" % n,
