@@ -144,8 +144,10 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
   g->small = d <= 32;
   g->dpf = g->small ? round_up(d, 4) : round_up(d, 32);
   g->es = (p == FLASHOT_PREC_BF16) ? 2 : 4;
-  g->dpt = round_up(d, 128 / g->es);  // one 128-byte swizzle row per k-chunk
-  if (p == FLASHOT_PREC_TF32X3) g->dpt *= 3;  // [hi | hi | lo] against [hi | lo | hi]
+  // One 128-byte swizzle row per k-chunk. Split tf32 packs the three parts of the
+  // coordinates back to back ([hi | hi | lo] against [hi | lo | hi], d elements each) and
+  // pads the 3d elements once.
+  g->dpt = round_up(p == FLASHOT_PREC_TF32X3 ? 3 * d : d, 128 / g->es);
   return true;
 }
 

@@ -17,21 +17,25 @@ __device__ __forceinline__ uint32_t tf32_rna(float v) {
   return t;
 }
 
-// Split-tf32 packing: dst (rows_pad x 3*seg) holds three segments of seg columns each;
-// segment k holds part[k] of every coordinate, where part 0 = hi = tf32(x), part 1 = lo =
-// tf32(x - hi). pattern encodes the three parts (bits 0, 1, 2): 0b100 = [hi|hi|lo],
-// 0b010 = [hi|lo|hi]. Zero padding everywhere outside (rows, d).
+// Split-tf32 packing: row r of dst (ld elements) holds three segments of d columns each,
+// back to back; segment k holds part[k] of every coordinate, where part 0 = hi = tf32(x),
+// part 1 = lo = tf32(x - hi). pattern encodes the three parts (bits 0, 1, 2): 0b100 =
+// [hi|hi|lo], 0b010 = [hi|lo|hi]. Zero padding from column 3d to ld and in rows >= rows.
 static __global__ void pack_rows_tf32x3_kernel(const float* __restrict__ src, uint32_t* __restrict__ dst,
-                                        int64_t rows, int64_t d, int64_t rows_pad, int64_t seg,
+                                        int64_t rows, int64_t d, int64_t rows_pad, int64_t ld,
                                         int pattern) {
-  const int64_t total = rows_pad * 3 * seg;
+  const int64_t total = rows_pad * ld;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = e / (3 * seg);
-    const int64_t cc = e - r * 3 * seg;
-    const int part = (int)(cc / seg);
-    const int64_t c = cc - part * seg;
-    const float v = (r < rows && c < d) ? src[r * d + c] : 0.0f;
+    const int64_t r = e / ld;
+    const int64_t cc = e - r * ld;
+    if (cc >= 3 * d) {
+      dst[e] = 0u;
+      continue;
+    }
+    const int part = (int)(cc / d);
+    const int64_t c = cc - part * d;
+    const float v = r < rows ? src[r * d + c] : 0.0f;
     const uint32_t hi = tf32_rna(v);
     const uint32_t lo = tf32_rna(v - __uint_as_float(hi));
     dst[e] = ((pattern >> part) & 1) ? lo : hi;

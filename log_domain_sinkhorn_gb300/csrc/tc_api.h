@@ -15,7 +15,8 @@ int tc_selftest_bounded_wait(unsigned* status, int64_t limit_ns, cudaStream_t st
 
 // Pack X (n x d) and Y (m x d) fp32 into row-padded, K-padded operand copies for the
 // tensor cores: bf16 (round to nearest even) or tf32-rounded fp32.
-// mode: 0 = tf32, 1 = bf16, 2 = split tf32 (X = [hi|hi|lo], Y = [hi|lo|hi]; dpt = 3 segments).
+// mode: 0 = tf32, 1 = bf16, 2 = split tf32 (X = [hi|hi|lo], Y = [hi|lo|hi], three segments of
+// d elements back to back, padded to dpt).
 int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t m, int64_t d,
                    int64_t n_pad, int64_t m_pad, int64_t dpt, void* xq, void* yq, int sms,
                    cudaStream_t st);

@@ -742,12 +742,11 @@ int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t 
   const unsigned g2 = (unsigned)std::min<int64_t>((m_pad * dpt + T - 1) / T, (int64_t)sms * 16);
   const bool bf16 = (mode == 1);
   if (mode == 2) {
-    const int64_t seg = dpt / 3;
     { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
-      pack_rows_tf32x3_kernel<<<g1, T, 0, st>>>(X, static_cast<uint32_t*>(xq), n, d, n_pad, seg,
+      pack_rows_tf32x3_kernel<<<g1, T, 0, st>>>(X, static_cast<uint32_t*>(xq), n, d, n_pad, dpt,
                                                 0b100); }
     { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
-      pack_rows_tf32x3_kernel<<<g2, T, 0, st>>>(Y, static_cast<uint32_t*>(yq), m, d, m_pad, seg,
+      pack_rows_tf32x3_kernel<<<g2, T, 0, st>>>(Y, static_cast<uint32_t*>(yq), m, d, m_pad, dpt,
                                                 0b010); }
   } else if (bf16) {
     { TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
