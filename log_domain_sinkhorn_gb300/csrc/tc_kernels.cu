@@ -53,8 +53,8 @@ struct __align__(128) Ctrl {
   uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
-  uint64_t a_full;
-  uint64_t a_empty;
+  uint64_t a_full[2];   // resident row tile, up to two buffers (a_bufs)
+  uint64_t a_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -148,8 +148,8 @@ template <bool kBF16, bool kARes, bool kStageBias>
 __global__ void __launch_bounds__(kLseThreads, 1)
 lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
-              int kc_count, int stages, float kappa, float2* __restrict__ partial, int64_t ld,
-              unsigned* __restrict__ status) {
+              int kc_count, int stages, int a_bufs, float kappa, float2* __restrict__ partial,
+              int64_t ld, unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
   constexpr int kGroups = 2;               // partial slots per CTA and row tile
@@ -179,8 +179,10 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
       // staged biases: the four warps of one tile parity read a tile; otherwise all eight
       ptx::mbar_init(&ctl.acc_empty[b], kStageBias ? kLseEpiThreads / 2 : kLseEpiThreads);
     }
-    ptx::mbar_init(&ctl.a_full, 1);
-    ptx::mbar_init(&ctl.a_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl.a_full[b], 1);
+      ptx::mbar_init(&ctl.a_empty[b], 1);
+    }
     ptx::mbar_init(&ctl.mma_done, 1);
     ctl.abort_flag = 0;
     ptx::fence_barrier_init();
@@ -206,26 +208,30 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------- TMA producer -------------------------------------
-      uint32_t stage = 0, ph = 0, a_ph = 0;
-      int64_t issued = 0, a_issued = 0;
+      uint32_t stage = 0, ph = 0;
+      int64_t issued = 0, segs = 0;
       bool ok = true;
       for (int64_t t = t_begin; ok && t < t_end;) {
         const int64_t rt = t / NT;
         const int64_t seg_end = min(t_end, (rt + 1) * NT);
         if constexpr (kARes) {
-          if (!ptx::mbar_wait(&ctl.a_empty, a_ph ^ 1u)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(&ctl.a_full, a_bytes);
+          // segment s uses row-tile buffer s % a_bufs (its (s / a_bufs)-th use): with two
+          // buffers the next segment's rows load while the current one is still in use
+          const int ab = (int)(segs % a_bufs);
+          const uint32_t use = (uint32_t)(segs / a_bufs);
+          if (!ptx::mbar_wait(&ctl.a_empty[ab], (use & 1u) ^ 1u)) { ok = false; break; }
+          ptx::mbar_arrive_expect_tx(&ctl.a_full[ab], a_bytes);
           for (int kc = 0; kc < kc_count; ++kc)
-            ptx::tma_load_2d(&mapA, &ctl.a_full, smem + (size_t)kc * kChunk, kc * kElems,
+            ptx::tma_load_2d(&mapA, &ctl.a_full[ab],
+                             smem + (size_t)ab * a_bytes + (size_t)kc * kChunk, kc * kElems,
                              (int)(rt * kBM));
-          a_ph ^= 1u;
-          ++a_issued;
+          ++segs;
         }
         for (int64_t tt = t; ok && tt < seg_end; ++tt) {
           const int jt = (int)(tt - rt * NT);
           for (int kc = 0; kc < kc_count; ++kc) {
             if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
-            uint8_t* st = smem + a_bytes + (size_t)stage * stage_bytes;
+            uint8_t* st = smem + (size_t)a_bufs * a_bytes + (size_t)stage * stage_bytes;
             ptx::mbar_arrive_expect_tx(&ctl.full[stage], stage_bytes);
             if constexpr (!kARes)
               ptx::tma_load_2d(&mapA, &ctl.full[stage], st, kc * kElems, (int)(rt * kBM));
@@ -242,20 +248,27 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
         const int64_t arms = issued / stages + (s < issued % stages ? 1 : 0);
         if (arms > 0) ptx::mbar_wait(&ctl.full[s], (uint32_t)((arms - 1) & 1));
       }
-      if (a_issued > 0) ptx::mbar_wait(&ctl.a_full, (uint32_t)((a_issued - 1) & 1));
+      for (int b = 0; b < a_bufs && b < 2; ++b) {
+        const int64_t uses = segs / a_bufs + (b < segs % a_bufs ? 1 : 0);
+        if (uses > 0) ptx::mbar_wait(&ctl.a_full[b], (uint32_t)((uses - 1) & 1));
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------- MMA issuer ----------------------------------------
       constexpr uint32_t idesc = ptx::make_idesc<kBF16>(kBM, kLseBN);
-      uint32_t stage = 0, ph = 0, a_ph = 0, ab = 0, acc_ph = 0;
+      uint32_t stage = 0, ph = 0, ab = 0, acc_ph = 0;
+      int64_t segs = 0;
       bool ok = true;
       for (int64_t t = t_begin; ok && t < t_end;) {
         const int64_t rt = t / NT;
         const int64_t seg_end = min(t_end, (rt + 1) * NT);
+        const int abuf = kARes ? (int)(segs % a_bufs) : 0;
         if constexpr (kARes) {
-          if (!ptx::mbar_wait(&ctl.a_full, a_ph)) { ok = false; break; }
-          a_ph ^= 1u;
+          if (!ptx::mbar_wait(&ctl.a_full[abuf], (uint32_t)((segs / a_bufs) & 1))) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
         }
         for (int64_t tt = t; ok && tt < seg_end; ++tt) {
@@ -265,8 +278,9 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           for (int kc = 0; kc < kc_count; ++kc) {
             if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t st = base + a_bytes + stage * stage_bytes;
-            const uint32_t a_addr = kARes ? base + (uint32_t)kc * kChunk : st;
+            const uint32_t st = base + (uint32_t)a_bufs * a_bytes + stage * stage_bytes;
+            const uint32_t a_addr =
+                kARes ? base + (uint32_t)abuf * a_bytes + (uint32_t)kc * kChunk : st;
             const uint64_t a_desc = ptx::sdesc_k128(a_addr);
             const uint64_t b_desc = ptx::sdesc_k128(st + b_off);
 #pragma unroll
@@ -280,7 +294,8 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
           ptx::umma_commit(&ctl.acc_full[ab]);
           if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
         }
-        if constexpr (kARes) ptx::umma_commit(&ctl.a_empty);
+        if constexpr (kARes) ptx::umma_commit(&ctl.a_empty[abuf]);
+        ++segs;
         t = seg_end;
       }
       if (!ok) flag_error(ctl, status);
@@ -771,10 +786,13 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
                    (kStageBias ? kLseEpiThreads / 32 * 2 * kLseBN : 2 * 4) * (int)sizeof(float);
   const int a_bytes = kARes ? kc * kChunk : 0;
   const int stage_bytes = kARes ? 2 * kChunk : 3 * kChunk;
-  const int budget = kSmemLimit - ctrl - 1024 - a_bytes;
+  // A second row-tile buffer when at least four operand stages still fit beside it.
+  const int a_bufs =
+      (kARes && (kSmemLimit - ctrl - 1024 - 2 * a_bytes) / stage_bytes >= 4) ? 2 : 1;
+  const int budget = kSmemLimit - ctrl - 1024 - a_bufs * a_bytes;
   const int stages = std::min(kMaxStages, budget / stage_bytes);
   if (stages < 2) return FLASHOT_ERR_INVALID_ARG;
-  const int dyn = a_bytes + stages * stage_bytes + 1024;
+  const int dyn = a_bufs * a_bytes + stages * stage_bytes + 1024;
   auto kern = lse_tc_kernel<kBF16, kARes, kStageBias>;
   int rc = set_smem(kern, dyn);
   if (rc != FLASHOT_OK) return rc;
@@ -792,12 +810,12 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
       attr[0].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, kappa,
-                             partial, ld, status) != cudaSuccess)
+      if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, a_bufs,
+                             kappa, partial, ld, status) != cudaSuccess)
         return FLASHOT_ERR_CUDA;
     } else {
       kern<<<(unsigned)G, kLseThreads, dyn, st>>>(mA, mB, colBias, n_rows, NT, T, kc, stages,
-                                                  kappa, partial, ld, status);
+                                                  a_bufs, kappa, partial, ld, status);
     }
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
