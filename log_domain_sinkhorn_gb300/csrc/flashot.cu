@@ -479,10 +479,16 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
   wsum_fma_small_kernel<DPV, MODEV, KOV, RV><<<grid, kFmaThreads, 0, c.st>>>(                \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
       out, ldo, rowU, tps, part, rows_pad, kp)
-#define FLASHOT_WSUM_PAIR(DPV, MODEV, KOV, RV)                                               \
-  wsum_fma_pair_kernel<DPV, MODEV, KOV, RV><<<grid, kFmaThreads, 0, c.st>>>(                 \
+#define FLASHOT_WSUM_PAIR_F(DPV, MODEV, KOV, RV, FOLD)                                       \
+  wsum_fma_pair_kernel<DPV, MODEV, KOV, RV, FOLD><<<grid, kFmaThreads, 0, c.st>>>(           \
       rowP, colP, colBias, rowBias, n_rows, n_cols, n_tiles, kappa, V, ldv, k, rowW, X, g.d, \
       out, ldo, rowU, tps, part, rows_pad, kp)
+  // the row bias rides in the first padding lane when there is one
+#define FLASHOT_WSUM_PAIR(DPV, MODEV, KOV, RV)                                               \
+  do {                                                                                       \
+    if (g.d < (DPV)) FLASHOT_WSUM_PAIR_F(DPV, MODEV, KOV, RV, true);                         \
+    else FLASHOT_WSUM_PAIR_F(DPV, MODEV, KOV, RV, false);                                    \
+  } while (0)
 #define FLASHOT_WSUM_MODES(DPV)                                                     \
   case DPV:                                                                         \
     if (narrow) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 1, ((DPV) <= 16 ? 4 : 2));       \
@@ -506,6 +512,7 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
     }
 #undef FLASHOT_WSUM_MODES
 #undef FLASHOT_WSUM_PAIR
+#undef FLASHOT_WSUM_PAIR_F
 #undef FLASHOT_WSUM_SMALL
   } else {
 #define FLASHOT_WSUM_GENERIC(MODEV, KOV)                                                      \

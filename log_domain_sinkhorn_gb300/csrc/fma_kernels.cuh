@@ -404,7 +404,10 @@ wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ 
 // held as pairs x2[p][k] = (x_{2p,k}, x_{2p+1,k}); the staged column coordinates, biases and
 // values of V are duplicated, (v, v), so every packed operand is one shared-memory load.
 // Same arguments, grid and outputs as wsum_fma_small_kernel.
-template <int DP, int MODE, int KO, int R>
+// kFoldRow (d < DP, Apply and HessT only): the row bias rides in the first padding lane,
+// x_{i,d} = r_i / kappa against y_{j,d} = 1 in the staged column tile, so the dot product
+// already carries it and the epilogue saves the add (kappa dot + c_j, with no + r_i).
+template <int DP, int MODE, int KO, int R, bool kFoldRow = false>
 __global__ void __launch_bounds__(kFmaThreads)
 wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                      const float* __restrict__ colBias, const float* __restrict__ rowBias,
@@ -420,6 +423,7 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
   constexpr bool kHess = (MODE == kWsumHessT);
   constexpr bool kHad = (MODE == kWsumHadamard);
   constexpr int KV = kHad ? 1 : KO;
+  static_assert(!(kFoldRow && kHad), "the Hadamard sum needs the plain dot product");
   __shared__ __align__(16) float2 ys2[32 * DP];
   __shared__ __align__(16) float2 cs2[32];
   __shared__ __align__(16) float2 vs2[32][KV];
@@ -454,8 +458,15 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
         u2[p][4 * q + 3] = ptx::pack2(a.w, b.w);
       }
     }
-    rb2[p] = ptx::pack2(ra < n_rows ? rowBias[ra] : neg_inf(),
-                        rb < n_rows ? rowBias[rb] : neg_inf());
+    const float rba = ra < n_rows ? rowBias[ra] : neg_inf();
+    const float rbb = rb < n_rows ? rowBias[rb] : neg_inf();
+    rb2[p] = ptx::pack2(rba, rbb);
+    if constexpr (kFoldRow) {
+      const uint64_t f2 = ptx::pack2(rba / kappa, rbb / kappa);
+#pragma unroll
+      for (int kk = 0; kk < DP; ++kk)
+        if (kk == d) x2[p][kk] = f2;
+    }
   }
   uint64_t acc2[P][KV], sw2[P], hd2[P];
 #pragma unroll
@@ -475,7 +486,7 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
     __syncthreads();
     const float* src = colP + (int64_t)t * 32 * DP;
     for (int e = tid; e < 32 * DP; e += kFmaThreads) {
-      const float v = src[e];
+      const float v = (kFoldRow && e % DP == d) ? 1.0f : src[e];
       ys2[e] = make_float2(v, v);
     }
     if (tid < 32) {
@@ -521,7 +532,10 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
 #pragma unroll
       for (int p = 0; p < P; ++p) {
         float e0, e1;
-        ptx::unpack2(ptx::add2(ptx::fma2(k2, dot[p], c2), rb2[p]), e0, e1);
+        if constexpr (kFoldRow)
+          ptx::unpack2(ptx::fma2(k2, dot[p], c2), e0, e1);
+        else
+          ptx::unpack2(ptx::add2(ptx::fma2(k2, dot[p], c2), rb2[p]), e0, e1);
         uint64_t w2 = ptx::pack2(ex2(e0), ex2(e1));
         if constexpr (kHad) {
           hd2[p] = ptx::fma2(w2, dot[p], hd2[p]);
