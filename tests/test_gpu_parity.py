@@ -159,7 +159,11 @@ def _potentials(pr, iters=30):
                                      (1000, 700, 3, 1), (513, 1200, 20, 1), (700, 500, 30, 1),
                                      (2000, 3000, 16, 2), (300, 257, 64, 1),
                                      # 8-wide accumulator, two rows per thread
-                                     (1500, 900, 3, 5), (777, 1300, 28, 8)])
+                                     (1500, 900, 3, 5), (777, 1300, 28, 8),
+                                     # d not a multiple of 4: the row bias rides in the
+                                     # first padding lane (lane 1, 2, 5, 7, 13, 23)
+                                     (97, 131, 1, 1), (140, 90, 2, 3), (130, 70, 5, 1),
+                                     (65, 129, 7, 6), (255, 33, 13, 1), (31, 600, 23, 4)])
 def test_transport_apply_matches_oracle(cuda_lib, precision, n, m, d, k):
     lds = cuda_lib
     pr = make_problem(n, m, d, x_dist="normal_over_d", weights="dirichlet1", eps=0.1,
