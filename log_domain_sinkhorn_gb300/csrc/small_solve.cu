@@ -2,8 +2,8 @@
 //
 // When both clouds, all potentials and the score biases fit in one SM's shared memory, the
 // iteration is bound by launch latency (four launches per iteration on the streaming path).
-// Here one thread-block cluster of kCluster CTAs runs every stage and iteration inside a
-// single kernel (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract: the
+// Here one thread-block cluster (16 CTAs where the GPU can co-schedule that many, else 8)
+// runs every stage and iteration inside a single kernel (FlashSinkhorn: IO-Aware Entropic Optimal Transport on GPU, abstract: the
 // f- and g-updates as row-wise log-sum-exps; arithmetic identical to the CUDA-core path):
 //  - every CTA keeps X, Y, |x|^2, |y|^2, log2 a, log2 b and full copies of f and g;
 //  - for an f-update each CTA computes its slice of rows: lanes own rows, warps own slices
@@ -25,7 +25,8 @@
 namespace flashot {
 namespace small {
 
-constexpr int kCluster = 8;
+constexpr int kClusterPortable = 8;  // the portable cluster size
+constexpr int kClusterLarge = 16;    // non-portable (opt-in) cluster size
 constexpr int kThreads = 512;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -46,7 +47,8 @@ __device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v)
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
 }
 
-// Rows per lane in a half-step (registers hold R points of DP floats).
+// Rows per lane in a half-step when a CTA owns more than 32 rows (registers hold R points
+// of DP floats); with at most 32 rows one row per lane keeps every lane busy.
 template <int DP>
 constexpr int rows_per_lane() {
   return DP <= 16 ? 2 : 1;
@@ -59,13 +61,13 @@ constexpr int rows_per_lane() {
 // point and bias are one broadcast shared-memory read per warp; each warp keeps an online
 // (max, sum) per row over its slice in chunks of 8 columns, and the kWarps partials of a row
 // are merged through shared memory before the row's value is broadcast to the cluster.
-template <int DP>
+template <int DP, int R>
 __device__ __forceinline__ void half_step(const float* __restrict__ P, const float* __restrict__ Q,
                                           int nq, const float* __restrict__ cq,
                                           const float* __restrict__ nrmp, int r0, int r1,
                                           float kappa, float eps, float* out, float2* red) {
-  constexpr int R = rows_per_lane<DP>();
   constexpr int kWarps = kThreads / 32;
+  const uint32_t ncta = gridDim.x;  // the grid is one cluster
   constexpr int Q4 = DP / 4;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cs = (nq + kWarps - 1) / kWarps;
@@ -142,15 +144,16 @@ __device__ __forceinline__ void half_step(const float* __restrict__ P, const flo
         }
         const float L = Mx + log2f(Sm);
         const float v = nrmp[i] - eps * kLn2 * L;
-        for (uint32_t rk = 0; rk < (uint32_t)kCluster; ++rk) st_cluster(out + i, rk, v);
+        for (uint32_t rk = 0; rk < ncta; ++rk) st_cluster(out + i, rk, v);
       }
     }
     __syncthreads();
   }
 }
 
+// Launched as a single cluster of gridDim.x CTAs (the cluster size is set at launch).
 template <int DP>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
                    const float* __restrict__ a, const float* __restrict__ b, int n, int m, int d,
                    EpsSchedule sched, int iters, int warm, float* __restrict__ f_out,
@@ -200,8 +203,12 @@ small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
   __syncthreads();
   cluster_sync();  // every CTA's shared memory is initialised before any remote store
 
-  const int fr0 = (int)(((int64_t)n * rank) / kCluster), fr1 = (int)(((int64_t)n * (rank + 1)) / kCluster);
-  const int gr0 = (int)(((int64_t)m * rank) / kCluster), gr1 = (int)(((int64_t)m * (rank + 1)) / kCluster);
+  const int ncta = (int)gridDim.x;
+  const int fr0 = (int)(((int64_t)n * rank) / ncta), fr1 = (int)(((int64_t)n * (rank + 1)) / ncta);
+  const int gr0 = (int)(((int64_t)m * rank) / ncta), gr1 = (int)(((int64_t)m * (rank + 1)) / ncta);
+  constexpr int R2 = rows_per_lane<DP>();
+  // every CTA has the same row counts to within one: the choice is uniform over the cluster
+  const bool f_one = fr1 - fr0 <= 32, g_one = gr1 - gr0 <= 32;
   for (int s = 0; s < sched.n_stages; ++s) {
     const float eps = sched.eps[s];
     const float kappa = 2.0f * kLog2e / eps;
@@ -210,12 +217,14 @@ small_solve_kernel(const float* __restrict__ X, const float* __restrict__ Y,
       // f-update: bias of the columns (Y side) from g
       for (int j = tid; j < m; j += kThreads) cb[j] = (ga[j] - be[j]) * inv + lb[j];
       __syncthreads();
-      half_step<DP>(Xs, Ys, m, cb, al, fr0, fr1, kappa, eps, fa, red);
+      if (f_one) half_step<DP, 1>(Xs, Ys, m, cb, al, fr0, fr1, kappa, eps, fa, red);
+      else half_step<DP, R2>(Xs, Ys, m, cb, al, fr0, fr1, kappa, eps, fa, red);
       cluster_sync();
       // g-update: bias of the columns (X side) from f
       for (int i = tid; i < n; i += kThreads) cb[i] = (fa[i] - al[i]) * inv + la[i];
       __syncthreads();
-      half_step<DP>(Ys, Xs, n, cb, be, gr0, gr1, kappa, eps, ga, red);
+      if (g_one) half_step<DP, 1>(Ys, Xs, n, cb, be, gr0, gr1, kappa, eps, ga, red);
+      else half_step<DP, R2>(Ys, Xs, n, cb, be, gr0, gr1, kappa, eps, ga, red);
       cluster_sync();
     }
   }
@@ -248,6 +257,38 @@ size_t smem_bytes(int64_t n, int64_t m, int dp) {
   return (size_t)floats * sizeof(float) + (size_t)(kThreads / 32) * 64 * sizeof(float2);
 }
 
+// Cluster size for a problem: 16 CTAs (non-portable) when the clouds are large enough to
+// use them and the GPU can co-schedule a 16-CTA cluster of this kernel, else 8.
+template <int DP>
+int cluster_size(int n, int m, size_t bytes) {
+  if ((n > m ? n : m) <= 256) return kClusterPortable;
+  static int can16 = -1;  // per DP instantiation, decided once per process
+  if (can16 < 0) {
+    can16 = 0;
+    if (cudaFuncSetAttribute(small_solve_kernel<DP>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kClusterLarge);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = bytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kClusterLarge;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, small_solve_kernel<DP>, &cfg) ==
+              cudaSuccess &&
+          clusters >= 1)
+        can16 = 1;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+  }
+  return can16 ? kClusterLarge : kClusterPortable;
+}
+
 template <int DP>
 int launch(const float* X, const float* Y, const float* a, const float* b, int n, int m, int d,
            const EpsSchedule& sched, int iters, int warm, float* f, float* g, double* loss,
@@ -256,11 +297,25 @@ int launch(const float* X, const float* Y, const float* a, const float* b, int n
   cudaError_t e = cudaFuncSetAttribute(small_solve_kernel<DP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return FLASHOT_ERR_CUDA;
+  const int ncta = cluster_size<DP>(n, m, bytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ncta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   {
     TraceScope ts_(FLASHOT_KERNEL_LSE, st);
-    small_solve_kernel<DP><<<kCluster, kThreads, bytes, st>>>(X, Y, a, b, n, m, d, sched, iters,
-                                                              warm, f, g, loss);
+    e = cudaLaunchKernelEx(&cfg, small_solve_kernel<DP>, X, Y, a, b, n, m, d, sched, iters, warm,
+                           f, g, loss);
   }
+  if (e != cudaSuccess) return FLASHOT_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
 

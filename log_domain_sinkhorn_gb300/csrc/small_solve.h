@@ -21,8 +21,8 @@ struct EpsSchedule {
 // latency, not arithmetic, bounds the streaming path (n * m <= 2^20).
 bool small_solve_eligible(int64_t n, int64_t m, int64_t dp, int n_stages);
 
-// Runs all stages and iterations of the alternating solve in one launch of one 8-CTA
-// cluster; writes f, g and (if loss != NULL) the dual loss. a / b NULL = uniform.
+// Runs all stages and iterations of the alternating solve in one launch of one cluster
+// (16 CTAs where possible, else 8); writes f, g and (if loss != NULL) the dual loss. a / b NULL = uniform.
 int small_solve(const float* X, const float* Y, const float* a, const float* b, int64_t n,
                 int64_t m, int64_t d, int64_t dp, const float* eps_sched, int n_stages,
                 int iters, bool warm, float* f, float* g, double* loss, cudaStream_t st);
