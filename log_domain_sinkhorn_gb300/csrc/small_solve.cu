@@ -265,7 +265,11 @@ int cluster_size(int n, int m, size_t bytes) {
   static int can16 = -1;  // per DP instantiation, decided once per process
   if (can16 < 0) {
     can16 = 0;
+    // the query needs the kernel's dynamic shared-memory limit raised to `bytes` first
     if (cudaFuncSetAttribute(small_solve_kernel<DP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(small_solve_kernel<DP>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClusterLarge);
@@ -322,6 +326,10 @@ int launch(const float* X, const float* Y, const float* a, const float* b, int n
 }  // namespace small
 
 bool small_solve_eligible(int64_t n, int64_t m, int64_t dp, int n_stages) {
+  // Up to n m = 2^20 the single launch is ahead of the streaming path, which is bound by
+  // launch latency here (about 21 us per iteration up to 2048^2 at d = 3; the 16-CTA
+  // cluster takes 11 us at 1024^2). Just above, a CTA of the 16-CTA cluster owns more than
+  // 64 rows and needs a second pass over its row group (1040^2: 23 us per iteration).
   return n_stages <= kSmallMaxStages && dp <= 32 && dp % 4 == 0 && n * m <= (int64_t(1) << 20) &&
          small::smem_bytes(n, m, (int)dp) <= (size_t)200 * 1024;
 }
