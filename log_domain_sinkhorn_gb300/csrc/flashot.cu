@@ -152,8 +152,8 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
 }
 
 struct Layout {
-  size_t status, xp, yp, xq, yq, vtq, wsp, alpha, beta, wa, wb, la2, lb2, biasF, biasG, ftilde,
-      lse2, partial, loss, total;
+  size_t status, xp, yp, xq, yq, vtq, wsp, tsp, alpha, beta, wa, wb, la2, lb2, biasF, biasG,
+      ftilde, lse2, partial, loss, total;
 };
 
 Layout make_layout(const Geometry& g) {
@@ -194,6 +194,9 @@ Layout make_layout(const Geometry& g) {
   // Partial sums of the bf16 weighted-sum pass (stream-K over 128 x 256 tiles).
   if (g.prec == FLASHOT_PREC_BF16)
     L.wsp = take(tc_wsum2_scratch_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)));
+  // Partial sums of the tf32 weighted-sum passes' column splits.
+  if (g.prec == FLASHOT_PREC_TF32 || g.prec == FLASHOT_PREC_TF32X3)
+    L.tsp = take(tc_wsum_split_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)));
   L.total = off + 256;
   return L;
 }
@@ -434,7 +437,8 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
                         c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows, n_cols,
                         x_rows ? g.n_pad : g.m_pad, cols_pad, g.d, g.dpt, kappa, V, ldv, k,
                         c.at<void>(c.L.vtq), rowW, X, out, ldo, c.sms,
-                        c.at<unsigned>(c.L.status), c.st);
+                        c.at<unsigned>(c.L.status), c.st, c.at<void>(c.L.tsp),
+                        tc_wsum_split_bytes(std::max(g.n_pad, g.m_pad), std::max(g.k, g.d)));
   }
   const float* rowP = c.at<float>(x_rows ? c.L.xp : c.L.yp);
   const float* colP = c.at<float>(x_rows ? c.L.yp : c.L.xp);

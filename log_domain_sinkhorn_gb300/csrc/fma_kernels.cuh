@@ -188,7 +188,8 @@ lse_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ c
 // accumulated over 32-wide k-chunks staged in shared memory.
 // colP has n_col_tiles*32 rows.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kFmaThreads)
+// static: this header is included by more than one translation unit
+static __global__ void __launch_bounds__(kFmaThreads)
 lse_fma_generic_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                        const float* __restrict__ colBias, int64_t n_rows, int64_t d_pad,
                        int n_col_tiles, int tiles_per_split, float kappa,

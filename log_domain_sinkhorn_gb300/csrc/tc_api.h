@@ -32,12 +32,19 @@ int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colB
 // fma_kernels.cuh (apply / grad / Hadamard). V (n_cols x k, fp32, row stride ldv) is the
 // right operand of the second contraction (the column points themselves for the
 // gradient); it is transposed and packed into vtq first. X is the row points (fp32) for
-// the gradient's epilogue.
+// the gradient's epilogue. When one CTA per (row tile, output group) would leave a wave
+// mostly empty, the column tiles are split over up to 8 CTAs whose raw sums go to split_buf
+// and are added in a fixed order by a second kernel.
 int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const float* colBias,
                  const float* rowBias, int64_t n_rows, int64_t n_cols, int64_t rows_pad,
                  int64_t cols_pad, int64_t d, int64_t dpt, float kappa, const float* V,
                  int64_t ldv, int64_t k, void* vtq, const float* rowW, const float* X,
-                 float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st);
+                 float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st,
+                 void* split_buf, size_t split_bytes);
+// Partial-sum buffer of tc_wsum_pass's column splits (tf32): enough for up to 8 splits of
+// rows_pad rows with max(k, d) output columns, capped at 64 MB; fewer splits run when the
+// buffer holds fewer.
+size_t tc_wsum_split_bytes(int64_t rows_pad, int64_t k_or_d);
 
 // bf16 weighted-sum pass on 128 x 256 tiles with stream-K partials (tc_wsum2.cu). scratch
 // holds tc_wsum2_scratch_bytes(rows_pad, max(k, d)) bytes for the partial sums.

@@ -28,6 +28,7 @@
 
 #include "flashot.h"
 #include "common.cuh"
+#include "fma_kernels.cuh"  // wsum_split_reduce_kernel
 #include "pack_kernels.cuh"
 #include "ptx.cuh"
 #include "tc_api.h"
@@ -464,7 +465,8 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
                const float* __restrict__ rowBias, int64_t n_rows, int NT, int kc_count, int n_st,
                int n_w, int n_v, float kappa, const float* __restrict__ rowW,
                const float* __restrict__ Xrow, int64_t d, int64_t k, float* __restrict__ out,
-               int64_t ldo, unsigned* __restrict__ status) {
+               int64_t ldo, unsigned* __restrict__ status, int tps, float* __restrict__ part,
+               int64_t rows_pad, int kp) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ WCtrl ctl;
   constexpr bool kHad = (kKV == 0);
@@ -485,6 +487,10 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
   const uint32_t v_base = w_base + (uint32_t)n_w * kWBytes;
   const int64_t rt = blockIdx.x;
   const int64_t o0 = (int64_t)blockIdx.y * kKV;
+  // Column split blockIdx.z: global column tiles [j_begin, j_begin + NTl); the loops below
+  // count local tiles (buffer parities), the loads and biases use global ones.
+  const int j_begin = (int)blockIdx.z * tps;
+  const int NTl = min(NT, j_begin + tps) - j_begin;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < n_st; ++s) {
@@ -524,13 +530,14 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       uint32_t stage = 0, ph = 0;
       int64_t issued = 0, v_issued = 0;
       bool ok = true;
-      for (int jt = 0; ok && jt < NT; ++jt) {
+      for (int jt = 0; ok && jt < NTl; ++jt) {
         for (int kc = 0; kc < kc_count; ++kc) {
           if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
           uint8_t* st = smem + st_base + (size_t)stage * 2 * kChunk;
           ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2 * kChunk);
           ptx::tma_load_2d(&mapA, &ctl.full[stage], st, kc * kElems, (int)(rt * kBM));
-          ptx::tma_load_2d(&mapB, &ctl.full[stage], st + kChunk, kc * kElems, jt * kBN);
+          ptx::tma_load_2d(&mapB, &ctl.full[stage], st + kChunk, kc * kElems,
+                           (j_begin + jt) * kBN);
           ++issued;
           if (++stage == (uint32_t)n_st) { stage = 0; ph ^= 1u; }
         }
@@ -543,7 +550,7 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
           for (int vc = 0; vc < kWChunks; ++vc)
             for (int ob = 0; ob < kKV / kVBoxRows; ++ob)
               ptx::tma_load_2d(&mapV, &ctl.v_full[vs], vt + (size_t)vc * kVChunkBytes + ob * kVBoxRows * 128,
-                               jt * kBN + vc * kElems, (int)(o0 + ob * kVBoxRows));
+                               (j_begin + jt) * kBN + vc * kElems, (int)(o0 + ob * kVBoxRows));
           ++v_issued;
         }
       }
@@ -564,8 +571,8 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
       constexpr uint32_t idesc_o = ptx::make_idesc<kBF16>(kBM, kKV > 0 ? kKV : 128);
       uint32_t stage = 0, ph = 0;
       bool ok = true;
-      for (int t = 0; ok && t <= NT; ++t) {
-        if (t < NT) {
+      for (int t = 0; ok && t <= NTl; ++t) {
+        if (t < NTl) {
           const uint32_t ab = (uint32_t)(t & 1);
           if (!ptx::mbar_wait(&ctl.acc_empty[ab], (uint32_t)((t >> 1) & 1) ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
@@ -621,12 +628,13 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
     const float rb = row < n_rows ? rowBias[row] : neg_inf();
     float sumw = 0.0f, had = 0.0f;
     bool ok = true;
-    float4 bnext = __ldg(reinterpret_cast<const float4*>(colBias) + lane);
-    for (int jt = 0; jt < NT; ++jt) {
+    float4 bnext = __ldg(reinterpret_cast<const float4*>(colBias + (int64_t)j_begin * kBN) + lane);
+    for (int jt = 0; jt < NTl; ++jt) {
       const int bb = jt & 1;
       reinterpret_cast<float4*>(ctl.bias[ew][bb])[lane] = bnext;
-      if (jt + 1 < NT)
-        bnext = __ldg(reinterpret_cast<const float4*>(colBias + (int64_t)(jt + 1) * kBN) + lane);
+      if (jt + 1 < NTl)
+        bnext = __ldg(reinterpret_cast<const float4*>(colBias + (int64_t)(j_begin + jt + 1) * kBN) +
+                      lane);
       __syncwarp();
       const uint32_t ab = (uint32_t)(jt & 1);
       if (!ptx::mbar_wait(&ctl.acc_full[ab], (uint32_t)((jt >> 1) & 1))) { ok = false; break; }
@@ -689,8 +697,14 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         ptx::mbar_arrive(&ctl.w_full[wb]);
       }
     }
+    // With column splits (part != NULL) the raw sums go to part[(split rows_pad + row) kp + o]
+    // (sum w or the Hadamard sum in column kp - 1) for wsum_split_reduce_kernel.
+    float* pr = part != nullptr ? part + ((int64_t)blockIdx.z * rows_pad + row) * kp : nullptr;
     if constexpr (kHad) {
-      if (ok && row < n_rows) out[row] = had;
+      if (ok && row < n_rows) {
+        if (pr != nullptr) pr[kp - 1] = had;
+        else out[row] = had;
+      }
     } else {
       if (ok && !ptx::mbar_wait(&ctl.o_full, 0)) ok = false;
       if (ok) {
@@ -701,7 +715,14 @@ wsum_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__
         for (int c = 0; c < kKV / 32; ++c) {
           float o[32];
           ptx::tmem_ld_x32_sync(tmem + lane_base + 256 + c * 32, o);
-          if (row < n_rows) {
+          if (row < n_rows && pr != nullptr) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int64_t oo = o0 + c * 32 + t;
+              if (oo < kp - 1) pr[oo] = o[t];
+            }
+            if (c == 0 && blockIdx.y == 0) pr[kp - 1] = sumw;
+          } else if (row < n_rows) {
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
               const int64_t oo = o0 + c * 32 + t;
@@ -860,7 +881,8 @@ static int launch_wsum(const CUtensorMap& mA, const CUtensorMap& mB, const CUten
                        const float* colBias, const float* rowBias, int64_t n_rows,
                        int64_t row_tiles, int groups, int NT, int kc, float kappa,
                        const float* rowW, const float* X, int64_t d, int64_t k, float* out,
-                       int64_t ldo, unsigned* status, cudaStream_t st) {
+                       int64_t ldo, unsigned* status, cudaStream_t st, int splits, int tps,
+                       float* part, int64_t rows_pad, int kp) {
   constexpr int es = kBF16 ? 2 : 4;
   const int w_bytes = (kKV == 0) ? 0 : kBN * es * 128;             // 128 rows x 128 columns
   const int v_bytes = (kKV == 0) ? 0 : kKV * 128 * (kBN * es / 128);
@@ -876,38 +898,81 @@ static int launch_wsum(const CUtensorMap& mA, const CUtensorMap& mB, const CUten
   auto kern = wsum_tc_kernel<kBF16, kMode, kKV>;
   int rc = set_smem(kern, dyn);
   if (rc != FLASHOT_OK) return rc;
-  dim3 grid((unsigned)row_tiles, (unsigned)groups);
+  dim3 grid((unsigned)row_tiles, (unsigned)groups, (unsigned)splits);
   {
     TraceScope ts_(FLASHOT_KERNEL_WSUM, st);
     kern<<<grid, kThreads, dyn, st>>>(mA, mB, mV, colBias, rowBias, n_rows, NT, kc, n_st,
                                       std::max(n_w, 1), std::max(n_v, 1), kappa, rowW, X, d, k,
-                                      out, ldo, status);
+                                      out, ldo, status, tps, splits > 1 ? part : nullptr,
+                                      rows_pad, kp);
+  }
+  if (cudaGetLastError() != cudaSuccess) return FLASHOT_ERR_CUDA;
+  if (splits > 1) {
+    // the splits' raw sums, added in a fixed order, and the mode's epilogue
+    const int64_t total = n_rows * (kMode == kWsumHadamard ? 1 : (kMode == kWsumGrad ? d : k));
+    TraceScope ts2_(FLASHOT_KERNEL_OTHER, st);
+    wsum_split_reduce_kernel<kMode><<<(unsigned)std::min<int64_t>((total + 255) / 256, 1 << 20),
+                                      256, 0, st>>>(part, splits, rows_pad, kp, n_rows,
+                                                    kMode == kWsumGrad ? d : k, rowW, X, d, out,
+                                                    ldo);
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+// Column splits for the tf32 weighted sums: the split count s (at most 8, and as many as the
+// partial buffer holds) that minimises the makespan ceil(CTAs s / SMs) / s, in units of one
+// CTA covering a whole row of column tiles; 1 when one wave already fits.
+static int choose_splits(int64_t ctas, int NT, int sms, int64_t cap) {
+  int best = 1;
+  double best_mk = (double)((ctas + sms - 1) / sms);
+  for (int sp = 2; sp <= 8 && sp <= NT && sp <= cap; ++sp) {
+    const double mk = (double)((ctas * sp + sms - 1) / sms) / sp;
+    if (mk < best_mk - 1e-9) {
+      best_mk = mk;
+      best = sp;
+    }
+  }
+  return best;
+}
+
+size_t tc_wsum_split_bytes(int64_t rows_pad, int64_t k_or_d) {
+  // kp = output columns (whole 64- or 128-column groups) + 1, at most 8 splits, capped at
+  // 64 MB (wide outputs have enough CTAs in their column groups anyway)
+  const int64_t kv = k_or_d <= 64 ? 64 : 128;
+  const int64_t kp = (k_or_d + kv - 1) / kv * kv + 1;
+  return (size_t)std::min<int64_t>(8 * rows_pad * kp * (int64_t)sizeof(float), 64ll << 20);
 }
 
 int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const float* colBias,
                  const float* rowBias, int64_t n_rows, int64_t n_cols, int64_t rows_pad,
                  int64_t cols_pad, int64_t d, int64_t dpt, float kappa, const float* V,
                  int64_t ldv, int64_t k, void* vtq, const float* rowW, const float* X,
-                 float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st) {
-  (void)sms;
+                 float* out, int64_t ldo, int sms, unsigned* status, cudaStream_t st,
+                 void* split_buf, size_t split_bytes) {
   const int es = bf16 ? 2 : 4;
   const int kc = (int)(dpt * es / 128);
   const int64_t row_tiles = rows_pad / kBM;
   const int NT = (int)(cols_pad / kBN);
+  float* part = static_cast<float*>(split_buf);
   CUtensorMap mA, mB, mV;
   int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
   if (rc == FLASHOT_OK) rc = make_map(&mB, colQ, cols_pad, dpt, bf16);
   if (rc != FLASHOT_OK) return rc;
   if (mode == kWsumHadamard) {
     mV = mB;  // unused
+    const int kp = 2;
+    const int64_t cap = part ? (int64_t)(split_bytes / ((size_t)rows_pad * kp * sizeof(float))) : 1;
+    int splits = choose_splits(row_tiles, NT, sms, cap);
+    const int tps = (NT + splits - 1) / splits;
+    splits = (NT + tps - 1) / tps;
     return bf16 ? launch_wsum<true, kWsumHadamard, 0>(mA, mB, mV, colBias, rowBias, n_rows,
                                                       row_tiles, 1, NT, kc, kappa, rowW, X, d, 1,
-                                                      out, ldo, status, st)
+                                                      out, ldo, status, st, splits, tps, part,
+                                                      rows_pad, kp)
                 : launch_wsum<false, kWsumHadamard, 0>(mA, mB, mV, colBias, rowBias, n_rows,
                                                        row_tiles, 1, NT, kc, kappa, rowW, X, d,
-                                                       1, out, ldo, status, st);
+                                                       1, out, ldo, status, st, splits, tps, part,
+                                                       rows_pad, kp);
   }
   // Output-column group width: 64, 128, or 256 (bf16 only; tf32 W/V tiles are twice as big).
   const int kv = (k <= 64) ? 64 : (k <= 128 || !bf16) ? 128 : 256;
@@ -927,9 +992,14 @@ int tc_wsum_pass(bool bf16, int mode, const void* rowQ, const void* colQ, const 
   if (cudaGetLastError() != cudaSuccess) return FLASHOT_ERR_CUDA;
   rc = make_map_rows(&mV, vtq, out_rows_pad, cols_pad, bf16, kv > 128 ? 128 : kv);
   if (rc != FLASHOT_OK) return rc;
+  const int kp = (int)out_rows_pad + 1;
+  const int64_t cap = part ? (int64_t)(split_bytes / ((size_t)rows_pad * kp * sizeof(float))) : 1;
+  int splits = choose_splits(row_tiles * groups, NT, sms, cap);
+  const int tps = (NT + splits - 1) / splits;
+  splits = (NT + tps - 1) / tps;
 #define FLASHOT_WSUM_TC(B, M, KV)                                                             \
   launch_wsum<B, M, KV>(mA, mB, mV, colBias, rowBias, n_rows, row_tiles, groups, NT, kc, kappa, \
-                        rowW, X, d, k, out, ldo, status, st)
+                        rowW, X, d, k, out, ldo, status, st, splits, tps, part, rows_pad, kp)
   if (mode == kWsumGrad) {
     if (bf16) {
       if (kv == 64) return FLASHOT_WSUM_TC(true, kWsumGrad, 64);
