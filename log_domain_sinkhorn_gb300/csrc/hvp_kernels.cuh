@@ -69,6 +69,21 @@ __global__ void hvp_div_kernel(const float* __restrict__ a, const float* __restr
   y[i] = bi > 0.0f ? a[i] / bi : 0.0f;
 }
 
+// Per-thread running sum in fp32 with Neumaier compensation (the pair s + c carries about
+// twice fp32's precision). The CG's single-block reductions accumulate their ~m / 1024 terms
+// per thread this way and combine only the 1024 partials in fp64: GB300's fp64 pipe is a
+// small fraction of its fp32 one, and fp64 per element made these one-SM kernels the
+// largest cost of a CG step after the streaming passes.
+struct Sum32 {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = s + x;
+    c += (fabsf(s) >= fabsf(x)) ? (s - t) + x : (x - t) + s;
+    s = t;
+  }
+  __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+};
+
 // Block-wide fp64 sum (blockDim.x == 1024); every thread receives the result.
 __device__ __forceinline__ double block_sum(double v, double* red) {
 #pragma unroll
@@ -101,7 +116,8 @@ hvp_cg_init_kernel(const float* __restrict__ Y, const float* __restrict__ OB,
                    float* __restrict__ z, float* __restrict__ res, float* __restrict__ yv,
                    float* __restrict__ p, double* __restrict__ sc) {
   __shared__ double red[33];
-  double sum = 0.0, cnt = 0.0;
+  Sum32 s_sum;
+  int n_mass = 0;
   for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
     const float* ob = OB + j * (d + 2);
     float rhs = 0.0f;
@@ -109,15 +125,15 @@ hvp_cg_init_kernel(const float* __restrict__ Y, const float* __restrict__ OB,
       float yptv = 0.0f;
       for (int64_t k = 0; k < d; ++k) yptv = fmaf(Y[j * d + k], ob[k], yptv);
       rhs = (2.0f / eps) * (ob[d] - yptv) - PtT[j];
-      sum += (double)rhs;
-      cnt += 1.0;
+      s_sum.add(rhs);
+      ++n_mass;
     }
     res[j] = rhs;
   }
-  sum = block_sum(sum, red);
-  cnt = block_sum(cnt, red);
+  const double sum = block_sum(s_sum.value(), red);
+  const double cnt = block_sum((double)n_mass, red);
   const float mean = cnt > 0.0 ? (float)(sum / cnt) : 0.0f;
-  double rho = 0.0, rr = 0.0;
+  Sum32 s_rho, s_rr;
   for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
     const float cj = OB[j * (d + 2) + d + 1];
     const float r = cj > 0.0f ? res[j] - mean : 0.0f;
@@ -126,11 +142,11 @@ hvp_cg_init_kernel(const float* __restrict__ Y, const float* __restrict__ OB,
     res[j] = r;
     yv[j] = y;
     p[j] = y;
-    rho += (double)r * (double)y;
-    rr += (double)r * (double)r;
+    s_rho.add(r * y);
+    s_rr.add(r * r);
   }
-  rho = block_sum(rho, red);
-  rr = block_sum(rr, red);
+  const double rho = block_sum(s_rho.value(), red);
+  const double rr = block_sum(s_rr.value(), red);
   if (threadIdx.x == 0) {
     sc[kHvpRho] = rho;
     sc[kHvpRR] = rr;
@@ -148,21 +164,23 @@ hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, 
                    int64_t d, float* __restrict__ z, float* __restrict__ res,
                    float* __restrict__ yv, float* __restrict__ p, double* __restrict__ sc) {
   __shared__ double red[33];
-  double sq = 0.0, spq = 0.0, sp = 0.0, cnt = 0.0;
+  Sum32 s_q, s_pq, s_p;
+  int n_mass = 0;
+#pragma unroll 4
   for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
-    const float cj = OB[j * (d + 2) + d + 1];
+    const float cj = OB[j * (d + 2) + d + 1], pj = p[j], tj = PtT[j];
     if (cj > 0.0f) {
-      const float q = cj * p[j] - PtT[j];
-      sq += (double)q;
-      spq += (double)p[j] * (double)q;
-      sp += (double)p[j];
-      cnt += 1.0;
+      const float q = cj * pj - tj;
+      s_q.add(q);
+      s_pq.add(pj * q);
+      s_p.add(pj);
+      ++n_mass;
     }
   }
-  sq = block_sum(sq, red);
-  spq = block_sum(spq, red);
-  sp = block_sum(sp, red);
-  cnt = block_sum(cnt, red);
+  const double sq = block_sum(s_q.value(), red);
+  const double spq = block_sum(s_pq.value(), red);
+  const double sp = block_sum(s_p.value(), red);
+  const double cnt = block_sum((double)n_mass, red);
   const double qbar = cnt > 0.0 ? sq / cnt : 0.0;
   const double pq = spq - qbar * sp;
   const double rho = sc[kHvpRho];
@@ -172,23 +190,25 @@ hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, 
   }
   const float alpha = (float)(rho / pq);
   const float qb = (float)qbar;
-  double rho_new = 0.0, rr = 0.0;
+  Sum32 s_rho, s_rr;
+#pragma unroll 4
   for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
-    const float cj = OB[j * (d + 2) + d + 1];
+    const float cj = OB[j * (d + 2) + d + 1], pj = p[j], tj = PtT[j], zj = z[j], rsj = res[j];
     if (cj > 0.0f) {
-      const float q = (cj * p[j] - PtT[j]) - qb;
-      z[j] = fmaf(alpha, p[j], z[j]);
-      const float rj = fmaf(-alpha, q, res[j]);
+      const float q = (cj * pj - tj) - qb;
+      z[j] = fmaf(alpha, pj, zj);
+      const float rj = fmaf(-alpha, q, rsj);
       res[j] = rj;
       const float y = rj / cj;
       yv[j] = y;
-      rho_new += (double)rj * (double)y;
-      rr += (double)rj * (double)rj;
+      s_rho.add(rj * y);
+      s_rr.add(rj * rj);
     }
   }
-  rho_new = block_sum(rho_new, red);
-  rr = block_sum(rr, red);
+  const double rho_new = block_sum(s_rho.value(), red);
+  const double rr = block_sum(s_rr.value(), red);
   const float beta = (float)(rho_new / rho);
+#pragma unroll 8
   for (int64_t j = threadIdx.x; j < m; j += blockDim.x) p[j] = fmaf(beta, p[j], yv[j]);
   if (threadIdx.x == 0) {
     sc[kHvpRho] = rho_new;
