@@ -673,15 +673,15 @@ def run_hvp(args):
     passes = 2 * cg_iters + 5  # CG: P p and P^T t; plus [PY|r], [P^T V|P^T s|c], T, rhs, final
     pass_avg = ms_ws / max(n_ws, 1) / 1e3
     # FMA-pipe lane operations per score of each streaming pass (d = 3, padded to 4): the
-    # dot product (4, the padding lane carrying the row bias r_i / kappa), kappa * dot + c_j
-    # (1), then the weighted sums: one output column for P t / P^T t (1 + 2 per CG
-    # iteration), 8 (the kernel's padded output width) for [PY | r], [P^T V | P^T s | c] and
-    # [P diag(z) Y | P z], and for the curvature pass T also the dot <u_i, y_j> (4) and its
-    # product with the weight (1). The ex2 (one per score) runs on the SFU at 32 per clock
-    # per SM, never the limit here.
+    # exponent (4: kappa rides on the row coordinates, the dot starts from c_j and the
+    # padding lane carries the row bias r_i), then the weighted sums: one output column for
+    # P t / P^T t (1 + 2 per CG iteration), 8 (the kernel's padded output width) for
+    # [PY | r], [P^T V | P^T s | c] and [P diag(z) Y | P z], and for the curvature pass T
+    # also the dot <u_i, y_j> (4) and its product with the weight (1). The ex2 (one per
+    # score) runs on the SFU at 32 per clock per SM, never the limit here.
     d_pad = 4
-    lane_ops = nm * ((d_pad + 2) * (1 + 2 * cg_iters) + (d_pad + 1 + 8) * 3
-                     + (d_pad + 1 + 8 + d_pad + 1))
+    lane_ops = nm * ((d_pad + 1) * (1 + 2 * cg_iters) + (d_pad + 8) * 3
+                     + (d_pad + 8 + d_pad + 1))
     passes_s = ms_ws / args.steps / 1e3
     line = {"metric": "Hessian-vector products of the OT loss w.r.t. X", "supplementary": True,
             "value": 1e3 / ms, "unit": "HVPs/s", "ms_per_hvp": ms, "cg_iterations": cg_iters,

@@ -405,11 +405,15 @@ wsum_fma_small_kernel(const float* __restrict__ rowP, const float* __restrict__ 
 // held as pairs x2[p][k] = (x_{2p,k}, x_{2p+1,k}); the staged column coordinates, biases and
 // values of V are duplicated, (v, v), so every packed operand is one shared-memory load.
 // Same arguments, grid and outputs as wsum_fma_small_kernel.
-// kFoldRow (d < DP, Apply and HessT only): the row bias rides in the first padding lane,
-// x_{i,d} = r_i / kappa against y_{j,d} = 1 in the staged column tile, so the dot product
-// already carries it and the epilogue saves the add (kappa dot + c_j, with no + r_i).
+// kFoldRow (d < DP, Apply and HessT only): the whole exponent comes out of the dot product.
+// kappa is applied to the row coordinates once at load, the row bias rides in the first
+// padding lane (x_{i,d} = r_i against y_{j,d} = 1 in the staged column tile) and the dot
+// starts from c_j, so s_ij = c_j + sum_k (kappa x_ik) y_jk + r_i with no epilogue
+// arithmetic: d_pad + 1 FMA-pipe operations per score instead of d_pad + 2.
+// Column tiles are double-buffered: the next tile's loads are issued before the current
+// tile's scores and stored to the other buffer after them, one barrier per tile.
 template <int DP, int MODE, int KO, int R, bool kFoldRow = false>
-__global__ void __launch_bounds__(kFmaThreads)
+__global__ void __launch_bounds__(kFmaThreads, DP <= 4 ? 8 : 1)  // 8 CTAs per SM at d_pad 4
 wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ colP,
                      const float* __restrict__ colBias, const float* __restrict__ rowBias,
                      int64_t n_rows, int64_t n_cols, int n_col_tiles, float kappa,
@@ -425,12 +429,16 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
   constexpr bool kHad = (MODE == kWsumHadamard);
   constexpr int KV = kHad ? 1 : KO;
   static_assert(!(kFoldRow && kHad), "the Hadamard sum needs the plain dot product");
-  __shared__ __align__(16) float2 ys2[32 * DP];
-  __shared__ __align__(16) float2 cs2[32];
-  __shared__ __align__(16) float2 vs2[32][KV];
+  static_assert((32 * DP) % kFmaThreads == 0, "whole column tiles per thread");
+  constexpr int kYPer = 32 * DP / kFmaThreads;               // staged coordinates per thread
+  constexpr int kVPer = (32 * KV + kFmaThreads - 1) / kFmaThreads;  // staged V entries
+  __shared__ __align__(16) float2 ys2[2][32 * DP];
+  __shared__ __align__(16) float2 cs2[2][32];
+  __shared__ __align__(16) float2 vs2[2][32][KV];
   const int tid = threadIdx.x;
   const int64_t row0 = (int64_t)blockIdx.x * kFmaThreads * R + tid;
   const int64_t o0 = (int64_t)blockIdx.y * KO;
+  const uint64_t k2 = ptx::pack2(kappa, kappa);
   uint64_t x2[P][DP], u2[P][kHess ? DP : 1], rb2[P];
 #pragma unroll
   for (int p = 0; p < P; ++p) {
@@ -463,10 +471,9 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
     const float rbb = rb < n_rows ? rowBias[rb] : neg_inf();
     rb2[p] = ptx::pack2(rba, rbb);
     if constexpr (kFoldRow) {
-      const uint64_t f2 = ptx::pack2(rba / kappa, rbb / kappa);
+      const uint64_t f2 = ptx::pack2(rba, rbb);
 #pragma unroll
-      for (int kk = 0; kk < DP; ++kk)
-        if (kk == d) x2[p][kk] = f2;
+      for (int kk = 0; kk < DP; ++kk) x2[p][kk] = (kk == d) ? f2 : ptx::mul2(k2, x2[p][kk]);
     }
   }
   uint64_t acc2[P][KV], sw2[P], hd2[P];
@@ -477,48 +484,69 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
 #pragma unroll
     for (int o = 0; o < KV; ++o) acc2[p][o] = 0ull;
   }
-  const uint64_t k2 = ptx::pack2(kappa, kappa);
   int t_begin = 0, t_end = n_col_tiles;
   if (part != nullptr) {
     t_begin = (int)blockIdx.z * tiles_per_split;
     t_end = min(n_col_tiles, t_begin + tiles_per_split);
   }
-  for (int t = t_begin; t < t_end; ++t) {
-    __syncthreads();
+  // staging of column tile t: global loads into registers (fetch), then duplicated into
+  // buffer b of shared memory (put)
+  float ypre[kYPer], cpre = 0.0f, vpre[kVPer];
+  auto fetch = [&](int t) {
     const float* src = colP + (int64_t)t * 32 * DP;
-    for (int e = tid; e < 32 * DP; e += kFmaThreads) {
-      const float v = (kFoldRow && e % DP == d) ? 1.0f : src[e];
-      ys2[e] = make_float2(v, v);
+#pragma unroll
+    for (int i = 0; i < kYPer; ++i) {
+      const int e = tid + i * kFmaThreads;
+      ypre[i] = (kFoldRow && e % DP == d) ? 1.0f : src[e];
     }
-    if (tid < 32) {
-      const float cb = colBias[(int64_t)t * 32 + tid];
-      cs2[tid] = make_float2(cb, cb);
-    }
+    if (tid < 32) cpre = colBias[(int64_t)t * 32 + tid];
     if constexpr (!kHad) {
-      for (int e = tid; e < 32 * KO; e += kFmaThreads) {
+#pragma unroll
+      for (int i = 0; i < kVPer; ++i) {
+        const int e = tid + i * kFmaThreads;
         const int c = e / KO, o = e % KO;
         const int64_t j = (int64_t)t * 32 + c, oo = o0 + o;
-        const float v = (j < n_cols && oo < k) ? V[j * ldv + oo] : 0.0f;
-        vs2[c][o] = make_float2(v, v);
+        vpre[i] = (e < 32 * KO && j < n_cols && oo < k) ? V[j * ldv + oo] : 0.0f;
       }
     }
-    __syncthreads();
-    const uint64_t* ysp = reinterpret_cast<const uint64_t*>(ys2);
-    const uint64_t* csp = reinterpret_cast<const uint64_t*>(cs2);
+  };
+  auto put = [&](int b) {
+#pragma unroll
+    for (int i = 0; i < kYPer; ++i) ys2[b][tid + i * kFmaThreads] = make_float2(ypre[i], ypre[i]);
+    if (tid < 32) cs2[b][tid] = make_float2(cpre, cpre);
+    if constexpr (!kHad) {
+#pragma unroll
+      for (int i = 0; i < kVPer; ++i) {
+        const int e = tid + i * kFmaThreads;
+        if (e < 32 * KO) vs2[b][e / KO][e % KO] = make_float2(vpre[i], vpre[i]);
+      }
+    }
+  };
+  if (t_begin < t_end) {
+    fetch(t_begin);
+    put(0);
+  }
+  __syncthreads();
+  for (int t = t_begin; t < t_end; ++t) {
+    const int b = (t - t_begin) & 1;
+    const bool more = t + 1 < t_end;
+    if (more) fetch(t + 1);
+    const uint64_t* ysp = reinterpret_cast<const uint64_t*>(ys2[b]);
+    const uint64_t* csp = reinterpret_cast<const uint64_t*>(cs2[b]);
 #pragma unroll 2
     for (int c = 0; c < 32; ++c) {
       const uint64_t* y2 = ysp + c * DP;
       const uint64_t c2 = csp[c];
       uint64_t vv[KV];
       if constexpr (!kHad) {
-        const uint64_t* vp = reinterpret_cast<const uint64_t*>(vs2[c]);
+        const uint64_t* vp = reinterpret_cast<const uint64_t*>(vs2[b][c]);
 #pragma unroll
         for (int o = 0; o < KV; ++o) vv[o] = vp[o];
       }
       uint64_t dot[P], tu[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) {
-        dot[p] = 0ull;
+        dot[p] = kFoldRow ? c2 : 0ull;
         tu[p] = 0ull;
       }
 #pragma unroll
@@ -534,7 +562,7 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
       for (int p = 0; p < P; ++p) {
         float e0, e1;
         if constexpr (kFoldRow)
-          ptx::unpack2(ptx::fma2(k2, dot[p], c2), e0, e1);
+          ptx::unpack2(dot[p], e0, e1);
         else
           ptx::unpack2(ptx::add2(ptx::fma2(k2, dot[p], c2), rb2[p]), e0, e1);
         uint64_t w2 = ptx::pack2(ex2(e0), ex2(e1));
@@ -548,6 +576,9 @@ wsum_fma_pair_kernel(const float* __restrict__ rowP, const float* __restrict__ c
         }
       }
     }
+    // buffer b ^ 1 was last read in the previous tile, before the previous barrier
+    if (more) put(b ^ 1);
+    __syncthreads();
   }
 #pragma unroll
   for (int p = 0; p < P; ++p) {
