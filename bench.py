@@ -674,14 +674,14 @@ def run_hvp(args):
     pass_avg = ms_ws / max(n_ws, 1) / 1e3
     # FMA-pipe lane operations per score of each streaming pass (d = 3, padded to 4): the
     # exponent (4: kappa rides on the row coordinates, the dot starts from c_j and the
-    # padding lane carries the row bias r_i), then the weighted sums: one output column for
-    # P t / P^T t (1 + 2 per CG iteration), 8 (the kernel's padded output width) for
-    # [PY | r], [P^T V | P^T s | c] and [P diag(z) Y | P z], and for the curvature pass T
-    # also the dot <u_i, y_j> (4) and its product with the weight (1). The ex2 (one per
-    # score) runs on the SFU at 32 per clock per SM, never the limit here.
+    # padding lane carries the row bias r_i), then the weighted sums at the kernel's padded
+    # output width: 1 for P t / P^T t (1 + 2 per CG iteration), 4 for [PY | r] and
+    # [P diag(z) Y | P z], 8 for [P^T V | P^T s | c] (5 columns), and 4 for the curvature
+    # pass T plus its dot <u_i, y_j> (4) and the product with the weight (1). The ex2 (one
+    # per score) runs on the SFU at 32 per clock per SM, never the limit here.
     d_pad = 4
-    lane_ops = nm * ((d_pad + 1) * (1 + 2 * cg_iters) + (d_pad + 8) * 3
-                     + (d_pad + 8 + d_pad + 1))
+    lane_ops = nm * ((d_pad + 1) * (1 + 2 * cg_iters) + (d_pad + 4) * 2 + (d_pad + 8)
+                     + (d_pad + 4 + d_pad + 1))
     passes_s = ms_ws / args.steps / 1e3
     line = {"metric": "Hessian-vector products of the OT loss w.r.t. X", "supplementary": True,
             "value": 1e3 / ms, "unit": "HVPs/s", "ms_per_hvp": ms, "cg_iterations": cg_iters,

@@ -337,7 +337,10 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
     const int64_t rows_per_block = g.small ? (int64_t)kFmaThreads * R : kFmaThreads;
     const int64_t row_blocks = ceil_div(n_rows, rows_per_block);
     const int n_tiles = (int)(cols_pad / (g.small ? kFmaBN : 32));
-    const int64_t target = (int64_t)c.sms * 8;
+    // CTAs to aim for: 16 per SM for the small-d kernel (several waves, 4 CTAs fit per SM at
+    // d_pad = 16: the uneven finish of one wave's CTAs is evened out by the next; 20k x 80k,
+    // d = 16 measured 5% faster than at 8 per SM), 8 for the generic one.
+    const int64_t target = (int64_t)c.sms * (g.small ? 16 : 8);
     n_splits = (int)std::min<int64_t>({ceil_div(target, row_blocks), (int64_t)n_tiles,
                                         (int64_t)kMaxSplits});
     n_splits = std::max(n_splits, 1);
@@ -451,24 +454,28 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
   const int64_t kk = (mode == kWsumHadamard) ? 1 : k;
   // One output column (a transport-vector application): a narrow accumulator.
   const bool narrow = (mode == kWsumApply && k == 1);
-  // Up to 8 output columns (apply / curvature passes of small d): an 8-wide accumulator.
+  // Up to 4 or 8 output columns (apply / curvature passes of small d): a 4- or 8-wide
+  // accumulator.
   const bool mid = g.small && !narrow && k <= 8 && (mode == kWsumApply || mode == kWsumHessT);
-  const int KO = narrow ? 1 : (mid ? 8 : 32);
+  const bool quad = mid && k <= 4;
+  const int KO = narrow ? 1 : (quad ? 4 : (mid ? 8 : 32));
   // Rows per thread of the small-d kernel: 4 for the narrow pass (2 when d_pad > 16), 2 for
-  // the 8-wide one.
+  // the 4- and 8-wide ones.
   const int R = (g.small && narrow) ? (g.dpf <= 16 ? 4 : 2) : (mid ? 2 : 1);
   const int64_t row_blocks = ceil_div(n_rows, (int64_t)kFmaThreads * R);
   const int64_t k_groups = ceil_div(kk, KO);
   const int n_tiles = (int)(cols_pad / 32);
-  // Column splits for the small-d kernel when rows x output groups give fewer than 8 CTAs
-  // per SM; the partials ([split][row][kp] floats) live in the workspace's partial region.
+  // Column splits for the small-d kernel when rows x output groups give fewer than 16 CTAs
+  // per SM (two waves of the 8 that fit at d_pad = 4: CTAs finish unevenly, and a second
+  // wave evens the SMs' loads; measured 5% faster than one wave on 50k x 50k, d = 3); the
+  // partials ([split][row][kp] floats) live in the workspace's partial region.
   int n_splits = 1, tps = n_tiles, kp = 0;
   if (g.small) {
     kp = (int)(mode == kWsumHadamard ? 1 : k_groups * KO) + 1;
     const int64_t cap_floats = (int64_t)kMaxSplits * std::max(g.n_pad, g.m_pad) * 2;
     const int64_t rows_pad_ = x_rows ? g.n_pad : g.m_pad;
     const int64_t max_splits = std::min<int64_t>(cap_floats / (rows_pad_ * kp), n_tiles);
-    const int64_t want = ceil_div((int64_t)c.sms * 8, row_blocks * k_groups);
+    const int64_t want = ceil_div((int64_t)c.sms * 16, row_blocks * k_groups);
     n_splits = (int)std::max<int64_t>(1, std::min(want, max_splits));
     tps = (int)ceil_div(n_tiles, n_splits);
     n_splits = (int)ceil_div(n_tiles, tps);
@@ -496,6 +503,8 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
 #define FLASHOT_WSUM_MODES(DPV)                                                     \
   case DPV:                                                                         \
     if (narrow) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 1, ((DPV) <= 16 ? 4 : 2));       \
+    else if (quad && mode == kWsumApply) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 4, 2);  \
+    else if (quad) FLASHOT_WSUM_PAIR(DPV, kWsumHessT, 4, 2);                        \
     else if (mid && mode == kWsumApply) FLASHOT_WSUM_PAIR(DPV, kWsumApply, 8, 2);   \
     else if (mid) FLASHOT_WSUM_PAIR(DPV, kWsumHessT, 8, 2);                         \
     else if (mode == kWsumApply) FLASHOT_WSUM_SMALL(DPV, kWsumApply, 32, 1);        \
