@@ -545,10 +545,9 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
     if (rc != FLASHOT_OK) return rc;
     const int64_t total = n_rows * kk;
     TraceScope ts2_(FLASHOT_KERNEL_OTHER, c.st);
-#define FLASHOT_WSUM_REDUCE(MODEV)                                                          \
-  wsum_split_reduce_kernel<MODEV><<<grid1(total, 256), 256, 0, c.st>>>(part, n_splits, rows_pad, \
-                                                                    kp, n_rows, k, rowW, X,   \
-                                                                    g.d, out, ldo)
+#define FLASHOT_WSUM_REDUCE(MODEV)                                                       \
+  wsum_split_reduce_lanes_kernel<MODEV><<<grid1(total * kSplitLanes, 256), 256, 0, c.st>>>( \
+      part, n_splits, rows_pad, kp, n_rows, k, rowW, X, g.d, out, ldo)
     if (mode == kWsumApply) FLASHOT_WSUM_REDUCE(kWsumApply);
     else if (mode == kWsumGrad) FLASHOT_WSUM_REDUCE(kWsumGrad);
     else if (mode == kWsumHessT) FLASHOT_WSUM_REDUCE(kWsumHessT);
@@ -560,7 +559,7 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
 
 // ---- Hessian-vector product scratch (after the ordinary workspace) ----------------------
 struct HvpLayout {
-  size_t vp, VA, OA, VB, OB, T, wf, t1, PtT, z, res, yv, p, Pp, tn, VD, OD, sc, total;
+  size_t vp, VA, OA, VB, OB, T, wf, t1, PtT, z, res, yv, p, Pp, tn, VD, OD, sc, cgp, total;
 };
 
 HvpLayout make_hvp_layout(const Geometry& g, size_t base) {
@@ -590,6 +589,7 @@ HvpLayout make_hvp_layout(const Geometry& g, size_t base) {
   H.VD = take(m * (d + 1));
   H.OD = take(n * (d + 1));
   H.sc = take(2 * kHvpScalars);
+  H.cgp = take(2 * 6 * kCgMaxBlocks);  // doubles: 4 and 2 partials per CG block
   H.total = off + 256;
   return H;
 }
@@ -916,6 +916,10 @@ int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float
   float* VD = c.at<float>(H.VD);
   float* OD = c.at<float>(H.OD);
   double* sc = c.at<double>(H.sc);
+  double* cgp = c.at<double>(H.cgp);
+  double* cgp2 = cgp + 4 * kCgMaxBlocks;
+  const int cg_blocks = (int)std::min<int64_t>(std::max<int64_t>(ceil_div(m, kCgThreads), 1),
+                                               kCgMaxBlocks);
   const int T256 = 256;
   const int64_t nm = std::max(n, m);
   {
@@ -972,7 +976,16 @@ int flashot_ot_hvp_x(const float* X, const float* Y, const float* a, const float
       return rc;
     {
       TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
-      hvp_cg_step_kernel<<<1, 1024, 0, c.st>>>(OB, PtT, m, d, z, res, yv, pv, sc);
+      hvp_cg_q_kernel<<<cg_blocks, kCgThreads, 0, c.st>>>(OB, PtT, m, d, pv, cgp);
+    }
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      hvp_cg_update_kernel<<<cg_blocks, kCgThreads, 0, c.st>>>(OB, PtT, m, d, z, res, yv, pv,
+                                                                cgp, cgp2, sc);
+    }
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      hvp_cg_dir_kernel<<<cg_blocks, kCgThreads, 0, c.st>>>(m, pv, yv, cgp2, sc);
     }
     if ((rc = launch_check()) != FLASHOT_OK) return rc;
     if ((rc = read_scalars()) != FLASHOT_OK) return rc;

@@ -643,6 +643,53 @@ __global__ void wsum_split_reduce_kernel(const float* __restrict__ part, int n_s
   }
 }
 
+// The same sum with kSplitLanes consecutive threads per (row, output column): lane l adds
+// splits l, l + 8, ... and the lanes combine by a fixed xor tree, so each thread waits on
+// n_splits / 8 loads instead of n_splits (the CUDA-core passes split their columns up to
+// 64 ways). blockDim.x must be a multiple of 32; any grid size (grid-stride).
+constexpr int kSplitLanes = 8;
+template <int MODE>
+__global__ void wsum_split_reduce_lanes_kernel(const float* __restrict__ part, int n_splits,
+                                               int64_t rows_pad, int kp, int64_t n_rows,
+                                               int64_t k, const float* __restrict__ rowW,
+                                               const float* __restrict__ Xrow, int64_t d,
+                                               float* __restrict__ out, int64_t ldo) {
+  const int64_t kk = (MODE == kWsumHadamard) ? 1 : k;
+  const int64_t n_el = n_rows * kk;
+  const int l = threadIdx.x % kSplitLanes;
+  // the loop bound depends on the block only: every lane of a warp runs every shuffle
+  for (int64_t base = blockIdx.x * (int64_t)blockDim.x; base < n_el * kSplitLanes;
+       base += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = (base + threadIdx.x) / kSplitLanes;
+    const bool valid = e < n_el;
+    const int64_t row = valid ? e / kk : 0, o = valid ? e - row * kk : 0;
+    const int col = (MODE == kWsumHadamard) ? kp - 1 : (int)o;
+    float acc = 0.0f, sumw = 0.0f;
+    if (valid) {
+      for (int sp = l; sp < n_splits; sp += kSplitLanes) {
+        const float* pr = part + ((int64_t)sp * rows_pad + row) * kp;
+        acc += pr[col];
+        if constexpr (MODE == kWsumGrad) sumw += pr[kp - 1];
+      }
+    }
+#pragma unroll
+    for (int x = kSplitLanes / 2; x > 0; x >>= 1) {
+      acc += __shfl_xor_sync(0xffffffffu, acc, x);
+      if constexpr (MODE == kWsumGrad) sumw += __shfl_xor_sync(0xffffffffu, sumw, x);
+    }
+    if (!valid || l != 0) continue;
+    if constexpr (MODE == kWsumGrad) {
+      const float a = rowW[row];
+      const float inv = sumw > 0.0f ? 1.0f / sumw : 0.0f;
+      out[row * ldo + o] = a > 0.0f ? 2.0f * a * (Xrow[row * d + o] - acc * inv) : 0.0f;
+    } else if constexpr (MODE == kWsumHadamard) {
+      out[row] = acc;
+    } else {
+      out[row * ldo + o] = acc;
+    }
+  }
+}
+
 // Weighted sums, any d_pad (multiple of 32): dots for 32 columns accumulated over 32-wide
 // k-chunks, then the same epilogue as the small-d kernel.
 template <int MODE, int KO = 32>

@@ -13,7 +13,7 @@
 //             + 2 ((r_i x_i - (PY)_i) u_i + x_i (P z)_i - (P diag(z) Y)_i).
 // The streaming passes (P [Y | 1], P^T [V | s | 1], T, the CG's P p and P^T t, and
 // P [diag(z) Y | z]) run in the weighted-sum kernels; the kernels here assemble their
-// inputs and outputs. Every reduction is one block in a fixed order (deterministic).
+// inputs and outputs. Every reduction runs in a fixed order (deterministic).
 #pragma once
 
 #include "common.cuh"
@@ -21,7 +21,14 @@
 namespace flashot {
 
 // Scalars the CG keeps on the device (doubles).
-enum HvpScalar : int { kHvpRho = 0, kHvpRR = 1, kHvpRR0 = 2, kHvpBreak = 3, kHvpScalars = 8 };
+enum HvpScalar : int {
+  kHvpRho = 0, kHvpRR = 1, kHvpRR0 = 2, kHvpBreak = 3, kHvpRhoOld = 4, kHvpScalars = 8
+};
+// A CG step runs on up to kCgMaxBlocks CTAs of kCgThreads threads; each writes its block's
+// partial sums, and every CTA of the next kernel reduces all of them in the same order.
+constexpr int kCgMaxBlocks = 256;
+constexpr int kCgThreads = 256;
+static_assert(kCgMaxBlocks <= kCgThreads, "one block partial per thread of the reducing CTA");
 
 // VA (m x (d+1)) = [Y | 1];  VB (n x (d+2)) = [V | s | 1] with s_i = <x_i, v_i>.
 __global__ void hvp_prep_kernel(const float* __restrict__ X, const float* __restrict__ Y,
@@ -84,7 +91,8 @@ struct Sum32 {
   __device__ __forceinline__ double value() const { return (double)s + (double)c; }
 };
 
-// Block-wide fp64 sum (blockDim.x == 1024); every thread receives the result.
+// Block-wide fp64 sum (blockDim.x a multiple of 32, at most 1024); every thread receives
+// the result. The tree is fixed, so every block reducing the same values gets the same sum.
 __device__ __forceinline__ double block_sum(double v, double* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -92,7 +100,7 @@ __device__ __forceinline__ double block_sum(double v, double* red) {
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   if (threadIdx.x < 32) {
-    double s = red[threadIdx.x];
+    double s = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (threadIdx.x == 0) red[32] = s;
@@ -159,15 +167,19 @@ hvp_cg_init_kernel(const float* __restrict__ Y, const float* __restrict__ OB,
 //   q = c p - PtT (projected), alpha = rho / <p, q>, z += alpha p, res -= alpha q,
 //   yv = res / c, rho' = <res, yv>, p = yv + (rho'/rho) p.  <p, q> <= 0 (S is PSD, so only
 //   round-off gives it) stops the iteration (kHvpBreak = 1) without changing z.
-__global__ void __launch_bounds__(1024)
-hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, int64_t m,
-                   int64_t d, float* __restrict__ z, float* __restrict__ res,
-                   float* __restrict__ yv, float* __restrict__ p, double* __restrict__ sc) {
+// Three kernels over the same grid of G CTAs, each global sum taken between two of them:
+//   hvp_cg_q_kernel      partial sums of q, p q, p and the count of columns with mass;
+//   hvp_cg_update_kernel alpha from those; z, res, yv; partial sums of res yv and res^2;
+//   hvp_cg_dir_kernel    beta from those; p.
+// Per thread Sum32, fp64 across the block, fp64 across the G block partials.
+__global__ void __launch_bounds__(kCgThreads)
+hvp_cg_q_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, int64_t m,
+                int64_t d, const float* __restrict__ p, double* __restrict__ part) {
   __shared__ double red[33];
   Sum32 s_q, s_pq, s_p;
   int n_mass = 0;
-#pragma unroll 4
-  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
+  for (int64_t j = blockIdx.x * (int64_t)kCgThreads + threadIdx.x; j < m;
+       j += (int64_t)gridDim.x * kCgThreads) {
     const float cj = OB[j * (d + 2) + d + 1], pj = p[j], tj = PtT[j];
     if (cj > 0.0f) {
       const float q = cj * pj - tj;
@@ -181,23 +193,45 @@ hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, 
   const double spq = block_sum(s_pq.value(), red);
   const double sp = block_sum(s_p.value(), red);
   const double cnt = block_sum((double)n_mass, red);
+  if (threadIdx.x == 0) {
+    double* o = part + 4 * (int64_t)blockIdx.x;
+    o[0] = sq;
+    o[1] = spq;
+    o[2] = sp;
+    o[3] = cnt;
+  }
+}
+
+__global__ void __launch_bounds__(kCgThreads)
+hvp_cg_update_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, int64_t m,
+                     int64_t d, float* __restrict__ z, float* __restrict__ res,
+                     float* __restrict__ yv, const float* __restrict__ p,
+                     const double* __restrict__ part, double* __restrict__ part2,
+                     double* __restrict__ sc) {
+  __shared__ double red[33];
+  const int G = gridDim.x;  // <= kCgThreads: one partial per thread
+  const int t = threadIdx.x;
+  const double sq = block_sum(t < G ? part[4 * t + 0] : 0.0, red);
+  const double spq = block_sum(t < G ? part[4 * t + 1] : 0.0, red);
+  const double sp = block_sum(t < G ? part[4 * t + 2] : 0.0, red);
+  const double cnt = block_sum(t < G ? part[4 * t + 3] : 0.0, red);
   const double qbar = cnt > 0.0 ? sq / cnt : 0.0;
   const double pq = spq - qbar * sp;
   const double rho = sc[kHvpRho];
-  if (!(pq > 0.0) || !(rho > 0.0)) {
-    if (threadIdx.x == 0) sc[kHvpBreak] = 1.0;
+  if (!(pq > 0.0) || !(rho > 0.0)) {  // the same decision in every block
+    if (blockIdx.x == 0 && t == 0) sc[kHvpBreak] = 1.0;
     return;
   }
   const float alpha = (float)(rho / pq);
   const float qb = (float)qbar;
   Sum32 s_rho, s_rr;
-#pragma unroll 4
-  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) {
-    const float cj = OB[j * (d + 2) + d + 1], pj = p[j], tj = PtT[j], zj = z[j], rsj = res[j];
+  for (int64_t j = blockIdx.x * (int64_t)kCgThreads + t; j < m;
+       j += (int64_t)gridDim.x * kCgThreads) {
+    const float cj = OB[j * (d + 2) + d + 1], pj = p[j], tj = PtT[j];
     if (cj > 0.0f) {
       const float q = (cj * pj - tj) - qb;
-      z[j] = fmaf(alpha, pj, zj);
-      const float rj = fmaf(-alpha, q, rsj);
+      z[j] = fmaf(alpha, pj, z[j]);
+      const float rj = fmaf(-alpha, q, res[j]);
       res[j] = rj;
       const float y = rj / cj;
       yv[j] = y;
@@ -205,12 +239,30 @@ hvp_cg_step_kernel(const float* __restrict__ OB, const float* __restrict__ PtT, 
       s_rr.add(rj * rj);
     }
   }
-  const double rho_new = block_sum(s_rho.value(), red);
-  const double rr = block_sum(s_rr.value(), red);
-  const float beta = (float)(rho_new / rho);
-#pragma unroll 8
-  for (int64_t j = threadIdx.x; j < m; j += blockDim.x) p[j] = fmaf(beta, p[j], yv[j]);
-  if (threadIdx.x == 0) {
+  const double r0 = block_sum(s_rho.value(), red);
+  const double r1 = block_sum(s_rr.value(), red);
+  if (t == 0) {
+    part2[2 * (int64_t)blockIdx.x + 0] = r0;
+    part2[2 * (int64_t)blockIdx.x + 1] = r1;
+    // kHvpRho itself is rewritten by the next kernel while its blocks still need the old one
+    if (blockIdx.x == 0) sc[kHvpRhoOld] = rho;
+  }
+}
+
+__global__ void __launch_bounds__(kCgThreads)
+hvp_cg_dir_kernel(int64_t m, float* __restrict__ p, const float* __restrict__ yv,
+                  const double* __restrict__ part2, double* __restrict__ sc) {
+  __shared__ double red[33];
+  if (sc[kHvpBreak] != 0.0) return;
+  const int G = gridDim.x;
+  const int t = threadIdx.x;
+  const double rho_new = block_sum(t < G ? part2[2 * t + 0] : 0.0, red);
+  const double rr = block_sum(t < G ? part2[2 * t + 1] : 0.0, red);
+  const float beta = (float)(rho_new / sc[kHvpRhoOld]);
+  for (int64_t j = blockIdx.x * (int64_t)kCgThreads + t; j < m;
+       j += (int64_t)gridDim.x * kCgThreads)
+    p[j] = fmaf(beta, p[j], yv[j]);
+  if (blockIdx.x == 0 && t == 0) {
     sc[kHvpRho] = rho_new;
     sc[kHvpRR] = rr;
   }
