@@ -77,6 +77,27 @@ def test_hvp_uniform_translation_closed_form(cuda_lib):
     assert np.all(err_abs <= 2.0 * np.abs(t) * 1e-5 + 1e-3 * np.abs(want).sum(0))
 
 
+def test_hvp_translation_many_columns(cuda_lib):
+    """The translation closed form with 70,000 columns and 2,000 rows: the CG step's grid is
+    capped (256 CTAs of 256 threads, so threads stride over two columns) and the row passes
+    split their columns over 548 CTAs per row block (about 69 partials per lane of the split
+    reduction)."""
+    n, m, d, eps = 2000, 70000, 3, 0.1
+    pr = _problem(n, m, d, seed=14)
+    X, Y = to_dev(pr.X), to_dev(pr.Y)
+    a, b = to_dev(pr.a), to_dev(pr.b)
+    f, g, _, _, err, _ = cuda_lib.sinkhorn_solve_tol(X, Y, a, b, eps, 1e-5, 3000, 10,
+                                                     precision="fp32")
+    assert err < 1e-5
+    t = np.array([-0.3, 0.8, 0.15], np.float32)
+    V = np.tile(t, (n, 1)).astype(np.float32)
+    HV, iters, rel = cuda_lib.ot_hvp_x(X, Y, f, g, eps, to_dev(V), a, b, cg_tol=1e-6)
+    assert 0 < iters < 1000 and rel <= 1e-6
+    want = 2.0 * pr.a.astype(np.float64)[:, None] * t[None, :]
+    err_abs = np.abs(HV.cpu().numpy() - want).sum(0)
+    assert np.all(err_abs <= 2.0 * np.abs(t) * 1e-5 + 1e-3 * np.abs(want).sum(0))
+
+
 def test_hvp_is_symmetric_at_scale(cuda_lib):
     """<V1, H V2> = <V2, H V1> on 4000 x 5000 points, d = 3."""
     n, m, d, eps = 4000, 5000, 3, 0.05
