@@ -39,6 +39,8 @@ MUTATIONS = {
     "sk_output_drops_u": ("p[i * n + j] = u[i] * M[i * n + j] * v[j];", "p[i * n + j] = M[i * n + j] * v[j];"),
     "diag_kl_drops_mass_terms": ("kl += -mass + suma * sumb;", "kl += 0.0;"),
     "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
+    "diag_col_err_drops_b": ("col_err += fabs(col[j] - b[j]);", "col_err += fabs(col[j]);"),
+    "diag_dual_drops_mass_term": ("out[1] = dual - eps * (mass - suma * sumb);", "out[1] = dual;"),
 }
 
 
@@ -48,6 +50,7 @@ PY_MUTATIONS = {
     "hvp_outer_product_sign": ("blk -= (4.0 / eps)", "blk += (4.0 / eps)"),
     "hvp_drops_eps_in_response": ("dphi = eps * (", "dphi = ("),
     "hvp_self_term_sign": ("B[i * d:(i + 1) * d, i] += (2.0 / eps)", "B[i * d:(i + 1) * d, i] -= (2.0 / eps)"),
+    "divergence_wrong_debias_weight": ("return lxy - 0.5 * lxx - 0.5 * lyy", "return lxy - lxx - 0.5 * lyy"),
 }
 _TARGETS = {**{k: ("sinkhorn_oracle.c", v) for k, v in MUTATIONS.items()},
             **{k: ("__init__.py", v) for k, v in PY_MUTATIONS.items()}}
