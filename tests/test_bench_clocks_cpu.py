@@ -1,0 +1,52 @@
+"""The benchmark's clock record (median SM clock, the largest maximum clock and power, and the
+throttle reasons seen during the timed region), parsed from nvidia-smi's CSV. On the CPU a
+stand-in `nvidia-smi` on PATH prints canned samples; nothing here queries or changes a GPU."""
+import importlib.util
+import os
+import stat
+import time
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SAMPLES = [
+    "0, 1900, 2070, 900.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+    "0, 1950, 2070, 950.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+    "0, 2000, 2070, 1000.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active",
+    "0, [N/A], 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+]
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _fake_smi(tmp_path, lines):
+    exe = tmp_path / "nvidia-smi"
+    body = "".join(f"echo '{ln}'\n" for ln in lines)
+    exe.write_text("#!/bin/sh\n" + body + "exec sleep 30\n")
+    exe.chmod(exe.stat().st_mode | stat.S_IXUSR)
+    return str(tmp_path)
+
+
+def _sample(monkeypatch, tmp_path, lines):
+    monkeypatch.setenv("PATH", _fake_smi(tmp_path, lines) + os.pathsep + os.environ["PATH"])
+    sampler = _bench().ClockSampler(0).start()
+    time.sleep(0.5)
+    return sampler.stop()
+
+
+def test_median_clock_maxima_and_reasons(monkeypatch, tmp_path):
+    rec = _sample(monkeypatch, tmp_path, SAMPLES)
+    assert rec["samples"] == 4
+    assert rec["sm_mhz"] == 1950.0  # median of the three numeric samples
+    assert rec["sm_max_mhz"] == 2070.0
+    assert rec["power_w_max"] == 1000.0
+    assert rec["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_no_samples_is_reported(monkeypatch, tmp_path):
+    rec = _sample(monkeypatch, tmp_path, [])
+    assert rec["sm_mhz"] is None and rec["reasons"] == ["no samples"]
