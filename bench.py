@@ -267,8 +267,10 @@ def run_reference(args):
 # ---------------------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------------------
-# The sources the tensor-core LSE kernel is compiled from (its translation unit and the
-# headers it includes); the recorded ncu traffic is valid while these are unchanged.
+# The sources that define the tensor-core LSE kernel: its translation unit and the headers
+# whose code it runs. (fma_kernels.cuh and flashot.h are included there as well but hold
+# nothing the LSE kernel executes: the split reduction of the tf32 weighted sums, and the
+# public API.) The recorded ncu traffic is valid while these are unchanged.
 LSE_KERNEL_SOURCES = ("tc_kernels.cu", "common.cuh", "pack_kernels.cuh", "ptx.cuh",
                       "tc_api.h", "tc_host.h", "trace.h")
 
