@@ -1,6 +1,10 @@
-"""The benchmark's clock record (median SM clock, the largest maximum clock and power, and the
-throttle reasons seen during the timed region), parsed from nvidia-smi's CSV. On the CPU a
-stand-in `nvidia-smi` on PATH prints canned samples; nothing here queries or changes a GPU."""
+"""Host logic of the benchmark, on the CPU.
+
+The clock record (median SM clock, the largest maximum clock and power, and the throttle
+reasons seen during the timed region) is parsed from nvidia-smi's CSV; a stand-in
+`nvidia-smi` on PATH prints canned samples, so nothing here queries or changes a GPU. The
+LSE kernel's DRAM traffic is read from the committed ncu record only while the kernel's
+sources hash to the value the record was taken on."""
 import importlib.util
 import os
 import stat
@@ -50,3 +54,11 @@ def test_median_clock_maxima_and_reasons(monkeypatch, tmp_path):
 def test_no_samples_is_reported(monkeypatch, tmp_path):
     rec = _sample(monkeypatch, tmp_path, [])
     assert rec["sm_mhz"] is None and rec["reasons"] == ["no samples"]
+
+
+def test_traffic_record_is_keyed_on_the_kernel_sources(monkeypatch):
+    bench = _bench()
+    assert bench.profiled_traffic("bf16") is not None and bench.profiled_traffic("bf16") > 0
+    assert bench.profiled_traffic("no-such-precision") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.profiled_traffic("bf16") is None
