@@ -62,3 +62,35 @@ def test_traffic_record_is_keyed_on_the_kernel_sources(monkeypatch):
     assert bench.profiled_traffic("no-such-precision") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.profiled_traffic("bf16") is None
+
+
+def _profile_commands():
+    """Every `python bench.py ...` command line in the committed profile summaries (the
+    backslash continuations joined)."""
+    import glob
+    out = []
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        text = open(path).read().replace("\\\n", " ")
+        for line in text.splitlines():
+            if "bench.py" not in line:
+                continue
+            for part in line.split("&&"):
+                words = part.split()  # the commands quote nothing
+                while words and words[0] != "python":
+                    words.pop(0)  # drop an ncu prefix and its options
+                if words[:2] == ["python", "bench.py"]:
+                    out.append((os.path.basename(path), words[2:]))
+    return out
+
+
+def test_profile_commands_are_valid_bench_invocations(monkeypatch):
+    """The commands the profile summaries were made with run committed files only and still
+    parse with the benchmark's current options (warm-up and step rules included)."""
+    cmds = _profile_commands()
+    names = {name for name, _ in cmds}
+    assert len(names) == len([p for p in os.listdir(os.path.join(ROOT, "profiles"))
+                              if p.endswith(".md")])
+    bench = _bench()
+    for name, argv in cmds:
+        monkeypatch.setattr("sys.argv", ["bench.py", *argv])
+        bench.parse_args()  # exits (SystemExit) on an unknown flag or a broken rule
