@@ -14,6 +14,8 @@ inputs are promoted to fp64 before the call (fp32 -> fp64 is exact).
 Parity status of each function (what pins it, in tests/test_oracle_pins.py):
   half_step_f / half_step_g  marginal identities, the attention-form (LSE-rewrite)
                              identity, n=1 closed form, two-point closed form.
+  solve_dense                bitwise equal to solve (zero weights, rectangular shapes,
+                             eps schedules, warm starts).
   solve / dual_loss          two-point closed form, eps->inf closed form, eps->0
                              brute-force assignment bound, 1-D sorted-matching bound,
                              strong duality, monotone dual ascent, invariances.
@@ -93,6 +95,10 @@ def _lib():
                                          ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _dp, _dp, _dp]
             lib.oracle_solve.restype = ctypes.c_int
+            lib.oracle_solve_dense.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _dp,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               _dp, _dp, _dp]
+            lib.oracle_solve_dense.restype = ctypes.c_int
             lib.oracle_solve_symmetric.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _dp,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    _dp, _dp, _dp]
@@ -186,6 +192,26 @@ def solve(X, Y, a, b, eps_schedule, iters_per_stage, g0=None):
     _lib().oracle_solve(_p(X), _p(Y), _p(a), _p(b), n, m, d, _p(sched), int(sched.size),
                         int(iters_per_stage), 0 if g0 is None else 1, _p(f), _p(g),
                         ctypes.byref(loss))
+    return f, g, float(loss.value)
+
+
+def solve_dense(X, Y, a, b, eps_schedule, iters_per_stage, g0=None):
+    """The alternating solve of ``solve`` with the dense fp64 cost matrix built once and
+    read by every half-step (8nm bytes of host memory): bitwise the same (f, g, loss), at
+    O(nm) per half-step after one O(nmd) pass. For the long full-size solves that write
+    stored fixtures. Raises MemoryError when the cost matrix cannot be allocated."""
+    X, Y, a, b = _f64(X), _f64(Y), _f64(a), _f64(b)
+    n, d = X.shape
+    m = Y.shape[0]
+    sched = _f64(np.atleast_1d(eps_schedule))
+    f = np.zeros(n, dtype=np.float64)
+    g = np.zeros(m, dtype=np.float64) if g0 is None else _f64(g0).copy()
+    loss = ctypes.c_double(0.0)
+    rc = _lib().oracle_solve_dense(_p(X), _p(Y), _p(a), _p(b), n, m, d, _p(sched),
+                                   int(sched.size), int(iters_per_stage),
+                                   0 if g0 is None else 1, _p(f), _p(g), ctypes.byref(loss))
+    if rc != 0:
+        raise MemoryError(f"oracle_solve_dense: cannot allocate the {n}x{m} cost matrix")
     return f, g, float(loss.value)
 
 

@@ -136,6 +136,107 @@ int oracle_solve(const double *X, const double *Y, const double *a, const double
 }
 
 /*
+ * The same alternating solve as oracle_solve, with the dense cost matrix built once
+ * (C_ij = sq_cost(x_i, y_j), n x m fp64, row-major) and read by every half-step, so a
+ * long solve costs one O(nmd) pass plus O(nm) per half-step instead of O(nmd) each.
+ * Every value it forms is the one oracle_half_step forms, in the same order:
+ *   - (x - y)^2 == (y - x)^2 exactly, so C_ij is the cost either half-step computes;
+ *   - log(w) is the same libm call on the same double, taken once per point;
+ *   - each row (F) or column (G) takes its max over all terms, then sums
+ *     exp(e - max) in increasing index order.
+ * The G-update walks the rows of C for a block of columns at a time (loop interchange
+ * only: the per-column sums still run i = 0, 1, ..., n-1), so the result is bitwise
+ * that of oracle_solve. Needs 8nm bytes of host memory; returns -1 if it cannot get
+ * them (nothing written), else 0.
+ */
+int oracle_solve_dense(const double *X, const double *Y, const double *a, const double *b,
+                       int64_t n, int64_t m, int64_t d, const double *eps_sched, int n_stages,
+                       int iters_per_stage, int warm_start, double *f, double *g, double *loss)
+{
+    double *C = (double *)malloc((size_t)(n > 0 ? n : 1) * (size_t)(m > 0 ? m : 1) * sizeof(double));
+    double *la = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    double *lb = (double *)malloc((size_t)(m > 0 ? m : 1) * sizeof(double));
+    if (!C || !la || !lb) {
+        free(C);
+        free(la);
+        free(lb);
+        return -1;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = 0; j < m; ++j) C[i * m + j] = sq_cost(X + i * d, Y + j * d, d);
+    for (int64_t i = 0; i < n; ++i) la[i] = a[i] > 0.0 ? log(a[i]) : -INFINITY;
+    for (int64_t j = 0; j < m; ++j) lb[j] = b[j] > 0.0 ? log(b[j]) : -INFINITY;
+    if (!warm_start)
+        for (int64_t j = 0; j < m; ++j) g[j] = 0.0;
+    enum { CB = 32 }; /* columns per block of the G-update */
+    const int64_t nblk = (m + CB - 1) / CB;
+    for (int s = 0; s < n_stages; ++s) {
+        const double eps = eps_sched[s];
+        for (int it = 0; it < iters_per_stage; ++it) {
+            /* f_i = -eps log sum_j b_j exp((g_j - C_ij) / eps), max-shifted */
+#pragma omp parallel
+            {
+                double *e = (double *)malloc((size_t)(m > 0 ? m : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+                for (int64_t i = 0; i < n; ++i) {
+                    const double *Ci = C + i * m;
+                    double mx = -INFINITY;
+                    for (int64_t j = 0; j < m; ++j) {
+                        if (b[j] > 0.0) {
+                            e[j] = (g[j] - Ci[j]) / eps + lb[j];
+                            if (e[j] > mx) mx = e[j];
+                        } else {
+                            e[j] = -INFINITY;
+                        }
+                    }
+                    double sum = 0.0;
+                    if (mx > -INFINITY)
+                        for (int64_t j = 0; j < m; ++j)
+                            if (e[j] > -INFINITY) sum += exp(e[j] - mx);
+                    f[i] = (mx > -INFINITY) ? -eps * (mx + log(sum)) : INFINITY;
+                }
+                free(e);
+            }
+            /* g_j = -eps log sum_i a_i exp((f_i - C_ij) / eps), max-shifted */
+#pragma omp parallel for schedule(dynamic, 1)
+            for (int64_t blk = 0; blk < nblk; ++blk) {
+                const int64_t j0 = blk * CB;
+                const int64_t nj = (m - j0) < CB ? (m - j0) : CB;
+                double mx[CB], sum[CB];
+                for (int64_t c = 0; c < nj; ++c) {
+                    mx[c] = -INFINITY;
+                    sum[c] = 0.0;
+                }
+                for (int64_t i = 0; i < n; ++i) {
+                    if (!(a[i] > 0.0)) continue;
+                    const double *Ci = C + i * m + j0;
+                    for (int64_t c = 0; c < nj; ++c) {
+                        const double e = (f[i] - Ci[c]) / eps + la[i];
+                        if (e > mx[c]) mx[c] = e;
+                    }
+                }
+                for (int64_t i = 0; i < n; ++i) {
+                    if (!(a[i] > 0.0)) continue;
+                    const double *Ci = C + i * m + j0;
+                    for (int64_t c = 0; c < nj; ++c) {
+                        const double e = (f[i] - Ci[c]) / eps + la[i];
+                        if (e > -INFINITY) sum[c] += exp(e - mx[c]);
+                    }
+                }
+                for (int64_t c = 0; c < nj; ++c)
+                    g[j0 + c] = (mx[c] > -INFINITY) ? -eps * (mx[c] + log(sum[c])) : INFINITY;
+            }
+        }
+    }
+    if (loss) *loss = oracle_dual_loss(a, b, f, g, n, m);
+    free(C);
+    free(la);
+    free(lb);
+    return 0;
+}
+
+/*
  * Symmetric (averaged) schedule (the "symmetric-vs-alternating" comparison of the SAI
  * replication review, "Strengths"): both half-steps use the previous iterate,
  *     f' = (f + F(g)) / 2,   g' = (g + G(f)) / 2,

@@ -41,6 +41,9 @@ MUTATIONS = {
     "symmetric_wrong_half": ("g[j] = 0.5 * (g[j] + gn[j]);", "g[j] = 0.5 * (f[j % n] + gn[j]);"),
     "diag_col_err_drops_b": ("col_err += fabs(col[j] - b[j]);", "col_err += fabs(col[j]);"),
     "diag_dual_drops_mass_term": ("out[1] = dual - eps * (mass - suma * sumb);", "out[1] = dual;"),
+    "dense_f_cost_sign": ("e[j] = (g[j] - Ci[j]) / eps + lb[j];", "e[j] = (g[j] + Ci[j]) / eps + lb[j];"),
+    "dense_g_sum_drops_weight": ("if (e > -INFINITY) sum[c] += exp(e - mx[c]);",
+                                 "if (e > -INFINITY) sum[c] += exp(e - la[i] - mx[c]);"),
 }
 
 
