@@ -34,8 +34,10 @@ UNIT = "iters/s"
 WORKLOAD_IDX = 3
 K_APPLY = 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25 -> tf32 peak = bf16 x 1.1/2.25.
+# Nominal dense tensor rates (PFLOP/s): tf32 1.1, bf16 2.25. Used only when no measured tf32
+# peak (bench.py --measure-tf32-peak, stored under profiles/) is present.
 TF32_OVER_BF16 = 1.1 / 2.25
+TF32_PEAK_FILE = os.path.join(ROOT, "profiles", "tf32_peak_gb300.json")
 L2_FLUSH_BYTES = 256 << 20
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -51,6 +53,13 @@ def parse_args():
     p.add_argument("--precision", choices=["bf16", "tf32", "tf32x3", "fp32"], default=None,
                    help="contraction precision (default: bf16; fp32 for the d < 32 workloads)")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    p.add_argument("--no-tf32", action="store_true",
+                   help="skip the tf32 record of the benchmark line")
+    p.add_argument("--measure-tf32-peak", action="store_true",
+                   help="time torch.matmul 8192^3 with tf32 allowed (best of 10, and back to "
+                        "back for 4 s) and print the record; with --write-peak also store it "
+                        "as profiles/tf32_peak_gb300.json, which the roofline lines use")
+    p.add_argument("--write-peak", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-passes", type=int, default=0, metavar="P",
                    help="profiling driver: pack once, run P f-updates and P g-updates of the "
@@ -130,6 +139,49 @@ def load_peaks():
         with open(path) as fh:
             return json.load(fh), "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_tf32_peak(peaks, peak_src):
+    """Sustained tf32 tensor-core peak (TFLOP/s), the median SM clock (MHz) it was measured
+    at, and where it comes from: the measured record under profiles/ when present, else
+    the bf16 sustained peak x the nominal tf32/bf16 ratio."""
+    if os.path.exists(TF32_PEAK_FILE):
+        with open(TF32_PEAK_FILE) as fh:
+            rec = json.load(fh)
+        return (float(rec["tf32_tflops_sustained"]), rec.get("clocks_sustained", {}).get("sm_mhz"),
+                "measured tf32_tflops_sustained (profiles/tf32_peak_gb300.json)")
+    bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    return (bf16_sus * TF32_OVER_BF16, peak_clock_mhz(peaks),
+            f"{peak_src} bf16_tflops_sustained x 1.1/2.25 (nominal ratio)")
+
+
+def peak_clock_mhz(peaks):
+    """Median SM clock (MHz) under which the sustained bf16 peak was measured, or None."""
+    c = peaks.get("clocks_under_load") or {}
+    v = c.get("sm_mhz_median")
+    return float(v) if v else None
+
+
+def clock_matched(frac, run_mhz, peak_mhz):
+    """The roofline fraction with the peak rescaled from the clock it was measured at to
+    the clock this run saw (time x clock is the work per clock)."""
+    if not frac or not run_mhz or not peak_mhz:
+        return None
+    return frac * float(peak_mhz) / float(run_mhz)
+
+
+def device_sms(dev=0):
+    """Streaming multiprocessors of the device (read from the device, not assumed)."""
+    import torch
+    return int(torch.cuda.get_device_properties(dev).multi_processor_count)
+
+
+def run_clock_hz(clk, peaks):
+    """SM clock for unit-count peaks (FP32 lanes, SFU): the median sampled during the
+    timed region, else the maximum clock. Returns (Hz, label)."""
+    if clk and clk.get("sm_mhz"):
+        return float(clk["sm_mhz"]) * 1e6, "median SM clock sampled during the timed region"
+    return float(peaks.get("sm_max_mhz", 2070.0)) * 1e6, "maximum SM clock (no samples)"
 
 
 def workload_config(prec, accumulate="f32 scores/LSE, f64 loss"):
@@ -230,7 +282,7 @@ def oracle_sample(pr, target_s=10.0):
     per_row = dt / r
     iter_s = per_row * pr.n + per_row * pr.m  # n = m rows of equal cost for the g-update
     return {"value": 1.0 / iter_s, "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "rows": int(r),
             "sample": f"f-update of {r} of {pr.n} rows against all {pr.m} columns (d={pr.d}, "
                       f"fp64), {dt:.1f} s; iteration time extrapolated as (n+m) x per-row time"}
 
@@ -242,24 +294,35 @@ def run_reference(args):
     from workloads import workload
     pr = workload(WORKLOAD_IDX)
     samples = []
+    step_s = []
     for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
         s = oracle_sample(pr, target_s=8.0)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
             samples.append(s)
+            step_s.append(dt)
     vals = [s["value"] for s in samples]
     v = statistics.median(vals)
-    iter_s = 1.0 / v
+    full_step_s = 100.0 / v  # one step of the workload = 100 iterations
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": iter_s * 100 * 1e3,
+        "steps": args.steps, "warmup": args.warmup,
+        # what each timed step executed: one bounded row sample of the f-update
+        "ms_per_step": statistics.median(step_s) * 1e3,
+        "extrapolated": True,
+        "sampled_rows_per_step": samples[-1]["rows"],
+        "extrapolated_ms_per_full_step": full_step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, same generator as the GPU arm)",
         "config": workload_config("f64", "f64 (CPU oracle, dense loops, no tiling)"),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": samples[-1]["cores"],
                          "kind": "oracle", "sample": samples[-1]["sample"]},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "fp64 plain-loop CPU oracle timed on the host cores; one step = 100 "
-                "iterations, extrapolated from a bounded row sample per step",
+        "note": "fp64 plain-loop CPU oracle timed on the host cores. Each timed step runs "
+                "the f-update for a bounded sample of rows against all columns "
+                "(ms_per_step is that sample's wall time); value is the iterations/s of "
+                "the whole 50k x 50k problem extrapolated from it as (n + m) x per-row time",
     }
     print(json.dumps(line), flush=True)
 
@@ -299,11 +362,13 @@ def profiled_traffic(prec):
     return ent.get("dram_bytes_per_full_launch")
 
 
-# Peak fp32 FMA throughput used for the CUDA-core path: 152 SMs x 128 FP32 lanes x 2 flops
-# per FMA x the maximum SM clock. The SFU peak for ex2 is taken as 32 per clock per SM.
+# Peak fp32 FMA throughput used for the CUDA-core path: SMs (read from the device) x 128
+# FP32 lanes x 2 flops per FMA x the SM clock sampled during the timed region. The SFU rate
+# for ex2.approx.ftz.f32 is 32 per clock per SM (measured with a throughput probe on GB300:
+# 32.7 per clock); the SFU reciprocal rate is 16.
 FP32_LANES_PER_SM = 128
 SFU_EX2_PER_SM_CLK = 32
-N_SMS = 152
+SFU_RCP_PER_SM_CLK = 16
 
 
 def run_other_workload(args):
@@ -395,11 +460,14 @@ def run_other_workload(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     launches0 = lds.launch_count()
+    clocks = ClockSampler(0).start()
+    time.sleep(0.3)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clk_rec = clocks.stop()
     ms = e0.elapsed_time(e1)
     launches = lds.launch_count() - launches0
     timer = lds.KernelTimer(cap=args.steps * 2200).start()
@@ -410,32 +478,39 @@ def run_other_workload(args):
     timer.stop()
     if lds.workspace_status(ws) != 0:
         raise RuntimeError("device timeout reported")
-    peaks, _ = load_peaks()
-    clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    peaks, peak_src = load_peaks()
+    sms = device_sms()
+    clk, clk_src = run_clock_hz(clk_rec, peaks)
     avg = ms_hot / max(n_hot, 1) / 1e3
     # Scores per timed launch of the hot kernel class: the streaming solve launches one LSE
     # pass per half-step; the single-launch cluster solve covers the whole solve.
     per_launch_scores = scores_per_step * args.steps / max(n_hot, 1)
     if prec == "fp32":
         roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
-                "peak": N_SMS * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)"}
+                "peak": sms * FP32_LANES_PER_SM * 2 * clk / 1e12, "unit": "TFLOP/s (fp32 FMA)",
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x {clk_src}"}
     else:
         bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        tf32, tf32_mhz, tf32_src = load_tf32_peak(peaks, peak_src)
         # Algorithmic flops (2d per score); split tf32 runs three tf32 contractions, so its
         # ceiling for the algorithmic rate is a third of the tf32 peak.
-        tf32 = bf16_sus * TF32_OVER_BF16
         roof = {"bound": "tensor", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
                 "peak": bf16_sus if prec == "bf16" else (tf32 / 3 if prec == "tf32x3" else tf32),
-                "unit": "TFLOP/s"}
+                "unit": "TFLOP/s",
+                "peak_source": (f"{peak_src} bf16_tflops_sustained" if prec == "bf16" else
+                                tf32_src + (" / 3 (split tf32)" if prec == "tf32x3" else ""))}
+        pk_mhz = peak_clock_mhz(peaks) if prec == "bf16" else tf32_mhz
+        roof["frac_clock_matched"] = clock_matched(roof["achieved"] / roof["peak"],
+                                                   clk_rec.get("sm_mhz"), pk_mhz)
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["sfu_frac"] = (per_launch_scores / avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk)
+    roof["sfu_frac"] = (per_launch_scores / avg) / (sms * SFU_EX2_PER_SM_CLK * clk)
     if prec == "fp32" and d <= 32:
         # FMA-pipe work per score of the small-d CUDA-core LSE: the padded dot product
         # (d_pad lanes), kappa * dot + bias, the max shift and the sum (the max itself runs
         # on the ALU pipe): d_pad + 3 lane operations against 128 lanes per SM per clock.
         d_pad = (d + 3) // 4 * 4
         roof["fma_pipe_frac"] = ((per_launch_scores / avg) * (d_pad + 3)
-                                 / (N_SMS * FP32_LANES_PER_SM * clk))
+                                 / (sms * FP32_LANES_PER_SM * clk))
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
     graph = None
@@ -478,7 +553,7 @@ def run_other_workload(args):
             "dtype": prec, "config": {"workload": pr.name, "n": n, "m": m, "d": d,
                                       "eps": sched if len(sched) > 1 else sched[0],
                                       "iters_per_stage": pr.iters_per_stage},
-            "roofline": roof, "gpu_launches": int(launches)}
+            "roofline": roof, "clocks": clk_rec, "gpu_launches": int(launches)}
     if graph is not None:
         line["cuda_graph"] = graph
     if args.diagnostics:
@@ -652,6 +727,8 @@ def run_hvp(args):
     timer = lds.KernelTimer(cap=args.steps * 4000).start()
     launches0 = lds.launch_count()
     stream = torch.cuda.current_stream()
+    clocks = ClockSampler(0).start()
+    time.sleep(0.3)
     times = []
     for _ in range(args.steps):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -662,6 +739,7 @@ def run_hvp(args):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1))
     launches = lds.launch_count() - launches0
+    clk_rec = clocks.stop()
     n_ws, ms_ws = timer.read(lds.KernelTimer.WSUM)
     n_ot, ms_ot = timer.read(lds.KernelTimer.OTHER)
     timer.stop()
@@ -670,7 +748,8 @@ def run_hvp(args):
     _, cg_iters, rel = res["r"]
     ms = statistics.median(times)
     peaks, _ = load_peaks()
-    clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    sms = device_sms()
+    clk, clk_src = run_clock_hz(clk_rec, peaks)
     nm = float(n) * float(n)
     passes = 2 * cg_iters + 5  # CG: P p and P^T t; plus [PY|r], [P^T V|P^T s|c], T, rhs, final
     pass_avg = ms_ws / max(n_ws, 1) / 1e3
@@ -694,11 +773,13 @@ def run_hvp(args):
             "roofline": {"bound": "alu (fp32 FMA pipe)",
                          "kernel": "wsum_fma_pair (streaming passes)",
                          "achieved": lane_ops / passes_s / 1e12,
-                         "peak": N_SMS * FP32_LANES_PER_SM * clk / 1e12,
+                         "peak": sms * FP32_LANES_PER_SM * clk / 1e12,
                          "unit": "T FMA-pipe lane-ops/s",
+                         "peak_source": f"{sms} SMs x 128 FP32 lanes x {clk_src}",
                          "lane_ops_per_hvp": lane_ops,
-                         "sfu_frac": (nm / pass_avg) / (N_SMS * SFU_EX2_PER_SM_CLK * clk),
+                         "sfu_frac": (nm / pass_avg) / (sms * SFU_EX2_PER_SM_CLK * clk),
                          "avg_pass_ms": pass_avg * 1e3},
+            "clocks": clk_rec,
             "steps": args.steps, "warmup": args.warmup, "dtype": "fp32",
             "gpu_launches": int(launches),
             "config": {"workload": "hvp50k_d3: n=m=%d, d=3, Uniform[0,1]^3, uniform weights" % n,
@@ -794,11 +875,12 @@ def run_sk(args):
     # (row and column sums, the final scaling), n^2 + 2 n n_iter SFU ops (exp and one
     # reciprocal per sum) and 2 n^2 4 bytes of HBM traffic. Its time floor is the largest of
     # the three at FP32 = 128 lanes, SFU reciprocal = 16 lanes per clock per SM.
-    clk_hz = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    sms = device_sms()
+    clk_hz, clk_src = run_clock_hz(clk, peaks)
     fma_ops = 2 * n * n * n_iter + 2 * n * n
     xu_ops = n * n + 2 * n * n_iter
-    t_fma = B * fma_ops / (N_SMS * FP32_LANES_PER_SM * clk_hz)
-    t_xu = B * xu_ops / (N_SMS * 16 * clk_hz)
+    t_fma = B * fma_ops / (sms * FP32_LANES_PER_SM * clk_hz)
+    t_xu = B * xu_ops / (sms * SFU_RCP_PER_SM_CLK * clk_hz)
     t_hbm = bytes_step / (hbm * 1e9)
     t_floor = max(t_fma, t_xu, t_hbm)
     line = {"metric": "batched Sinkhorn-Knopp (mHC %dx%d, %d iterations)" % (n, n, n_iter),
@@ -815,7 +897,7 @@ def run_sk(args):
                          "hbm_achieved_gbs": bytes_step / (ms / 1e3) / 1e9,
                          "hbm_frac": bytes_step / (ms / 1e3) / 1e9 / hbm,
                          "peak_source": f"{src} hbm_gbs; FP32 and SFU from unit counts x "
-                                        "max SM clock"},
+                                        f"{sms} SMs x {clk_src}"},
             "clocks": clk, "cpu_baseline": cpu, "gpu_launches": args.steps,
             "config": {"workload": "B=%d matrices %dx%d, logits N(0,1), %d iterations" % (B, n, n, n_iter),
                        "l2": "inputs larger than L2" if flush is None else "L2 flushed before each step"}}
@@ -916,13 +998,81 @@ def run_gpu(args):
 
     peaks, peak_src = load_peaks()
     bf16_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    # Split tf32 runs three tf32 contractions per algorithmic one: its ceiling for the
-    # algorithmic rate is a third of the tf32 peak.
-    peak = bf16_sus if prec == "bf16" else bf16_sus * TF32_OVER_BF16 / (3 if prec == "tf32x3" else 1)
+    tf32_sus, tf32_mhz, tf32_src = load_tf32_peak(peaks, peak_src)
+
+    def lse_peak(p):
+        # Split tf32 runs three tf32 contractions per algorithmic one: its ceiling for the
+        # algorithmic rate is a third of the tf32 peak.
+        if p == "bf16":
+            return bf16_sus, peak_clock_mhz(peaks), f"{peak_src} bf16_tflops_sustained"
+        div = 3 if p == "tf32x3" else 1
+        return (tf32_sus / div, tf32_mhz,
+                tf32_src + (" / 3 (split tf32)" if p == "tf32x3" else ""))
+
+    peak, peak_mhz, peak_label = lse_peak(prec)
     lse_avg_ms = ms_lse / max(n_lse, 1)
     flops_per_launch = 2.0 * nm * d
     achieved = flops_per_launch / (lse_avg_ms / 1e3) / 1e12
     traffic = profiled_traffic(prec)
+
+    # ---- the same step with a tf32 contraction (the pages' own precision) ----------------
+    tf32_rec = None
+    if prec == "bf16" and not args.no_tf32:
+        ws32 = lds.Workspace(lds.workspace_bytes(n, m, d, K_APPLY, "tf32"))
+
+        def step32():
+            flush.zero_()
+            lds.sinkhorn_solve(X, Y, None, None, eps, iters, precision="tf32", f_out=f,
+                               g_out=g, loss_out=loss, workspace=ws32)
+            lds.ot_grad_x(X, Y, g, eps, precision="tf32", out=grad, workspace=ws32,
+                          reuse_pack=True)
+            lds.transport_apply(X, Y, f, g, eps, V, precision="tf32", out=PV, workspace=ws32,
+                                reuse_pack=True)
+            lds.transport_apply(X, Y, f, g, eps, U, transpose=True, precision="tf32",
+                                out=PtU, workspace=ws32, reuse_pack=True)
+            lds.transport_hadamard_xy(X, Y, f, g, eps, precision="tf32", out=h,
+                                      workspace=ws32, reuse_pack=True)
+
+        for _ in range(args.warmup):
+            step32()
+        torch.cuda.synchronize()
+        timer32 = lds.KernelTimer(cap=args.steps * 600).start()
+        clocks32 = ClockSampler(local).start()
+        time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step32()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        clk32 = clocks32.stop()
+        ms32 = max_over_ranks(t0.elapsed_time(t1), world, dev)
+        n32, ms_lse32 = timer32.read(lds.KernelTimer.LSE)
+        timer32.stop()
+        if lds.workspace_status(ws32) != 0:
+            raise RuntimeError("a kernel reported a device timeout in the tf32 region")
+        avg32 = ms_lse32 / max(n32, 1)
+        ach32 = flops_per_launch / (avg32 / 1e3) / 1e12
+        pk32, pk32_mhz, pk32_label = lse_peak("tf32")
+        tf32_rec = {
+            "value": replica_throughput(args.steps * iters, ms32, world), "unit": UNIT,
+            "ms_per_step": ms32 / args.steps, "dtype": "tf32",
+            "score_evals_per_s": scores_per_step * args.steps * world / (ms32 / 1e3),
+            "roofline": {"bound": "tensor", "achieved": ach32, "peak": pk32,
+                         "unit": "TFLOP/s", "frac": ach32 / pk32,
+                         "frac_clock_matched": clock_matched(ach32 / pk32, clk32.get("sm_mhz"),
+                                                             pk32_mhz),
+                         "peak_clock_mhz": pk32_mhz, "avg_launch_ms": avg32,
+                         "launches_timed": n32, "peak_source": pk32_label},
+            "clocks": clk32,
+            "note": "the same step (solve, gradient, both applications, Hadamard) with every "
+                    "contraction on tf32 tensor cores, timed after the bf16 region",
+        }
+        del ws32
 
     # ---- end to end through the public API with host buffers -----------------------------
     e2e = None
@@ -1010,13 +1160,14 @@ def run_gpu(args):
             "config": workload_config(prec),
             "score_evals_per_s": score_evals,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "frac_clock_matched": clock_matched(achieved / peak, clk.get("sm_mhz"),
+                                                             peak_mhz),
+                         "peak_clock_mhz": peak_mhz, "traffic": traffic,
                          "kernel": "lse_tc_kernel (streaming LSE half-step)",
                          "algorithmic_flops_per_launch": flops_per_launch,
                          "avg_launch_ms": lse_avg_ms, "launches_timed": n_lse,
-                         "peak_source": f"{peak_src} bf16_tflops_sustained"
-                                        + ("" if prec == "bf16" else " x 1.1/2.25 (tf32)")
-                                        + (" / 3 (split tf32)" if prec == "tf32x3" else "")},
+                         "peak_source": peak_label},
             "kernels_ms_per_step": {"lse": ms_lse / args.steps, "wsum": ms_ws / args.steps,
                                     "other": ms_ot / args.steps,
                                     "launches_per_step": {"lse": n_lse / args.steps,
@@ -1024,6 +1175,7 @@ def run_gpu(args):
                                                           "other": n_ot / args.steps}},
             "clocks": clk,
             "e2e": e2e,
+            "tf32": tf32_rec,
             "gpu_launches": int(launches),
             "cpu_baseline": cpu,
             "replicas": "one independent problem per rank" if world > 1 else None,
@@ -1084,8 +1236,72 @@ def run_profile_driver(args):
           f"{2 * args.profile_passes + 1} LSE passes{extra}, f[0]={float(f[0]):.6f}")
 
 
+def run_measure_tf32_peak(args):
+    """Dense tf32 tensor-core throughput of this GPU, measured like the bf16 peaks the
+    roofline lines use: torch.matmul of two 8192 x 8192 fp32 matrices with tf32 allowed
+    (2 N^3 flops), best of 10 single launches (burst) and back to back for 4 s under the
+    power cap (sustained), CUDA events, SM clocks sampled during each."""
+    import torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    torch.set_float32_matmul_precision("high")  # allow tf32 tensor cores for fp32 matmul
+    N = 8192
+    gen = torch.Generator(device=dev).manual_seed(8192)
+    A = torch.randn(N, N, device=dev, generator=gen)
+    B = torch.randn(N, N, device=dev, generator=gen)
+    C = torch.empty(N, N, device=dev)
+    flops = 2.0 * N ** 3
+    for _ in range(5):
+        torch.matmul(A, B, out=C)
+    torch.cuda.synchronize()
+    err = float((C[:64, :64].double() - A[:64].double() @ B[:, :64].double()).abs().max())
+    clocks = ClockSampler(0).start()
+    time.sleep(0.3)
+    best = float("inf")
+    for _ in range(10):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(A, B, out=C)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    clk_burst = clocks.stop()
+    reps = max(1, int(4.0 / (best / 1e3)))
+    clocks = ClockSampler(0).start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        torch.matmul(A, B, out=C)
+    e1.record()
+    torch.cuda.synchronize()
+    clk_sus = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    rec = {"command": "python bench.py --measure-tf32-peak --write-peak",
+           "tf32_tflops": flops / (best / 1e3) / 1e12,
+           "tf32_tflops_sustained": flops * reps / (ms / 1e3) / 1e12,
+           "how": "torch.matmul fp32 8192^3 with torch.set_float32_matmul_precision('high') "
+                  "(tf32 tensor cores), 2*N^3 flops: best of 10 (burst) and %d back to back "
+                  "(sustained, %.1f s), CUDA events" % (reps, ms / 1e3),
+           "max_abs_err_vs_fp64_64x64": err,
+           "clocks_burst": clk_burst, "clocks_sustained": clk_sus,
+           "gpu_name": torch.cuda.get_device_name(0), "sms": device_sms(),
+           "torch": torch.__version__,
+           "when": time.strftime("%Y-%m-%dT%H:%M:%SZ", time.gmtime())}
+    print(json.dumps(rec), flush=True)
+    if args.write_peak:
+        with open(TF32_PEAK_FILE, "w") as fh:
+            json.dump(rec, fh, indent=1)
+            fh.write("\n")
+
+
 def main():
     args = parse_args()
+    if args.measure_tf32_peak:
+        run_measure_tf32_peak(args)
+        return
     if args.profile_passes > 0:
         args.precision = args.precision or "bf16"
         run_profile_driver(args)

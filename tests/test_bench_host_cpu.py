@@ -94,3 +94,30 @@ def test_profile_commands_are_valid_bench_invocations(monkeypatch):
     for name, argv in cmds:
         monkeypatch.setattr("sys.argv", ["bench.py", *argv])
         bench.parse_args()  # exits (SystemExit) on an unknown flag or a broken rule
+
+
+def test_clock_matched_fraction_and_peak_sources(monkeypatch, tmp_path):
+    """The clock-matched fraction rescales the peak from the clock it was measured at to
+    the run's clock; the tf32 peak comes from the measured record when present, else from
+    the bf16 peak times the nominal ratio, and says which; unit-count peaks use the
+    sampled clock, or the maximum clock when there are no samples."""
+    b = _bench()
+    assert b.clock_matched(0.98, 1725.0, 1462.0) == 0.98 * 1462.0 / 1725.0
+    assert b.clock_matched(0.98, None, 1462.0) is None
+    assert b.clock_matched(0.98, 1725.0, None) is None
+    peaks = {"bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+             "clocks_under_load": {"sm_mhz_median": 1440.0}}
+    assert b.peak_clock_mhz(peaks) == 1440.0
+    assert b.peak_clock_mhz({}) is None
+    monkeypatch.setattr(b, "TF32_PEAK_FILE", str(tmp_path / "absent.json"))
+    pk, mhz, src = b.load_tf32_peak(peaks, "measured")
+    assert pk == 1700.0 * 1.1 / 2.25 and mhz == 1440.0 and "nominal" in src
+    rec = tmp_path / "tf32.json"
+    rec.write_text('{"tf32_tflops_sustained": 900.0, "clocks_sustained": {"sm_mhz": 1500.0}}')
+    monkeypatch.setattr(b, "TF32_PEAK_FILE", str(rec))
+    pk, mhz, src = b.load_tf32_peak(peaks, "measured")
+    assert pk == 900.0 and mhz == 1500.0 and "measured" in src
+    hz, label = b.run_clock_hz({"sm_mhz": 1700.0}, peaks)
+    assert hz == 1.7e9 and "sampled" in label
+    hz, label = b.run_clock_hz({"sm_mhz": None}, peaks)
+    assert hz == 2.07e9 and "maximum" in label

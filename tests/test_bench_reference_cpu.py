@@ -5,6 +5,7 @@ import json
 import os
 import subprocess
 import sys
+import time
 
 import pytest
 
@@ -19,7 +20,9 @@ def _run(env_extra):
 
 
 def test_reference_arm_prints_one_contract_line():
+    t0 = time.perf_counter()
     r = _run({"RANK": "0", "WORLD_SIZE": "1"})
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -32,6 +35,11 @@ def test_reference_arm_prints_one_contract_line():
     cpu = line["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
     assert "rows" in cpu["sample"]
+    # The line says what it executed: each timed step is one bounded row sample, so the
+    # steps' time fits inside the run; the full-problem figure is marked extrapolated.
+    assert line["extrapolated"] is True and line["sampled_rows_per_step"] >= 1
+    assert line["ms_per_step"] * line["steps"] / 1e3 < wall
+    assert line["extrapolated_ms_per_full_step"] > line["ms_per_step"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
