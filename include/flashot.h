@@ -311,22 +311,34 @@ int flashot_plan_diagnostics(const float *X, const float *Y, const float *a, con
  *
  * flashot_sinkhorn_step_f_noalloc computes the same f = F(g) as flashot_sinkhorn_step_f
  * (same arguments, minus ws / ws_bytes) and allocates nothing: its scratch is one array of
- * FLASHOT_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library as device memory, which
- * every GPU that loads the library keeps reserved until the process exits. X, Y, b, g and
- * f are still the caller's device buffers.
+ * FLASHOT_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library as device memory. The
+ * array is reserved in a context when the library's module that holds it is loaded there:
+ * under CUDA's default lazy module loading that is the first call of either function below
+ * in that context; with CUDA_MODULE_LOADING=EAGER it is when the context is created. It
+ * stays reserved until the context is destroyed. X, Y, b, g and f are still the caller's
+ * device buffers.
  *  - Sizes whose workspace (flashot_workspace_bytes(n, m, d, 0, flags)) exceeds 64 MiB are
  *    rejected with FLASHOT_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *  - Only the precision bits of flags are used; the inputs are always re-packed, because
- *    the array keeps whatever the previous call left in it.
- *  - The first call on a device looks up the array's device address with that device
- *    current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - flags are those of flashot_sinkhorn_step_f (precision bits, FLASHOT_VALIDATE), except
+ *    that FLASHOT_REUSE_PACK is ignored: the array keeps whatever the previous call left in
+ *    it, so the inputs are always packed afresh (which also clears the status word).
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress), after checking that the current device is sm_103. The first
+ *    call in a context also loads the module; make it before any stream capture.
  *  - All calls on a device share the one array: calls whose GPU work may overlap (other
  *    streams, other host threads) race on it and give undefined results. Serialise them.
+ *
+ * flashot_noalloc_status(stream) is flashot_workspace_status for that array: it
+ * synchronises `stream` and returns FLASHOT_ERR_DEVICE_TIMEOUT if a kernel of an earlier
+ * flashot_sinkhorn_step_f_noalloc call in the current context gave up a bounded wait (and
+ * clears the word), else FLASHOT_OK; FLASHOT_ERR_UNSUPPORTED_DEVICE or FLASHOT_ERR_CUDA if
+ * the array cannot be reached. It allocates nothing either.
  */
 #define FLASHOT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 int flashot_sinkhorn_step_f_noalloc(const float *X, const float *Y, const float *b,
                                     const float *g, int64_t n, int64_t m, int64_t d, float eps,
                                     int flags, float *f, flashot_stream_t stream);
+int flashot_noalloc_status(flashot_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -98,6 +98,7 @@ SIGNATURES = {
         _vp, _vp, ctypes.c_size_t, _vp]),
     "flashot_sinkhorn_step_f_noalloc": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, ctypes.c_int, _vp, _vp]),
+    "flashot_noalloc_status": (ctypes.c_int, [_vp]),
     "flashot_ot_grad_x": (ctypes.c_int, [
         _vp, _vp, _vp, _vp, _vp, _c_i64, _c_i64, _c_i64, ctypes.c_float, _vp, ctypes.c_int,
         _vp, ctypes.c_size_t, _vp]),

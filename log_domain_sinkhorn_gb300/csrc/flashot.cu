@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "fma_kernels.cuh"
 #include "hvp_kernels.cuh"
+#include "host_internal.h"
 #include "prep_kernels.cuh"
 #include "small_solve.h"
 #include "tc_api.h"
@@ -617,6 +618,14 @@ int begin(int64_t n, int64_t m, int64_t d, int64_t k, int flags, void* ws, size_
 }
 
 }  // namespace
+
+int checked_current_device() {
+  int sms = 0;
+  return current_device(&sms);
+}
+
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 }  // namespace flashot
 
 using namespace flashot;

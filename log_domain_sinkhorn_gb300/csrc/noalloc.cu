@@ -8,46 +8,34 @@
 // fixed array compiled into the library instead of from the caller.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "flashot.h"
+#include "host_internal.h"
 
 namespace {
 
-// The scratch: FLASHOT_NOALLOC_SCRATCH_BYTES of device memory, reserved on every GPU that
-// loads this library for as long as the process lives. In host code `g_noalloc_scratch`
-// only names a host-side shadow of the symbol; its device address comes from
-// cudaGetSymbolAddress (see scratch_for_current_device).
+// The scratch: FLASHOT_NOALLOC_SCRATCH_BYTES of device memory in every context that loads
+// this file's module, held until the context goes away. Its first 4 bytes are the status
+// word of the workspace layout (sticky bounded-wait timeouts); static storage starts it at
+// zero. In host code `g_noalloc_scratch` only names a host-side shadow of the symbol; the
+// device address comes from cudaGetSymbolAddress (scratch_in_current_context).
 constexpr size_t kScratchBytes = FLASHOT_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-struct DeviceScratch {
-  bool ready = false;
-  void* ptr = nullptr;
-};
-DeviceScratch g_scratch[64];
-std::mutex g_scratch_mutex;
-
-// Device address of the scratch array on the current device, looked up once per device
-// (the first call on a device does this set-up, with that device current).
-int scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return FLASHOT_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return FLASHOT_ERR_UNSUPPORTED_DEVICE;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  DeviceScratch& s = g_scratch[dev];
-  if (!s.ready) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return FLASHOT_ERR_CUDA;
-    }
-    s.ptr = p;
-    s.ready = true;
-  }
-  *out = s.ptr;
+// Device address of the scratch array in the current context. The device check comes
+// first: on a GPU other than sm_103 the module has no image to resolve the symbol in.
+// The address is looked up on every call rather than cached, because it belongs to a
+// context, not to a device ordinal: after cudaDeviceReset, or with another context
+// current on the same device, a cached address would point into memory this context does
+// not own. Once the module is loaded the lookup allocates nothing; the first lookup in a
+// context is what loads it (under CUDA's default lazy module loading).
+int scratch_in_current_context(void** out) {
+  const int rc = flashot::checked_current_device();
+  if (rc != FLASHOT_OK) return rc;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return flashot::record_cuda_error(e);
+  if (p == nullptr) return FLASHOT_ERR_CUDA;
+  *out = p;
   return FLASHOT_OK;
 }
 
@@ -57,15 +45,23 @@ extern "C" int flashot_sinkhorn_step_f_noalloc(const float* X, const float* Y, c
                                                const float* g, int64_t n, int64_t m, int64_t d,
                                                float eps, int flags, float* f,
                                                flashot_stream_t stream) {
-  // Only the precision bits are honoured: the shared array may hold another call's data,
-  // so the inputs are always packed afresh.
-  const int prec = flags & FLASHOT_PREC_MASK;
-  const size_t need = flashot_workspace_bytes(n, m, d, 0, prec);
+  // FLASHOT_REUSE_PACK is dropped: the shared array may hold another call's packed
+  // inputs, so they are always packed afresh. Every other flag means what it means for
+  // flashot_sinkhorn_step_f (precision bits, FLASHOT_VALIDATE).
+  const int fl = flags & ~FLASHOT_REUSE_PACK;
+  const size_t need = flashot_workspace_bytes(n, m, d, 0, fl);
   if (need == 0) return FLASHOT_ERR_INVALID_ARG;
   if (need > kScratchBytes) return FLASHOT_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
-  const int rc = scratch_for_current_device(&scratch);
+  const int rc = scratch_in_current_context(&scratch);
   if (rc != FLASHOT_OK) return rc;
-  return flashot_sinkhorn_step_f(X, Y, b, g, n, m, d, eps, prec, f, scratch, kScratchBytes,
+  return flashot_sinkhorn_step_f(X, Y, b, g, n, m, d, eps, fl, f, scratch, kScratchBytes,
                                  stream);
+}
+
+extern "C" int flashot_noalloc_status(flashot_stream_t stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_in_current_context(&scratch);
+  if (rc != FLASHOT_OK) return rc;
+  return flashot_workspace_status(scratch, stream);
 }
