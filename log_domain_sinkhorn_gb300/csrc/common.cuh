@@ -59,12 +59,14 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t v, int64_t T, int64
 }
 
 // How the partials of one LSE pass are laid out: either n_splits fixed splits per row, or
-// (n_splits == 0) stream-K over T = row_tiles * NT tiles (128-row tiles) with G CTAs, where
-// the row tile rt has slots_per_owner * (owner((rt+1)NT-1) - owner(rt NT) + 1) slots.
+// (n_splits == 0) stream-K over T = row_tiles * NT tiles (row tiles of unit_rows rows: 128
+// for single CTAs, 256 for CTA pairs) with G owners (CTAs or CTA pairs), where the row
+// tile rt has slots_per_owner * (owner((rt+1)NT-1) - owner(rt NT) + 1) slots.
 struct SplitInfo {
   int n_splits;
-  int slots_per_owner;  // stream-K: partial slots each owning CTA writes per row tile
+  int slots_per_owner;  // stream-K: partial slots each owner writes per row tile
   int64_t sk_T, sk_G, sk_NT;
+  int unit_rows;        // stream-K: rows per row tile
 };
 
 }  // namespace flashot

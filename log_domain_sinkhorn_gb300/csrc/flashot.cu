@@ -329,7 +329,7 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
   const float* colBias = c.at<float>(x_rows ? c.L.biasF : c.L.biasG);
   float2* partial = c.at<float2>(c.L.partial);
   const float kappa = 2.0f * kLog2e / eps;
-  SplitInfo split{1, 1, 0, 0, 0};
+  SplitInfo split{1, 1, 0, 0, 0, 128};
   int n_splits = 1;
   if (g.prec == FLASHOT_PREC_FP32) {
     const float* rowP = c.at<float>(x_rows ? c.L.xp : c.L.yp);

@@ -90,7 +90,7 @@ __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo
   }
   int n_splits = split.n_splits;
   if (n_splits == 0) {
-    const int64_t rt = i / 128;
+    const int64_t rt = i / split.unit_rows;
     n_splits = split.slots_per_owner *
                (int)(sk_owner((rt + 1) * split.sk_NT - 1, split.sk_T, split.sk_G) -
                      sk_owner(rt * split.sk_NT, split.sk_T, split.sk_G) + 1);

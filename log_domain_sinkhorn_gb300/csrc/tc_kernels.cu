@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 
 #include "flashot.h"
 #include "common.cuh"
@@ -423,6 +424,223 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------------------
+// LSE pass on CTA pairs (long contractions): two CTAs of a cluster run one cta_group::2 MMA
+// per K step, M = 256 rows (128 from each CTA's resident or streamed row tile) x N = 256
+// columns, each CTA holding the K-chunk of 128 of the 256 column points. Per SM this halves
+// the column operand's share of the shared-memory traffic (TMA writes and MMA reads) and of
+// the stage ring, so more stages fit and the tensor pipe is not starved by operand
+// delivery. Each CTA's Tensor Memory receives the scores of its own 128 rows, and its eight
+// epilogue warps run the same online LSE as the single-CTA pass.
+//
+// Units are (256-row pair tile, 256-column tile); the pairs (gridDim.x / 2) split the
+// unit list stream-K. Roles in each CTA: warp 0 lane 0 loads this CTA's operand halves
+// (the byte counts complete on the even CTA's barriers), warp 1 lane 0 of the even CTA
+// issues the MMAs and commits to the barriers of both CTAs, warps 2..9 are the epilogue
+// (their "accumulator drained" arrivals go to the even CTA's barrier). The odd CTA's MMA
+// warp only takes part in the Tensor Memory allocation.
+// ---------------------------------------------------------------------------------------
+template <bool kBF16, bool kARes>
+__global__ void __launch_bounds__(kLseThreads, 1)
+lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
+                int kc_count, int stages, int a_bufs, float kappa, float2* __restrict__ partial,
+                int64_t ld, unsigned* __restrict__ status) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ Ctrl ctl;
+  constexpr int kGroups = 2;               // partial slots per CTA pair and row tile
+  constexpr int kElems = kBF16 ? 64 : 32;  // elements per 128-byte K-chunk row
+  constexpr int kEpiWarps = kLseEpiThreads / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0: the pair's MMA issuer
+  const uint32_t raw = ptx::smem_u32(dyn_smem);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = dyn_smem + (base - raw);
+  const uint32_t a_bytes = kARes ? (uint32_t)kc_count * kChunk : 0u;
+  const uint32_t stage_bytes = kARes ? kChunk : 2u * kChunk;  // [A chunk +] B half chunk
+  const uint32_t b_off = kARes ? 0u : (uint32_t)kChunk;
+  const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
+  const int64_t t_begin = sk_begin(pair, T, G), t_end = sk_begin(pair + 1, T, G);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(&ctl.full[s], 1);
+      ptx::mbar_init(&ctl.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&ctl.acc_full[b], 1);
+      ptx::mbar_init(&ctl.acc_empty[b], 2 * kEpiWarps);  // one lane per epilogue warp, both CTAs
+      ptx::mbar_init(&ctl.a_full[b], 1);
+      ptx::mbar_init(&ctl.a_empty[b], 1);
+    }
+    ptx::mbar_init(&ctl.mma_done, 1);
+    ctl.abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&mapA);
+    ptx::tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(&ctl.tmem_base, kLseTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // both CTAs' barriers initialised and Tensor Memory allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+  auto leader = [&](uint64_t* bar) { return ptx::mapa_shared(ptx::smem_u32(bar), 0u); };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------- TMA producer -------------------------------------
+      uint32_t stage = 0, ph = 0;
+      int64_t issued = 0, segs = 0;
+      bool ok = true;
+      for (int64_t t = t_begin; ok && t < t_end;) {
+        const int64_t rp = t / NT;
+        const int64_t seg_end = min(t_end, (rp + 1) * NT);
+        const int row0 = (int)(rp * 2 * kBM + rank * kBM);  // this CTA's 128 rows
+        if constexpr (kARes) {
+          const int ab = (int)(segs % a_bufs);
+          const uint32_t use = (uint32_t)(segs / a_bufs);
+          if (!ptx::mbar_wait(&ctl.a_empty[ab], (use & 1u) ^ 1u)) { ok = false; break; }
+          if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.a_full[ab], 2u * a_bytes);
+          const uint32_t bar = leader(&ctl.a_full[ab]);
+          for (int kc = 0; kc < kc_count; ++kc)
+            ptx::tma_load_2d_pair(&mapA, bar, smem + (size_t)ab * a_bytes + (size_t)kc * kChunk,
+                                  kc * kElems, row0);
+          ++segs;
+        }
+        for (int64_t tt = t; ok && tt < seg_end; ++tt) {
+          const int col0 = (int)((tt - rp * NT) * kLseBN + rank * kBM);  // this CTA's half
+          for (int kc = 0; kc < kc_count; ++kc) {
+            if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
+            uint8_t* st = smem + (size_t)a_bufs * a_bytes + (size_t)stage * stage_bytes;
+            if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2u * stage_bytes);
+            const uint32_t bar = leader(&ctl.full[stage]);
+            if constexpr (!kARes) ptx::tma_load_2d_pair(&mapA, bar, st, kc * kElems, row0);
+            ptx::tma_load_2d_pair(&mapB, bar, st + b_off, kc * kElems, col0);
+            ++issued;
+            if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
+          }
+        }
+        t = seg_end;
+      }
+      if (!ok) flag_error(ctl, status);
+      if (rank == 0) {
+        // Drain: every copy of both CTAs counted on these barriers has landed.
+        for (int s = 0; s < stages; ++s) {
+          const int64_t arms = issued / stages + (s < issued % stages ? 1 : 0);
+          if (arms > 0) ptx::mbar_wait(&ctl.full[s], (uint32_t)((arms - 1) & 1));
+        }
+        for (int b = 0; b < a_bufs && b < 2; ++b) {
+          const int64_t uses = segs / a_bufs + (b < segs % a_bufs ? 1 : 0);
+          if (uses > 0) ptx::mbar_wait(&ctl.a_full[b], (uint32_t)((uses - 1) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ------------------------------- MMA issuer ----------------------------------------
+      constexpr uint32_t idesc = ptx::make_idesc<kBF16>(2 * kBM, kLseBN);
+      uint32_t stage = 0, ph = 0, ab = 0, acc_ph = 0;
+      int64_t segs = 0;
+      bool ok = true;
+      for (int64_t t = t_begin; ok && t < t_end;) {
+        const int64_t rp = t / NT;
+        const int64_t seg_end = min(t_end, (rp + 1) * NT);
+        const int abuf = kARes ? (int)(segs % a_bufs) : 0;
+        if constexpr (kARes) {
+          if (!ptx::mbar_wait(&ctl.a_full[abuf], (uint32_t)((segs / a_bufs) & 1))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+        }
+        for (int64_t tt = t; ok && tt < seg_end; ++tt) {
+          if (!ptx::mbar_wait_cluster(&ctl.acc_empty[ab], acc_ph ^ 1u)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t d_tmem = tmem + ab * kLseBN;
+          for (int kc = 0; kc < kc_count; ++kc) {
+            if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t st = base + (uint32_t)a_bufs * a_bytes + stage * stage_bytes;
+            const uint32_t a_addr =
+                kARes ? base + (uint32_t)abuf * a_bytes + (uint32_t)kc * kChunk : st;
+            const uint64_t a_desc = ptx::sdesc_k128(a_addr);
+            const uint64_t b_desc = ptx::sdesc_k128(st + b_off);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // K advance: 32 bytes = 2 in the address field
+              ptx::umma_pair<kBF16>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+                                    (kc | kk) != 0 ? 1u : 0u);
+            ptx::umma_commit_pair(&ctl.empty[stage], 0x3);
+            if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
+          }
+          if (!ok) break;
+          ptx::umma_commit_pair(&ctl.acc_full[ab], 0x3);
+          if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+        }
+        if constexpr (kARes) ptx::umma_commit_pair(&ctl.a_empty[abuf], 0x3);
+        ++segs;
+        t = seg_end;
+      }
+      if (!ok) flag_error(ctl, status);
+      // Every MMA issued must have retired before either CTA releases its Tensor Memory.
+      ptx::umma_commit_pair(&ctl.mma_done, 0x1);
+      ptx::mbar_wait(&ctl.mma_done, 0);
+    }
+  } else {
+    // --------------------------------- epilogue ------------------------------------------
+    // Warp w reads TMEM lane quarter (w % 4) (this CTA's rows 32q .. 32q+31) and column half
+    // h = (w - 2) / 4 of every 256-column tile; each (row, half) keeps its own online
+    // (max, sum) and becomes its own partial slot.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t ab = 0, acc_ph = 0;
+    bool ok = true;
+    if (t_begin < t_end && lane < 4)   // 512 B of bias per half-tile: one line per lane
+      ptx::prefetch_l1(colBias + (t_begin % NT) * kLseBN + h * 128 + lane * 32);
+    for (int64_t t = t_begin; ok && t < t_end;) {
+      const int64_t rp = t / NT;
+      const int64_t seg_end = min(t_end, (rp + 1) * NT);
+      float M = kNegBig, S = 0.0f;
+      for (int64_t tt = t; tt < seg_end; ++tt) {
+        const float4* cb =
+            reinterpret_cast<const float4*>(colBias + (tt % NT) * kLseBN + h * 128);
+        if (tt + 1 < t_end && lane < 4)
+          ptx::prefetch_l1(colBias + ((tt + 1) % NT) * kLseBN + h * 128 + lane * 32);
+        if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t taddr = tmem + lane_base + ab * kLseBN + h * 128;
+        float v[64];
+        ptx::tmem_ld_x64_sync(taddr, v);
+        lse_chunk<64, true>(v, cb, kappa, M, S);
+        ptx::tmem_ld_x64_sync(taddr + 64, v);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(leader(&ctl.acc_empty[ab]));
+        if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+        lse_chunk<64, true>(v, cb + 16, kappa, M, S);
+      }
+      if (!ok) break;
+      const int64_t row = rp * 2 * kBM + rank * kBM + q * 32 + lane;
+      const int64_t slot = kGroups * (pair - sk_owner(rp * NT, T, G)) + h;
+      if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
+      t = seg_end;
+    }
+    if (!ok) flag_error(ctl, status);
+  }
+
+  ptx::tc_fence_before();
+  ptx::cluster_sync();  // neither CTA leaves while the pair's MMAs or copies may touch it
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, kLseTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Weighted-sum pass: transport application, barycentric gradient, Hadamard-weighted
 // transport (FlashSinkhorn, SAI replication review, "Summary" (i)-(ii)). Per CTA = (row
 // tile, group of kKV output columns):
@@ -798,6 +1016,18 @@ int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t 
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
 
+// Dynamic shared memory of the pair kernel: the row tile when resident, then as many
+// stages as fit (at least 4); 0 if fewer fit.
+template <bool kARes>
+static int lse_pair_smem(int kc) {
+  const int ctrl = (int)sizeof(Ctrl) + 2 * 4 * (int)sizeof(float);
+  const int a_bytes = kARes ? kc * kChunk : 0;
+  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
+  const int stages = std::min(kMaxStages, (kSmemLimit - ctrl - 1024 - a_bytes) / stage_bytes);
+  if (stages < 4) return 0;
+  return a_bytes + stages * stage_bytes + 1024;
+}
+
 template <bool kBF16, bool kARes, bool kStageBias>
 static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float* colBias,
                       int64_t n_rows, int64_t NT, int64_t T, int kc, int64_t G, float kappa,
@@ -842,6 +1072,77 @@ static int launch_lse(const CUtensorMap& mA, const CUtensorMap& mB, const float*
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
 
+// The CTA-pair pass: cluster launch of 2 CTAs, grid = 2 x pairs.
+template <bool kBF16, bool kARes>
+static int launch_lse_pair(const CUtensorMap& mA, const CUtensorMap& mB, const float* colBias,
+                           int64_t n_rows, int64_t NT, int64_t T, int kc, int64_t pairs,
+                           float kappa, float2* partial, int64_t ld, unsigned* status,
+                           cudaStream_t st) {
+  const int dyn = lse_pair_smem<kARes>(kc);
+  if (dyn <= 0) return FLASHOT_ERR_INVALID_ARG;
+  const int ctrl = (int)sizeof(Ctrl) + 2 * 4 * (int)sizeof(float);
+  const int a_bytes = kARes ? kc * kChunk : 0;
+  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
+  const int stages = std::min(kMaxStages, (kSmemLimit - ctrl - 1024 - a_bytes) / stage_bytes);
+  auto kern = lse_pair_kernel<kBF16, kARes>;
+  int rc = set_smem(kern, dyn);
+  if (rc != FLASHOT_OK) return rc;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_LSE, st);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(kLseThreads);
+    cfg.dynamicSmemBytes = (size_t)dyn;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, 1, kappa,
+                           partial, ld, status) != cudaSuccess)
+      return FLASHOT_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
+
+// How many 2-CTA clusters of the pair kernel can be resident at once (0 if none, or if
+// the query fails); cached per variant.
+template <bool kBF16, bool kARes>
+static int lse_pair_max_clusters(int kc) {
+  static int cached_kc = -1, cached = 0;
+  if (cached_kc == kc) return cached;
+  const int dyn = lse_pair_smem<kARes>(kc);
+  int n = 0;
+  if (dyn > 0) {
+    auto kern = lse_pair_kernel<kBF16, kARes>;
+    if (set_smem(kern, dyn) == FLASHOT_OK) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(kLseThreads);
+      cfg.dynamicSmemBytes = (size_t)dyn;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+    } else {
+      cudaGetLastError();
+    }
+  }
+  cached_kc = kc;
+  cached = n;
+  return n;
+}
+
 int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colBias,
                 int64_t n_rows, int64_t rows_pad, int64_t cols_pad, int64_t dpt, float kappa,
                 float2* partial, int max_splits, int sms, unsigned* status, SplitInfo* info,
@@ -851,22 +1152,53 @@ int tc_lse_pass(bool bf16, const void* rowQ, const void* colQ, const float* colB
   if (rows_pad % kBM != 0 || cols_pad % kLseBN != 0) return FLASHOT_ERR_INVALID_ARG;
   const int64_t row_tiles = rows_pad / kBM, NT = cols_pad / kLseBN;
   const int64_t T = row_tiles * NT;
-  // Two partial slots (column halves) per CTA and row tile.
-  const int64_t G = choose_grid(row_tiles, NT, sms, max_splits / 2);
-  CUtensorMap mA, mB;
-  int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
-  if (rc == FLASHOT_OK) rc = make_map_rows(&mB, colQ, cols_pad, dpt, bf16, kLseBN);
-  if (rc != FLASHOT_OK) return rc;
-  info->n_splits = 0;
-  info->slots_per_owner = 2;
-  info->sk_T = T;
-  info->sk_G = G;
-  info->sk_NT = NT;
   const bool ares = kc * kChunk <= 128 * 1024;
   // Stage the biases in shared memory when the contraction is short (at most 6 K-chunks,
   // e.g. d <= 192 in bf16 or d <= 64 in split tf32: the epilogue bounds the tile, and at
   // least 3 operand stages still fit).
   const bool stage = kc <= 6;
+  CUtensorMap mA, mB;
+  int rc = make_map(&mA, rowQ, rows_pad, dpt, bf16);
+  if (rc != FLASHOT_OK) return rc;
+  info->n_splits = 0;
+  info->slots_per_owner = 2;
+  info->sk_NT = NT;
+  // Long contractions run on CTA pairs (cta_group::2) when 256-row pair tiles divide the rows
+  // and enough 2-CTA clusters fit; FLASHOT_LSE_PAIRS=0 in the environment keeps them on
+  // single CTAs (for comparisons).
+  static const bool pairs_enabled = [] {
+    const char* e = std::getenv("FLASHOT_LSE_PAIRS");
+    return !(e && e[0] == '0');
+  }();
+  if (!stage && pairs_enabled && rows_pad % (2 * kBM) == 0) {
+    const int max_cl = bf16 ? (ares ? lse_pair_max_clusters<true, true>(kc)
+                                    : lse_pair_max_clusters<true, false>(kc))
+                            : (ares ? lse_pair_max_clusters<false, true>(kc)
+                                    : lse_pair_max_clusters<false, false>(kc));
+    const int64_t prt = rows_pad / (2 * kBM);
+    if (max_cl >= std::max(1, sms / 4)) {
+      const int64_t T2 = prt * NT;
+      // Two partial slots (column halves) per pair and pair tile.
+      const int64_t G2 = choose_grid(prt, NT, std::min(max_cl, sms / 2), max_splits / 2);
+      rc = make_map(&mB, colQ, cols_pad, dpt, bf16);
+      if (rc != FLASHOT_OK) return rc;
+      info->sk_T = T2;
+      info->sk_G = G2;
+      info->unit_rows = 2 * kBM;
+#define FLASHOT_LAUNCH_PAIR(BF, AR) \
+  launch_lse_pair<BF, AR>(mA, mB, colBias, n_rows, NT, T2, kc, G2, kappa, partial, rows_pad, status, st)
+      if (bf16) return ares ? FLASHOT_LAUNCH_PAIR(true, true) : FLASHOT_LAUNCH_PAIR(true, false);
+      return ares ? FLASHOT_LAUNCH_PAIR(false, true) : FLASHOT_LAUNCH_PAIR(false, false);
+#undef FLASHOT_LAUNCH_PAIR
+    }
+  }
+  // Two partial slots (column halves) per CTA and row tile.
+  const int64_t G = choose_grid(row_tiles, NT, sms, max_splits / 2);
+  rc = make_map_rows(&mB, colQ, cols_pad, dpt, bf16, kLseBN);
+  if (rc != FLASHOT_OK) return rc;
+  info->sk_T = T;
+  info->sk_G = G;
+  info->unit_rows = kBM;
 #define FLASHOT_LAUNCH_LSE(BF, AR, SB)                                                        \
   launch_lse<BF, AR, SB>(mA, mB, colBias, n_rows, NT, T, kc, G, kappa, partial, rows_pad, \
                          status, st)
