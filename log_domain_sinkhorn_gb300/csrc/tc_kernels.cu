@@ -429,21 +429,23 @@ lse_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ 
 // columns, each CTA holding the K-chunk of 128 of the 256 column points. Per SM this halves
 // the column operand's share of the shared-memory traffic (TMA writes and MMA reads) and of
 // the stage ring, so more stages fit and the tensor pipe is not starved by operand
-// delivery. Each CTA's Tensor Memory receives the scores of its own 128 rows, and its eight
-// epilogue warps run the same online LSE as the single-CTA pass.
+// delivery; a stage carries two K-chunks when the contraction has an even number of them,
+// which halves the barrier and commit traffic per MMA. Each CTA's Tensor Memory receives
+// the scores of its own 128 rows, and its eight epilogue warps run the same online LSE as
+// the single-CTA pass.
 //
 // Units are (256-row pair tile, 256-column tile); the pairs (gridDim.x / 2) split the
 // unit list stream-K. Roles in each CTA: warp 0 lane 0 loads this CTA's operand halves
 // (the byte counts complete on the even CTA's barriers), warp 1 lane 0 of the even CTA
 // issues the MMAs and commits to the barriers of both CTAs, warps 2..9 are the epilogue
-// (their "accumulator drained" arrivals go to the even CTA's barrier). The odd CTA's MMA
-// warp only takes part in the Tensor Memory allocation.
+// (local arrivals on "accumulator drained"; in the odd CTA, lane 0 of the MMA warp forwards
+// them to the even CTA's barrier once all eight warps have arrived).
 // ---------------------------------------------------------------------------------------
 template <bool kBF16, bool kARes>
 __global__ void __launch_bounds__(kLseThreads, 1)
 lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const float* __restrict__ colBias, int64_t n_rows, int64_t NT, int64_t T,
-                int kc_count, int stages, int a_bufs, float kappa, float2* __restrict__ partial,
+                int kc_count, int stages, int kps, float kappa, float2* __restrict__ partial,
                 int64_t ld, unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ Ctrl ctl;
@@ -456,8 +458,12 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = dyn_smem + (base - raw);
   const uint32_t a_bytes = kARes ? (uint32_t)kc_count * kChunk : 0u;
-  const uint32_t stage_bytes = kARes ? kChunk : 2u * kChunk;  // [A chunk +] B half chunk
+  // A stage holds kps K-chunks, each [A chunk +] B half chunk.
+  const uint32_t chunk_bytes = kARes ? kChunk : 2u * kChunk;
+  const uint32_t stage_bytes = (uint32_t)kps * chunk_bytes;
   const uint32_t b_off = kARes ? 0u : (uint32_t)kChunk;
+  const uint32_t abase = base;  // the resident row tile (one buffer)
+  const uint32_t sbase = base + a_bytes;
   const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
   const int64_t t_begin = sk_begin(pair, T, G), t_end = sk_begin(pair + 1, T, G);
 
@@ -468,7 +474,8 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&ctl.acc_full[b], 1);
-      ptx::mbar_init(&ctl.acc_empty[b], 2 * kEpiWarps);  // one lane per epilogue warp, both CTAs
+      // One lane per local epilogue warp; the even CTA's also counts the odd CTA's forwarder.
+      ptx::mbar_init(&ctl.acc_empty[b], kEpiWarps + (rank == 0 ? 1 : 0));
       ptx::mbar_init(&ctl.a_full[b], 1);
       ptx::mbar_init(&ctl.a_empty[b], 1);
     }
@@ -501,25 +508,26 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         const int64_t seg_end = min(t_end, (rp + 1) * NT);
         const int row0 = (int)(rp * 2 * kBM + rank * kBM);  // this CTA's 128 rows
         if constexpr (kARes) {
-          const int ab = (int)(segs % a_bufs);
-          const uint32_t use = (uint32_t)(segs / a_bufs);
-          if (!ptx::mbar_wait(&ctl.a_empty[ab], (use & 1u) ^ 1u)) { ok = false; break; }
-          if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.a_full[ab], 2u * a_bytes);
-          const uint32_t bar = leader(&ctl.a_full[ab]);
+          if (!ptx::mbar_wait(&ctl.a_empty[0], ((uint32_t)segs & 1u) ^ 1u)) { ok = false; break; }
+          if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.a_full[0], 2u * a_bytes);
+          const uint32_t bar = leader(&ctl.a_full[0]);
           for (int kc = 0; kc < kc_count; ++kc)
-            ptx::tma_load_2d_pair(&mapA, bar, smem + (size_t)ab * a_bytes + (size_t)kc * kChunk,
-                                  kc * kElems, row0);
+            ptx::tma_load_2d_pair(&mapA, bar, smem + (size_t)kc * kChunk, kc * kElems, row0);
           ++segs;
         }
         for (int64_t tt = t; ok && tt < seg_end; ++tt) {
           const int col0 = (int)((tt - rp * NT) * kLseBN + rank * kBM);  // this CTA's half
-          for (int kc = 0; kc < kc_count; ++kc) {
+          for (int kc = 0; kc < kc_count; kc += kps) {
             if (!ptx::mbar_wait(&ctl.empty[stage], ph ^ 1u)) { ok = false; break; }
-            uint8_t* st = smem + (size_t)a_bufs * a_bytes + (size_t)stage * stage_bytes;
+            uint8_t* st = smem + (size_t)a_bytes + (size_t)stage * stage_bytes;
             if (rank == 0) ptx::mbar_arrive_expect_tx(&ctl.full[stage], 2u * stage_bytes);
             const uint32_t bar = leader(&ctl.full[stage]);
-            if constexpr (!kARes) ptx::tma_load_2d_pair(&mapA, bar, st, kc * kElems, row0);
-            ptx::tma_load_2d_pair(&mapB, bar, st + b_off, kc * kElems, col0);
+            for (int c2 = 0; c2 < kps; ++c2) {
+              uint8_t* cst = st + (size_t)c2 * chunk_bytes;
+              if constexpr (!kARes)
+                ptx::tma_load_2d_pair(&mapA, bar, cst, (kc + c2) * kElems, row0);
+              ptx::tma_load_2d_pair(&mapB, bar, cst + b_off, (kc + c2) * kElems, col0);
+            }
             ++issued;
             if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
           }
@@ -533,10 +541,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           const int64_t arms = issued / stages + (s < issued % stages ? 1 : 0);
           if (arms > 0) ptx::mbar_wait(&ctl.full[s], (uint32_t)((arms - 1) & 1));
         }
-        for (int b = 0; b < a_bufs && b < 2; ++b) {
-          const int64_t uses = segs / a_bufs + (b < segs % a_bufs ? 1 : 0);
-          if (uses > 0) ptx::mbar_wait(&ctl.a_full[b], (uint32_t)((uses - 1) & 1));
-        }
+        if (segs > 0) ptx::mbar_wait(&ctl.a_full[0], (uint32_t)((segs - 1) & 1));
       }
     }
   } else if (warp == 1) {
@@ -549,30 +554,28 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       for (int64_t t = t_begin; ok && t < t_end;) {
         const int64_t rp = t / NT;
         const int64_t seg_end = min(t_end, (rp + 1) * NT);
-        const int abuf = kARes ? (int)(segs % a_bufs) : 0;
         if constexpr (kARes) {
-          if (!ptx::mbar_wait(&ctl.a_full[abuf], (uint32_t)((segs / a_bufs) & 1))) {
-            ok = false;
-            break;
-          }
+          if (!ptx::mbar_wait(&ctl.a_full[0], (uint32_t)(segs & 1))) { ok = false; break; }
           ptx::tc_fence_after();
         }
         for (int64_t tt = t; ok && tt < seg_end; ++tt) {
           if (!ptx::mbar_wait_cluster(&ctl.acc_empty[ab], acc_ph ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t d_tmem = tmem + ab * kLseBN;
-          for (int kc = 0; kc < kc_count; ++kc) {
+          for (int kc = 0; kc < kc_count; kc += kps) {
             if (!ptx::mbar_wait(&ctl.full[stage], ph)) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t st = base + (uint32_t)a_bufs * a_bytes + stage * stage_bytes;
-            const uint32_t a_addr =
-                kARes ? base + (uint32_t)abuf * a_bytes + (uint32_t)kc * kChunk : st;
-            const uint64_t a_desc = ptx::sdesc_k128(a_addr);
-            const uint64_t b_desc = ptx::sdesc_k128(st + b_off);
+            const uint32_t st = sbase + stage * stage_bytes;
+            for (int c2 = 0; c2 < kps; ++c2) {
+              const uint32_t cst = st + (uint32_t)c2 * chunk_bytes;
+              const uint32_t a_addr = kARes ? abase + (uint32_t)(kc + c2) * kChunk : cst;
+              const uint64_t a_desc = ptx::sdesc_k128(a_addr);
+              const uint64_t b_desc = ptx::sdesc_k128(cst + b_off);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // K advance: 32 bytes = 2 in the address field
-              ptx::umma_pair<kBF16>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
-                                    (kc | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)  // K advance: 32 bytes = 2 in the address field
+                ptx::umma_pair<kBF16>(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc,
+                                      (kc | c2 | kk) != 0 ? 1u : 0u);
+            }
             ptx::umma_commit_pair(&ctl.empty[stage], 0x3);
             if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
           }
@@ -580,7 +583,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           ptx::umma_commit_pair(&ctl.acc_full[ab], 0x3);
           if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
         }
-        if constexpr (kARes) ptx::umma_commit_pair(&ctl.a_empty[abuf], 0x3);
+        if constexpr (kARes) ptx::umma_commit_pair(&ctl.a_empty[0], 0x3);
         ++segs;
         t = seg_end;
       }
@@ -588,6 +591,21 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       // Every MMA issued must have retired before either CTA releases its Tensor Memory.
       ptx::umma_commit_pair(&ctl.mma_done, 0x1);
       ptx::mbar_wait(&ctl.mma_done, 0);
+    } else if (lane == 0) {
+      // --------------------- odd CTA: accumulator-drained forwarder ------------------------
+      // Once this CTA's eight epilogue warps have read an accumulator (local arrivals), one
+      // arrival at cluster scope tells the even CTA's MMA issuer; the epilogue warps never
+      // wait on a cluster-scope release themselves.
+      uint32_t ab = 0, acc_ph = 0;
+      bool ok = true;
+      for (int64_t tt = t_begin; tt < t_end; ++tt) {
+        if (!ptx::mbar_wait(&ctl.acc_empty[ab], acc_ph)) { ok = false; break; }
+        ptx::tc_fence_after();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive_cluster(leader(&ctl.acc_empty[ab]));
+        if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
+      }
+      if (!ok) flag_error(ctl, status);
     }
   } else {
     // --------------------------------- epilogue ------------------------------------------
@@ -619,7 +637,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         ptx::tmem_ld_x64_sync(taddr + 64, v);
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(leader(&ctl.acc_empty[ab]));
+        if (lane == 0) ptx::mbar_arrive(&ctl.acc_empty[ab]);
         if (++ab == 2) { ab = 0; acc_ph ^= 1u; }
         lse_chunk<64, true>(v, cb + 16, kappa, M, S);
       }
@@ -1018,14 +1036,26 @@ int tc_pack_inputs(int mode, const float* X, const float* Y, int64_t n, int64_t 
 
 // Dynamic shared memory of the pair kernel: the row tile when resident, then as many
 // stages as fit (at least 4); 0 if fewer fit.
+// Shared-memory plan of the pair kernel: the row tile when resident, then a ring of stages
+// of kps K-chunks. Two chunks per stage when the chunk count is even and at least three
+// such stages fit; else one chunk per stage and at least four stages. Returns the dynamic
+// shared memory (0 if no plan fits) and sets *stages and *kps.
 template <bool kARes>
-static int lse_pair_smem(int kc) {
+static int lse_pair_smem(int kc, int* stages_out = nullptr, int* kps_out = nullptr) {
   const int ctrl = (int)sizeof(Ctrl) + 2 * 4 * (int)sizeof(float);
   const int a_bytes = kARes ? kc * kChunk : 0;
-  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
-  const int stages = std::min(kMaxStages, (kSmemLimit - ctrl - 1024 - a_bytes) / stage_bytes);
-  if (stages < 4) return 0;
-  return a_bytes + stages * stage_bytes + 1024;
+  const int chunk_bytes = kARes ? kChunk : 2 * kChunk;
+  const int room = kSmemLimit - ctrl - 1024 - a_bytes;
+  int kps = 1, stages = std::min(kMaxStages, room / chunk_bytes);
+  if (kc % 2 == 0 && room / (2 * chunk_bytes) >= 3) {
+    kps = 2;
+    stages = std::min(kMaxStages, room / (2 * chunk_bytes));
+  } else if (stages < 4) {
+    return 0;
+  }
+  if (stages_out) *stages_out = stages;
+  if (kps_out) *kps_out = kps;
+  return a_bytes + stages * kps * chunk_bytes + 1024;
 }
 
 template <bool kBF16, bool kARes, bool kStageBias>
@@ -1078,12 +1108,9 @@ static int launch_lse_pair(const CUtensorMap& mA, const CUtensorMap& mB, const f
                            int64_t n_rows, int64_t NT, int64_t T, int kc, int64_t pairs,
                            float kappa, float2* partial, int64_t ld, unsigned* status,
                            cudaStream_t st) {
-  const int dyn = lse_pair_smem<kARes>(kc);
+  int stages = 0, kps = 1;
+  const int dyn = lse_pair_smem<kARes>(kc, &stages, &kps);
   if (dyn <= 0) return FLASHOT_ERR_INVALID_ARG;
-  const int ctrl = (int)sizeof(Ctrl) + 2 * 4 * (int)sizeof(float);
-  const int a_bytes = kARes ? kc * kChunk : 0;
-  const int stage_bytes = kARes ? kChunk : 2 * kChunk;
-  const int stages = std::min(kMaxStages, (kSmemLimit - ctrl - 1024 - a_bytes) / stage_bytes);
   auto kern = lse_pair_kernel<kBF16, kARes>;
   int rc = set_smem(kern, dyn);
   if (rc != FLASHOT_OK) return rc;
@@ -1101,7 +1128,7 @@ static int launch_lse_pair(const CUtensorMap& mA, const CUtensorMap& mB, const f
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, 1, kappa,
+    if (cudaLaunchKernelEx(&cfg, kern, mA, mB, colBias, n_rows, NT, T, kc, stages, kps, kappa,
                            partial, ld, status) != cudaSuccess)
       return FLASHOT_ERR_CUDA;
   }
