@@ -1064,6 +1064,7 @@ def run_gpu(args):
             "score_evals_per_s": scores_per_step * args.steps * world / (ms32 / 1e3),
             "roofline": {"bound": "tensor", "achieved": ach32, "peak": pk32,
                          "unit": "TFLOP/s", "frac": ach32 / pk32,
+                         "traffic": profiled_traffic("tf32"),
                          "frac_clock_matched": clock_matched(ach32 / pk32, clk32.get("sm_mhz"),
                                                              pk32_mhz),
                          "peak_clock_mhz": pk32_mhz, "avg_launch_ms": avg32,

@@ -397,13 +397,21 @@ int run_lse_pass(const Ctx& c, bool x_rows, float eps, float eps_next, float* ou
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(
-        &cfg, lse_combine_kernel, (const float2*)partial, split, (int64_t)rows_pad, n_rows,
-        (int64_t)rows_pad, (const float*)c.at<float>(x_rows ? c.L.alpha : c.L.beta), eps,
-        (const float*)c.at<float>(x_rows ? c.L.la2 : c.L.lb2), eps / eps_next, out_pot,
-        write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : (float*)nullptr,
-        out_lse2, average ? 1 : 0, (const float*)c.at<float>(x_rows ? c.L.wa : c.L.wb),
-        err_rows);
+    CombineArgs args;
+    args.rows = n_rows;
+    args.rows_pad = rows_pad;
+    args.norms = c.at<float>(x_rows ? c.L.alpha : c.L.beta);
+    args.eps = eps;
+    args.lw2 = c.at<float>(x_rows ? c.L.la2 : c.L.lb2);
+    args.eps_ratio = eps / eps_next;
+    args.out_pot = out_pot;
+    args.next_bias = write_next_bias ? c.at<float>(x_rows ? c.L.biasG : c.L.biasF) : nullptr;
+    args.out_lse2 = out_lse2;
+    args.average = average ? 1 : 0;
+    args.err_w = c.at<float>(x_rows ? c.L.wa : c.L.wb);
+    args.err_rows = err_rows;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lse_combine_kernel, (const float2*)partial, split,
+                                       (int64_t)rows_pad, args);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return launch_check();

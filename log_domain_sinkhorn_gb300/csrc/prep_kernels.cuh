@@ -5,6 +5,7 @@
 // replication review, "Weaknesses": cost of the form c_ij = alpha_i + beta_j - Q_i^T K_j).
 #pragma once
 
+#include "combine.cuh"
 #include "common.cuh"
 #include "pack_kernels.cuh"
 
@@ -60,59 +61,16 @@ __global__ void bias_kernel(const float* __restrict__ pot, const float* __restri
   }
 }
 
-// Merge per-split (max, sum) partials of the base-2 LSE and finish the half-step:
-//   L_i  = M + log2 S,   pot_i = norm_i - eps ln2 L_i   (averaged with the previous out_pot
-//   when `average` is set: the symmetric schedule),
-//   next_bias_i = lw2_i - L_i * (eps / eps_next)   (= (pot_i - norm_i) log2e/eps_next + lw2_i)
-// next_bias is the bias the following pass (the other side's update at eps_next) needs;
-// its padding entries [rows, rows_pad) are set to -inf so padded points carry no mass.
-// err_rows != NULL (the convergence check): before out_pot is overwritten, the row's share
-// of the L1 marginal error of the previous iterate,
-//   err_rows_i = w_i |exp((old_i - new_i) / eps) - 1|  (= |sum_j P_ij(old) - w_i|),
-// is written, with 0 for padding rows.
+// Merge per-split (max, sum) partials of the base-2 LSE and finish the half-step (see
+// combine_row): one thread per row of rows_pad.
 __global__ void lse_combine_kernel(const float2* __restrict__ partial, SplitInfo split,
-                                   int64_t ld, int64_t rows, int64_t rows_pad,
-                                   const float* __restrict__ norms, float eps,
-                                   const float* __restrict__ lw2, float eps_ratio,
-                                   float* __restrict__ out_pot, float* __restrict__ next_bias,
-                                   float* __restrict__ out_lse2, int average,
-                                   const float* __restrict__ err_w = nullptr,
-                                   float* __restrict__ err_rows = nullptr) {
+                                   int64_t ld, CombineArgs args) {
   // Launched as a programmatic dependent of the LSE pass: everything below reads its
   // partials, so wait for it first; the next pass may then start its own prologue.
   griddep_wait();
   griddep_launch_dependents();
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i >= rows) {
-    if (i < rows_pad && next_bias) next_bias[i] = neg_inf();
-    if (i < rows_pad && err_rows) err_rows[i] = 0.0f;
-    return;
-  }
-  int n_splits = split.n_splits;
-  if (n_splits == 0) {
-    const int64_t rt = i / split.unit_rows;
-    n_splits = split.slots_per_owner *
-               (int)(sk_owner((rt + 1) * split.sk_NT - 1, split.sk_T, split.sk_G) -
-                     sk_owner(rt * split.sk_NT, split.sk_T, split.sk_G) + 1);
-  }
-  float M = kNegBig;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, partial[s * ld + i].x);
-  float S = 0.0f;
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 p = partial[s * ld + i];
-    S += p.y * ex2(p.x - M);
-  }
-  const float L = M + log2f(S);  // S == 0 (no mass) gives -inf, so pot = +inf
-  const float fresh = norms[i] - eps * kLn2 * L;
-  // Symmetric schedule: the new potential is the mean of the previous one and the update.
-  const float pot = average ? 0.5f * (out_pot[i] + fresh) : fresh;
-  if (err_rows) {
-    const float w = err_w[i];
-    err_rows[i] = w > 0.0f ? w * fabsf(expm1f((out_pot[i] - fresh) / eps)) : 0.0f;
-  }
-  if (out_pot) out_pot[i] = pot;
-  if (next_bias) next_bias[i] = lw2[i] - L * eps_ratio;
-  if (out_lse2) out_lse2[i] = L;
+  if (i < args.rows_pad) combine_row(partial, ld, split, i, args);
 }
 
 // Input check (FLASHOT_VALIDATE): bit 1 of *flag if a coordinate of X or Y is not finite,
