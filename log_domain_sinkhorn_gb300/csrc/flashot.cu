@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <cstdlib>
 
 #include "flashot.h"
 #include "common.cuh"
@@ -19,6 +20,7 @@
 #include "prep_kernels.cuh"
 #include "small_solve.h"
 #include "tc_api.h"
+#include "tc_wsum_pair.h"
 #include "trace.h"
 #include <vector>
 
@@ -190,11 +192,16 @@ Layout make_layout(const Geometry& g) {
   // of the tensor-core weighted sums (V^T for apply, Y^T for the gradient), padded to
   // multiples of 256 output columns.
   if (g.prec != FLASHOT_PREC_FP32)
-    L.vtq = take((size_t)std::max(round_up(g.k, 256), round_up(g.d, 256)) * std::max(np, mp) *
-                 g.es);
-  // Partial sums of the bf16 weighted-sum pass (stream-K over 128 x 256 tiles).
-  if (g.prec == FLASHOT_PREC_BF16)
-    L.wsp = take(tc_wsum2_scratch_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)));
+    L.vtq = take(std::max((size_t)std::max(round_up(g.k, 256), round_up(g.d, 256)) *
+                              std::max(np, mp) * g.es,
+                          tc_wsum_pair_vt_bytes(g.prec, (int64_t)std::max(np, mp),
+                                                std::max(g.k, g.d))));
+  // Partial sums of the stream-K weighted-sum passes (bf16 single-CTA, and the CTA-pair pass
+  // of every tensor-core precision).
+  if (g.prec != FLASHOT_PREC_FP32)
+    L.wsp = take(std::max(tc_wsum2_scratch_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)),
+                          tc_wsum_pair_scratch_bytes((int64_t)std::max(np, mp),
+                                                     std::max(g.k, g.d))));
   // Partial sums of the tf32 weighted-sum passes' column splits.
   if (g.prec == FLASHOT_PREC_TF32 || g.prec == FLASHOT_PREC_TF32X3)
     L.tsp = take(tc_wsum_split_bytes((int64_t)std::max(np, mp), std::max(g.k, g.d)));
@@ -439,6 +446,18 @@ int run_wsum_pass(const Ctx& c, int mode, bool transpose, float eps, const float
       ldv = g.d;
       k = g.d;
     }
+    // CTA pairs unless FLASHOT_WSUM_PAIRS=0 in the environment (single-CTA kernels, for
+    // comparisons) or too few 2-CTA clusters fit.
+    static const bool pairs_enabled = [] {
+      const char* e = std::getenv("FLASHOT_WSUM_PAIRS");
+      return !(e && e[0] == '0');
+    }();
+    if (pairs_enabled && tc_wsum_pair_available(c.sms))
+      return tc_wsum_pair_pass(g.prec, mode, c.at<void>(x_rows ? c.L.xq : c.L.yq),
+                               c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows,
+                               n_cols, x_rows ? g.n_pad : g.m_pad, cols_pad, g.d, g.dpt, kappa,
+                               V, ldv, k, c.at<void>(c.L.vtq), c.at<void>(c.L.wsp), rowW, X,
+                               out, ldo, c.sms, c.at<unsigned>(c.L.status), c.st);
     if (g.prec == FLASHOT_PREC_BF16)
       return tc_wsum2_pass(mode, c.at<void>(x_rows ? c.L.xq : c.L.yq),
                            c.at<void>(x_rows ? c.L.yq : c.L.xq), colBias, rowBias, n_rows, n_cols,

@@ -18,9 +18,13 @@ LOSS_TOL = {"fp32": 1e-4, "tf32": 1e-4, "tf32x3": 1e-4, "bf16": 2e-3}
 # plan entry, plus u/sqrt(3) from rounding the weights for the second contraction; against
 # a random-sign V these do not average out. For the d = 1024, eps = 0.1 workload this
 # predicts a max error of ~4e-4 (tf32) and ~1.6e-3 (bf16) relative to max|P V|; the
-# bounds below are 2.5x that. The fp32 path keeps 1e-4.
-# tf32x3 splits only the score operands; its second contraction is single tf32.
-OUT_TOL = {"fp32": 1e-4, "tf32": 1e-3, "tf32x3": 1e-3, "bf16": 4e-3}
+# bounds below are 2.5x that. The fp32 path keeps 1e-4. Split tf32 splits both
+# contractions (the scores' operands, and W = W_hi + W_lo, V = V_hi + V_lo in the second),
+# so it is held to the fp32 bar too.
+OUT_TOL = {"fp32": 1e-4, "tf32": 1e-3, "tf32x3": 1e-4, "bf16": 4e-3}
+# The single-CTA tf32 kernels (FLASHOT_WSUM_PAIRS=0) split only the score operands: their
+# second contraction is single tf32, held to the tf32 bar.
+OUT_TOL_SINGLE_CTA = {"fp32": 1e-4, "tf32": 1e-3, "tf32x3": 1e-3, "bf16": 4e-3}
 
 
 def to_dev(arr):
@@ -60,8 +64,9 @@ def pot_err(f, g, f_ref, g_ref):
 # lo.hi, dropped terms ~2^-22) the bound is set by fp32 accumulation over up to ~3d terms,
 # taken as 2^-20.
 OPERAND_U = {"fp32": 2.0 ** -20, "tf32": 2.0 ** -11, "tf32x3": 2.0 ** -20, "bf16": 2.0 ** -9}
-# Rounding of the second contraction's operands (plan weights and V) in apply / gradient.
-SECOND_U = {"fp32": 2.0 ** -24, "tf32": 2.0 ** -11, "tf32x3": 2.0 ** -11, "bf16": 2.0 ** -9}
+# Rounding of the second contraction's operands (plan weights and V) in apply / gradient:
+# split tf32 rounds only W_lo = W - tf32(W) (to bf16) and drops W_lo V_lo, ~2^-20 of W.
+SECOND_U = {"fp32": 2.0 ** -24, "tf32": 2.0 ** -11, "tf32x3": 2.0 ** -20, "bf16": 2.0 ** -9}
 
 
 def half_step_bound(precision, P, Q, eps, ref):

@@ -61,9 +61,13 @@ def test_workspace_bytes_host_logic(lib):
     assert wb(10, 10, 3, 0, 0x7) == 0  # unknown precision code
     small = wb(512, 512, 3, 0, 1)
     assert small > 0
-    # O((n + m) d) memory: the n x m matrix is never stored.
+    # O((n + m) d) memory: the n x m matrix is never stored. Terms: the packed clouds, the
+    # LSE partials (64 float2 per row), the weighted sums' stream-K partials (4 owners x
+    # rows x output columns), the V^T planes of the split second contraction (10 bytes per
+    # element) and 64 MiB of fixed buffers.
     big = wb(50000, 50000, 512, 0, 2)
-    assert big < 2 * (50000 + 50000) * 512 * 4 + 64 * 100000 * 8 + (1 << 24)
+    assert big < (2 * (50000 + 50000) * 512 * 4 + 64 * 100000 * 8 + 4 * 50176 * 512 * 4
+                  + 50176 * 512 * 10 + (1 << 26))
     assert big > (50000 + 50000) * 512 * 4  # holds the packed clouds
     # Apply width k grows the workspace only on the tensor-core paths (V^T packing).
     assert wb(1000, 1000, 64, 512, 2) > wb(1000, 1000, 64, 0, 2)
