@@ -58,6 +58,27 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t v, int64_t T, int64
   return ((v + 1) * G + T - 1) / T - 1;
 }
 
+// The row-tile segments of a stream-K range [tb, te) of row-tile-major units (NT units per
+// row tile), in the order the CTA-pair passes walk them: the last segment (the head of the
+// last row tile, columns from 0) first, then the others in order. Every owner's range then
+// starts at column 0 and, after its first segment, runs about T/G mod NT columns behind,
+// so the owners sweep the column tiles nearly in step: each column tile is read by all of
+// them within a short window, and the column operand's L2 working set stays a few tiles
+// instead of the whole cloud (a row-major walk spreads the owners' columns over all of
+// it). The segments and their partial slots are those of the row-major walk.
+struct SegOrder {
+  int64_t tb, te, NT, v0, n;
+  __device__ __forceinline__ SegOrder(int64_t tb_, int64_t te_, int64_t nt)
+      : tb(tb_), te(te_), NT(nt), v0(tb_ / nt), n(te_ > tb_ ? (te_ - 1) / nt - tb_ / nt + 1 : 0) {}
+  // Segment i (0 <= i < n) as the unit range [a, b) of one row tile.
+  __device__ __forceinline__ void get(int64_t i, int64_t& a, int64_t& b) const {
+    const int64_t j = n >= 2 ? (i == 0 ? n - 1 : i - 1) : i;
+    const int64_t v = v0 + j;
+    a = tb > v * NT ? tb : v * NT;
+    b = te < (v + 1) * NT ? te : (v + 1) * NT;
+  }
+};
+
 // How the partials of one LSE pass are laid out: either n_splits fixed splits per row, or
 // (n_splits == 0) stream-K over T = row_tiles * NT tiles (row tiles of unit_rows rows: 128
 // for single CTAs, 256 for CTA pairs) with G owners (CTAs or CTA pairs), where the row

@@ -466,6 +466,7 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const uint32_t sbase = base + a_bytes;
   const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
   const int64_t t_begin = sk_begin(pair, T, G), t_end = sk_begin(pair + 1, T, G);
+  const SegOrder so(t_begin, t_end, NT);  // every role walks the segments in this order
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -503,9 +504,10 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       uint32_t stage = 0, ph = 0;
       int64_t issued = 0, segs = 0;
       bool ok = true;
-      for (int64_t t = t_begin; ok && t < t_end;) {
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+        int64_t t, seg_end;
+        so.get(i, t, seg_end);
         const int64_t rp = t / NT;
-        const int64_t seg_end = min(t_end, (rp + 1) * NT);
         const int row0 = (int)(rp * 2 * kBM + rank * kBM);  // this CTA's 128 rows
         if constexpr (kARes) {
           if (!ptx::mbar_wait(&ctl.a_empty[0], ((uint32_t)segs & 1u) ^ 1u)) { ok = false; break; }
@@ -532,7 +534,6 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             if (++stage == (uint32_t)stages) { stage = 0; ph ^= 1u; }
           }
         }
-        t = seg_end;
       }
       if (!ok) flag_error(ctl, status);
       if (rank == 0) {
@@ -551,9 +552,9 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       uint32_t stage = 0, ph = 0, ab = 0, acc_ph = 0;
       int64_t segs = 0;
       bool ok = true;
-      for (int64_t t = t_begin; ok && t < t_end;) {
-        const int64_t rp = t / NT;
-        const int64_t seg_end = min(t_end, (rp + 1) * NT);
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+        int64_t t, seg_end;
+        so.get(i, t, seg_end);
         if constexpr (kARes) {
           if (!ptx::mbar_wait(&ctl.a_full[0], (uint32_t)(segs & 1))) { ok = false; break; }
           ptx::tc_fence_after();
@@ -585,7 +586,6 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         }
         if constexpr (kARes) ptx::umma_commit_pair(&ctl.a_empty[0], 0x3);
         ++segs;
-        t = seg_end;
       }
       if (!ok) flag_error(ctl, status);
       // Every MMA issued must have retired before either CTA releases its Tensor Memory.
@@ -617,16 +617,20 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t ab = 0, acc_ph = 0;
     bool ok = true;
-    if (t_begin < t_end && lane < 4)   // 512 B of bias per half-tile: one line per lane
-      ptx::prefetch_l1(colBias + (t_begin % NT) * kLseBN + h * 128 + lane * 32);
-    for (int64_t t = t_begin; ok && t < t_end;) {
+    if (so.n > 0 && lane < 4) {  // 512 B of bias per half-tile: one line per lane
+      int64_t t0, t1;
+      so.get(0, t0, t1);
+      ptx::prefetch_l1(colBias + (t0 % NT) * kLseBN + h * 128 + lane * 32);
+    }
+    for (int64_t i = 0; ok && i < so.n; ++i) {
+      int64_t t, seg_end;
+      so.get(i, t, seg_end);
       const int64_t rp = t / NT;
-      const int64_t seg_end = min(t_end, (rp + 1) * NT);
       float M = kNegBig, S = 0.0f;
       for (int64_t tt = t; tt < seg_end; ++tt) {
         const float4* cb =
             reinterpret_cast<const float4*>(colBias + (tt % NT) * kLseBN + h * 128);
-        if (tt + 1 < t_end && lane < 4)
+        if (tt + 1 < seg_end && lane < 4)  // the next tile of the segment (a hint only)
           ptx::prefetch_l1(colBias + ((tt + 1) % NT) * kLseBN + h * 128 + lane * 32);
         if (!ptx::mbar_wait(&ctl.acc_full[ab], acc_ph)) { ok = false; break; }
         ptx::tc_fence_after();
@@ -645,7 +649,6 @@ lse_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       const int64_t row = rp * 2 * kBM + rank * kBM + q * 32 + lane;
       const int64_t slot = kGroups * (pair - sk_owner(rp * NT, T, G)) + h;
       if (row < n_rows) partial[slot * ld + row] = make_float2(M, S);
-      t = seg_end;
     }
     if (!ok) flag_error(ctl, status);
   }

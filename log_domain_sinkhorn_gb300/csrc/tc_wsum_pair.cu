@@ -124,6 +124,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
   const uint32_t v_base = (uint32_t)n_st * stage_bytes;
   const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
   const int64_t t_begin = sk_begin(pair, T, G), t_end = sk_begin(pair + 1, T, G);
+  const SegOrder so(t_begin, t_end, NT);  // every role walks the segments in this order
   auto leader = [&](uint64_t* bar) { return ptx::mapa_shared(ptx::smem_u32(bar), 0u); };
   // Barriers that the odd CTA's epilogue arrivals reach through a forwarder: local count 8,
   // plus the forwarder's one arrival in the even CTA.
@@ -171,7 +172,10 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
       uint32_t stage = 0, ph = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int64_t t = t_begin; ok && t < t_end; ++t) {
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+       int64_t ta, tb;
+       so.get(i, ta, tb);
+       for (int64_t t = ta; ok && t < tb; ++t) {
         const int64_t vr = t / NT;
         const int64_t jt = t - vr * NT;
         const int64_t rp = vr % pair_tiles;
@@ -190,6 +194,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
           ++issued;
           if (++stage == (uint32_t)n_st) { stage = 0; ph ^= 1u; }
         }
+       }
       }
       if (!ok) flag_error(ctl, status);
       if (rank == 0)  // drain: every copy of both CTAs counted on these barriers has landed
@@ -202,7 +207,10 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
       // A separate thread, so that waiting for the V buffer never holds back the S operands.
       int64_t v_issued = 0;
       bool ok = true;
-      for (int64_t t = t_begin; t < t_end; ++t) {
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+       int64_t ta, tb;
+       so.get(i, ta, tb);
+       for (int64_t t = ta; t < tb; ++t) {
         const int64_t vr = t / NT;
         const int64_t jt = t - vr * NT;
         const int64_t grp = vr / pair_tiles;
@@ -222,6 +230,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
                                   (int)(jt * kSBN) + vc * 64, vrow);
         }
         ++v_issued;
+       }
       }
       if (!ok) flag_error(ctl, status);
       if (rank == 0 && v_issued > 0) ptx::mbar_wait(&ctl.v_full, par(v_issued - 1));
@@ -302,9 +311,9 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
         ++w_uses;
         return true;
       };
-      for (int64_t t = t_begin; ok && t < t_end;) {
-        const int64_t vr = t / NT;
-        const int64_t seg_end = min(t_end, (vr + 1) * NT);
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+        int64_t t, seg_end;
+        so.get(i, t, seg_end);
         const int64_t L = seg_end - t;
         if constexpr (kAlias) {
           // S(u), then (once the epilogue has written W(u) over it) O(u), then S(u + 1),
@@ -334,7 +343,6 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
         if (!ok) break;
         if constexpr (!kHad) ptx::umma_commit_pair(&ctl.o_full, 0x3);
         ++segs;
-        t = seg_end;
       }
       if (!ok) flag_error(ctl, status);
       // Every MMA issued must have retired before either CTA releases its Tensor Memory.
@@ -348,9 +356,9 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
       // them in this order, so one thread forwards them in turn.
       int64_t n_s = 0, n_w = 0, n_o = 0;
       bool ok = true;
-      for (int64_t t = t_begin; ok && t < t_end;) {
-        const int64_t vr = t / NT;
-        const int64_t seg_end = min(t_end, (vr + 1) * NT);
+      for (int64_t i = 0; ok && i < so.n; ++i) {
+        int64_t t, seg_end;
+        so.get(i, t, seg_end);
         for (int64_t tt = t; tt < seg_end; ++tt) {
           if constexpr (!kAlias) {
             if (!ptx::mbar_wait(&ctl.s_empty, par(n_s++))) { ok = false; break; }
@@ -380,7 +388,6 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
           ptx::tc_fence_before();
           ptx::mbar_arrive_cluster(leader(&ctl.o_empty));
         }
-        t = seg_end;
       }
       if (!ok) flag_error(ctl, status);
     }
@@ -395,9 +402,10 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
     int64_t s_uses = 0, w_uses = 0, segs = 0;
     bool ok = true;
     const uint64_t k2 = ptx::pack2(kappa, kappa);
-    for (int64_t t = t_begin; ok && t < t_end;) {
+    for (int64_t i = 0; ok && i < so.n; ++i) {
+      int64_t t, seg_end;
+      so.get(i, t, seg_end);
       const int64_t vr = t / NT;
-      const int64_t seg_end = min(t_end, (vr + 1) * NT);
       const int64_t rp = vr % pair_tiles;
       const int64_t row = rp * 2 * kBM + rank * kBM + rloc;
       const float rb = row < n_rows ? rowBias[row] : neg_inf();
@@ -563,7 +571,6 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
       }
       pW[((size_t)(2 * slot + h)) * ldp + (size_t)prow] = make_float2(sumw, had);
       ++segs;
-      t = seg_end;
     }
     if (!ok) flag_error(ctl, status);
   }
