@@ -426,9 +426,14 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
           if (lane == 0) ptx::mbar_arrive(&ctl.o_empty);
         }
       };
+      // Column biases: 512 B per warp and unit, one 128-byte line per lane 0..3, fetched into
+      // L1 one unit ahead (the first unit of a segment while its S MMA runs).
+      if (lane < 4) ptx::prefetch_l1(colBias + (t - vr * NT) * kSBN + h * 128 + lane * 32);
       for (int64_t tt = t; tt < seg_end; ++tt) {
         const int64_t jt = tt - vr * NT;
         const float4* cb = reinterpret_cast<const float4*>(colBias + jt * kSBN + h * 128);
+        if (tt + 1 < seg_end && lane < 4)
+          ptx::prefetch_l1(colBias + (jt + 1) * kSBN + h * 128 + lane * 32);
         if (!ptx::mbar_wait(&ctl.s_full, par(s_uses))) { ok = false; break; }
         ++s_uses;
         ptx::tc_fence_after();
