@@ -102,7 +102,10 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
   constexpr bool kBf = (kPrec == kPrecBF16);
   constexpr bool kSplitW = (kPrec == kPrecSplit);
   // W overwrites S in tensor memory (tf32, split): the next S MMA waits for this unit's W V.
-  constexpr bool kAlias = !kBf && !kHad;
+  // bf16 with 256 output columns per group (wide outputs such as the gradient): O needs
+  // [256, 512), so W (bf16 pairs) is written over S as well.
+  constexpr bool kWide = kBf && kKV == 256;
+  constexpr bool kAlias = (!kBf || kWide) && !kHad;
   // Split tf32: each unit's W V lands in a fresh tensor-memory accumulator that the epilogue
   // adds into fp32 registers (round to nearest), so no accumulation chain in the tensor core
   // is longer than one unit's K = 256 (x 3 terms); long in-tensor-memory chains over a whole
@@ -111,8 +114,8 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
   constexpr int kElems = kBf ? 64 : 32;  // K elements per 128-byte chunk of the S operands
   using VS = VShape<kPrec, kKV>;
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kTmemW = kBf ? 256u : 0u;  // W (bf16 pairs) or W_hi (over S)
-  constexpr uint32_t kTmemO = kBf ? 384u : 256u;
+  constexpr uint32_t kTmemW = (kBf && !kWide) ? 256u : 0u;  // W (bf16 pairs) or W_hi (over S)
+  constexpr uint32_t kTmemO = (kBf && !kWide) ? 384u : 256u;
   constexpr uint32_t kTmemWL = 384u;            // W_lo bf16 pairs (split)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();  // 0: the pair's MMA issuer
@@ -283,10 +286,14 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
         for (int vc = 0; vc < VS::chunks_main; ++vc) {
           const uint64_t v_desc = ptx::sdesc_k128(vb + (uint32_t)vc * VS::chunk);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::umma_pair_ts<kBf>(tmem + kTmemO, tmem + kTmemW + (uint32_t)(vc * 4 + kk) * 8u,
-                                   v_desc + 2u * kk, idesc_o,
+          for (int kk = 0; kk < 4; ++kk) {
+            // wide bf16: warp half h wrote its 64 pair-columns (K = 128h .. 128h + 127) at
+            // column 128h, so K >= 128 starts at column 128
+            const uint32_t wcol = kWide ? (uint32_t)((vc >> 1) * 128 + ((vc & 1) * 4 + kk) * 8)
+                                        : (uint32_t)(vc * 4 + kk) * 8u;
+            ptx::umma_pair_ts<kBf>(tmem + kTmemO, tmem + kTmemW + wcol, v_desc + 2u * kk, idesc_o,
                                    ((!first && !kPromote) || vc > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         if constexpr (kSplitW) {
 #pragma unroll
@@ -498,7 +505,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
           for (int half = 0; half < 2; ++half) {
             float v[64];
             ptx::tmem_ld_x64_sync(s_addr + 64 * half, v);
-            uint32_t lo[kSplitW ? 32 : 1];
+            uint32_t lo[(kSplitW || kWide) ? 32 : 1];
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
               const float4 b4 = __ldg(cb + 16 * half + j / 4);
@@ -511,6 +518,13 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
               ptx::unpack2(e23, x2, x3);
               const float w0 = ex2(x0), w1 = ex2(x1), w2 = ex2(x2), w3 = ex2(x3);
               sw2 = ptx::add2(sw2, ptx::add2(ptx::pack2(w0, w1), ptx::pack2(w2, w3)));
+              if constexpr (kWide) {
+                __nv_bfloat162 p01 = __floats2bfloat162_rn(w0, w1);
+                __nv_bfloat162 p23 = __floats2bfloat162_rn(w2, w3);
+                lo[j / 2] = *reinterpret_cast<uint32_t*>(&p01);
+                lo[j / 2 + 1] = *reinterpret_cast<uint32_t*>(&p23);
+                continue;
+              }
               const uint32_t h0 = tf32_rna(w0), h1 = tf32_rna(w1), h2 = tf32_rna(w2),
                              h3 = tf32_rna(w3);
               if constexpr (kSplitW) {
@@ -525,6 +539,12 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
               v[j + 1] = __uint_as_float(h1);
               v[j + 2] = __uint_as_float(h2);
               v[j + 3] = __uint_as_float(h3);
+            }
+            if constexpr (kWide) {
+              // bf16 pairs of this half's 64 weights over the first half's (already read)
+              // S columns: pair-columns 128h + 32 half .. + 31
+              ptx::tmem_st_x32_sync(s_addr + 32 * half, lo);
+              continue;
             }
             ptx::tmem_st_x64_sync(s_addr + 64 * half, *reinterpret_cast<uint32_t(*)[64]>(v));
             if constexpr (kSplitW)
@@ -737,14 +757,14 @@ static int max_clusters() {
 size_t tc_wsum_pair_scratch_bytes(int64_t rows_pad, int64_t k_or_d) {
   // pO: kMaxOwners slots x rows_pad x (groups x kKV) floats, groups x kKV <= round_up(k, 128)
   // (or 64); pW: 2 kMaxOwners slots x groups x rows_pad float2, groups <= kk / 64.
-  const int64_t kk = k_or_d <= 64 ? 64 : (k_or_d + 127) / 128 * 128;
+  const int64_t kk = k_or_d <= 64 ? 64 : (k_or_d <= 128 ? 128 : (k_or_d + 255) / 256 * 256);
   return (size_t)tcp::kMaxOwners * rows_pad * kk * sizeof(float) +
          (size_t)2 * tcp::kMaxOwners * (kk / 64) * rows_pad * sizeof(float2) + 1024;
 }
 
 size_t tc_wsum_pair_vt_bytes(int prec, int64_t rows_pad, int64_t k_or_d) {
   // V^T planes: out_rows_pad (whole 64- or 128-column groups) x cols_pad elements each.
-  const int64_t kk = k_or_d <= 64 ? 64 : (k_or_d + 127) / 128 * 128;
+  const int64_t kk = k_or_d <= 64 ? 64 : (k_or_d <= 128 ? 128 : (k_or_d + 255) / 256 * 256);
   const int64_t e = kk * rows_pad;
   return (size_t)e * (prec == FLASHOT_PREC_BF16 ? 2 : (prec == FLASHOT_PREC_TF32 ? 4 : 10)) + 1024;
 }
@@ -768,7 +788,9 @@ int tc_wsum_pair_pass(int prec, int mode, const void* rowQ, const void* colQ,
   if (!had && ldv != k) return FLASHOT_ERR_INVALID_ARG;
   // Output columns per group: 128 (64 for split tf32, whose V planes need the room; 64 when
   // k <= 64).
-  const int kv = had ? 0 : ((k <= 64 || split) ? 64 : 128);
+  // bf16 outputs wider than 128 columns (the gradient at d = 512) take 256-column groups, so
+  // S is formed half as often.
+  const int kv = had ? 0 : ((k <= 64 || split) ? 64 : ((bf && k > 128) ? 256 : 128));
   const int64_t groups = had ? 1 : (k + kv - 1) / kv;
   const int64_t vrows = groups * pair_tiles;
   const int64_t T = vrows * NT;
@@ -817,7 +839,8 @@ int tc_wsum_pair_pass(int prec, int mode, const void* rowQ, const void* colQ,
   if (had)
     rc = bf ? FLASHOT_PAIR_WSUM(kPrecBF16, 0) : FLASHOT_PAIR_WSUM(kPrecTF32, 0);
   else if (bf)
-    rc = kv == 64 ? FLASHOT_PAIR_WSUM(kPrecBF16, 64) : FLASHOT_PAIR_WSUM(kPrecBF16, 128);
+    rc = kv == 64 ? FLASHOT_PAIR_WSUM(kPrecBF16, 64)
+                  : (kv == 128 ? FLASHOT_PAIR_WSUM(kPrecBF16, 128) : FLASHOT_PAIR_WSUM(kPrecBF16, 256));
   else if (!split)
     rc = kv == 64 ? FLASHOT_PAIR_WSUM(kPrecTF32, 64) : FLASHOT_PAIR_WSUM(kPrecTF32, 128);
   else
