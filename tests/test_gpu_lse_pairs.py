@@ -25,7 +25,10 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 CASES = [(257, 260, 512, "bf16"), (3000, 2100, 512, "bf16"), (700, 1500, 1024, "bf16"),
-         (520, 640, 256, "tf32"), (1100, 900, 512, "tf32"), (300, 333, 512, "tf32x3")]
+         (520, 640, 256, "tf32"), (1100, 900, 512, "tf32"), (300, 333, 512, "tf32x3"),
+         # one point against many, many against one: a single 256-row pair tile or a single
+         # column tile, rows and columns mostly padding
+         (1, 300, 1024, "bf16"), (300, 1, 512, "tf32"), (1, 1, 512, "bf16")]
 
 _CHILD = r"""
 import sys

@@ -121,6 +121,47 @@ def test_pair_weighted_sums_match_single_cta_and_oracle(cuda_lib, tmp_path):
                 (key, out, "single")
 
 
+@pytest.mark.parametrize("precision", ["bf16", "tf32", "tf32x3"])
+@pytest.mark.parametrize("n,m,d,k", [(1, 300, 1024, 8), (300, 1, 512, 130), (1, 1, 256, 1),
+                                     (3, 700, 512, 300)])
+def test_pair_weighted_sums_degenerate_shapes(cuda_lib, precision, n, m, d, k):
+    """One point against many and many against one (a single pair tile or column tile, rows
+    and columns mostly padding), and k = 300 (three output groups of 128, two of 256 for
+    bf16): P V, P^T U and the gradient on exact operands within the operands' rounding bound
+    2u (P |V|) (u of the second contraction's operands: bf16 2^-9, tf32 2^-11, split tf32
+    2^-20) plus the fp32 epilogue's 4e-6."""
+    from gpu_helpers import SECOND_U
+    lds = cuda_lib
+    rng = np.random.default_rng(n + 3 * m + d + k)
+    X = (rng.integers(-1, 2, size=(n, d)) * 0.25).astype(np.float32)
+    Y = (rng.integers(-1, 2, size=(m, d)) * 0.25).astype(np.float32)
+    V = (rng.integers(-2, 3, size=(m, k)) * 0.25).astype(np.float32)
+    U = (rng.integers(-2, 3, size=(n, k)) * 0.25).astype(np.float32)
+    a = rng.exponential(size=n)
+    b = rng.exponential(size=m)
+    a = (a / a.sum()).astype(np.float32)
+    b = (b / b.sum()).astype(np.float32)
+    eps = d / 32.0
+    f, g, _ = oracle.solve(X, Y, a, b, [eps], 10)
+    f, g = f.astype(np.float32), g.astype(np.float32)
+    args = (to_dev(X), to_dev(Y), to_dev(f), to_dev(g), eps)
+    u = SECOND_U[precision]
+    for W, tr in ((V, False), (U, True)):
+        got = lds.transport_apply(*args, to_dev(W), to_dev(a), to_dev(b), transpose=tr,
+                                  precision=precision).cpu().numpy()
+        ref = oracle.transport_apply(X, Y, a, b, f, g, eps, W, transpose=tr)
+        mag = oracle.transport_apply(X, Y, a, b, f, g, eps, np.abs(W), transpose=tr)
+        bound = (2 * u + 4e-6) * mag + 1e-7 * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= bound), (tr, np.abs(got - ref).max())
+    grad = lds.ot_grad_x(to_dev(X), to_dev(Y), to_dev(g), eps, to_dev(a), to_dev(b),
+                         precision=precision).cpu().numpy()
+    ref = oracle.grad_x(X, Y, a, b, g, eps)
+    ft = oracle.half_step_f(X, Y, b, g, eps)
+    mag = oracle.transport_apply(X, Y, a, b, ft, g, eps, np.abs(Y))
+    bound = 4 * u * mag + 8e-6 * (mag + np.abs(a)[:, None] * np.abs(X)) + 1e-7 * np.abs(ref).max()
+    assert np.all(np.abs(grad - ref) <= bound), np.abs(grad - ref).max()
+
+
 @pytest.mark.parametrize("n,m,d,k", [(300, 450, 64, 128), (200, 260, 512, 64),
                                      (130, 300, 1024, 200), (257, 129, 32, 16)])
 def test_split_second_contraction_exact_operands(cuda_lib, n, m, d, k):
