@@ -334,7 +334,7 @@ def run_reference(args):
 # whose code it runs. (fma_kernels.cuh and flashot.h are included there as well but hold
 # nothing the LSE kernel executes: the split reduction of the tf32 weighted sums, and the
 # public API.) The recorded ncu traffic is valid while these are unchanged.
-LSE_KERNEL_SOURCES = ("tc_kernels.cu", "common.cuh", "pack_kernels.cuh", "ptx.cuh",
+LSE_KERNEL_SOURCES = ("tc_kernels.cu", "lse_epilogue.cuh", "common.cuh", "pack_kernels.cuh", "ptx.cuh",
                       "tc_api.h", "tc_host.h", "trace.h")
 
 
@@ -483,7 +483,9 @@ def run_other_workload(args):
     clk, clk_src = run_clock_hz(clk_rec, peaks)
     avg = ms_hot / max(n_hot, 1) / 1e3
     # Scores per timed launch of the hot kernel class: the streaming solve launches one LSE
-    # pass per half-step; the single-launch cluster solve covers the whole solve.
+    # pass per half-step; the single-launch solves (the cluster solve of small fp32
+    # problems, the persistent solve of short tensor-core contractions) cover the whole
+    # solve.
     per_launch_scores = scores_per_step * args.steps / max(n_hot, 1)
     if prec == "fp32":
         roof = {"bound": "alu", "achieved": 2.0 * d * per_launch_scores / avg / 1e12,
@@ -513,6 +515,7 @@ def run_other_workload(args):
                                  / (sms * FP32_LANES_PER_SM * clk))
     roof["avg_launch_ms"] = avg * 1e3
     roof["launches_timed"] = n_hot
+    roof["scores_per_launch"] = per_launch_scores
     graph = None
     if args.graph and idx != 5 and not args.divergence and not args.diagnostics:
         # The same solve captured once into a CUDA graph (torch's capture stream is the

@@ -43,7 +43,9 @@ __device__ __forceinline__ int combine_slots(const SplitInfo& split, int64_t i) 
                sk_owner(rt * split.sk_NT, split.sk_T, split.sk_G) + 1);
 }
 
-// Row i (0 <= i < rows_pad).
+// Row i (0 <= i < rows_pad). kL2: read the partials from L2 (ld.global.cg), for a caller
+// inside the kernel whose other CTAs wrote them (a stale L1 line must not be read).
+template <bool kL2 = false>
 __device__ __forceinline__ void combine_row(const float2* __restrict__ partial, int64_t ld,
                                             const SplitInfo& split, int64_t i,
                                             const CombineArgs& a) {
@@ -53,7 +55,7 @@ __device__ __forceinline__ void combine_row(const float2* __restrict__ partial, 
     return;
   }
   const int n_splits = combine_slots(split, i);
-  auto load = [&](int s) { return partial[s * ld + i]; };
+  auto load = [&](int s) { return kL2 ? __ldcg(partial + s * ld + i) : partial[s * ld + i]; };
   float M = kNegBig;
   for (int s = 0; s < n_splits; ++s) M = fmaxf(M, load(s).x);
   float S = 0.0f;

@@ -20,6 +20,7 @@
 #include "prep_kernels.cuh"
 #include "small_solve.h"
 #include "tc_api.h"
+#include "tc_solve_short.h"
 #include "tc_wsum_pair.h"
 #include "trace.h"
 #include <vector>
@@ -156,7 +157,7 @@ bool make_geometry(int64_t n, int64_t m, int64_t d, int64_t k, int flags, Geomet
 
 struct Layout {
   size_t status, xp, yp, xq, yq, vtq, wsp, tsp, alpha, beta, wa, wb, la2, lb2, biasF, biasG,
-      ftilde, lse2, partial, loss, total;
+      ftilde, lse2, partial, loss, sync, total;
 };
 
 Layout make_layout(const Geometry& g) {
@@ -188,6 +189,8 @@ Layout make_layout(const Geometry& g) {
   L.lse2 = take(std::max(np, mp) * 4);
   L.partial = take((size_t)kMaxSplits * std::max(np, mp) * sizeof(float2));
   L.loss = take(64);
+  // Arrival counters and grid barrier of the persistent short-contraction solve.
+  if (g.prec != FLASHOT_PREC_FP32) L.sync = take(tc_short_solve_sync_bytes(g.n_pad, g.m_pad));
   // Last, so that every offset above is independent of k: the transposed right operand
   // of the tensor-core weighted sums (V^T for apply, Y^T for the gradient), padded to
   // multiples of 256 output columns.
@@ -810,7 +813,21 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
   if ((rc = launch_bias(c, (flags & FLASHOT_WARM_START) ? g : nullptr, false, eps_sched[0])) !=
       FLASHOT_OK)
     return rc;
-  for (int s = 0; s < n_stages; ++s) {
+  // Short tensor-core contractions: every half-step in one persistent launch (the same
+  // tiles, partials and merges as the passes below, so the same bits).
+  bool done = false;
+  if (c.g.prec != FLASHOT_PREC_FP32) {
+    rc = tc_short_solve(c.g.prec == FLASHOT_PREC_BF16, c.at<void>(c.L.xq), c.at<void>(c.L.yq), n,
+                        m, c.g.n_pad, c.g.m_pad, c.g.dpt, c.at<float>(c.L.alpha),
+                        c.at<float>(c.L.beta), c.at<float>(c.L.la2), c.at<float>(c.L.lb2),
+                        c.at<float>(c.L.biasF), c.at<float>(c.L.biasG), f, g, eps_sched,
+                        n_stages, iters_per_stage, c.at<float2>(c.L.partial), kMaxSplits,
+                        c.at<void>(c.L.sync), tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad),
+                        c.sms, c.at<unsigned>(c.L.status), c.st);
+    if (rc == FLASHOT_OK) done = true;
+    else if (rc != FLASHOT_ERR_NOT_IMPLEMENTED) return rc;
+  }
+  for (int s = 0; !done && s < n_stages; ++s) {
     const float eps = eps_sched[s];
     for (int it = 0; it < iters_per_stage; ++it) {
       const bool last_of_stage = (it == iters_per_stage - 1);

@@ -30,6 +30,7 @@
 #include "flashot.h"
 #include "common.cuh"
 #include "fma_kernels.cuh"  // wsum_split_reduce_kernel
+#include "lse_epilogue.cuh"
 #include "pack_kernels.cuh"
 #include "ptx.cuh"
 #include "tc_api.h"
@@ -65,73 +66,6 @@ struct __align__(128) Ctrl {
 __device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
   atomicOr(status, kErrTimeout);
   ctl.abort_flag = 1;
-}
-
-// Lazy rescaling of the online (max, sum): a chunk is exponentiated against the running max
-// M of the earlier chunks in the same pass that finds its own max, so the ex2 work does not
-// wait for the chunk's max. M is raised only when the chunk's max exceeds it by more than
-// kLazyRescale (then the chunk's sums are taken again against the new max); otherwise the
-// terms are at most 2^kLazyRescale, far inside fp32 range. The first chunk of a row
-// segment (M at its floor) always takes the second pass.
-constexpr float kLazyRescale = 8.0f;
-
-// kN (a multiple of 8) columns of one S-tile row: scores s2 = kappa * dot + bias and the online
-// base-2 (max, sum) update. Pairs of scores go through packed fp32x2 instructions: per
-// score half an FFMA2, half a 3-input max, half an FADD2, one SFU ex2 and half an FADD2.
-// kLdg: read the biases through the read-only path (global memory) rather than as plain
-// loads (biases staged in shared memory).
-template <int kN, bool kLdg>
-__device__ __forceinline__ void lse_chunk(float (&v)[kN], const float4* __restrict__ cb,
-                                          float kappa, float& M, float& S) {
-  const uint64_t k2 = ptx::pack2(kappa, kappa);
-  uint64_t nm2 = ptx::pack2(-M, -M);
-  // Four independent running maxima / four packed sums keep the dependency chains short.
-  float m0 = kNegBig, m1 = kNegBig, m2 = kNegBig, m3 = kNegBig;
-  uint64_t s2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-  for (int j = 0; j < kN; j += 8) {
-    const float4 b4 = kLdg ? __ldg(cb + j / 4) : cb[j / 4];
-    const float4 b5 = kLdg ? __ldg(cb + j / 4 + 1) : cb[j / 4 + 1];
-    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 0], v[j + 1]), ptx::pack2(b4.x, b4.y)),
-                 v[j + 0], v[j + 1]);
-    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 2], v[j + 3]), ptx::pack2(b4.z, b4.w)),
-                 v[j + 2], v[j + 3]);
-    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 4], v[j + 5]), ptx::pack2(b5.x, b5.y)),
-                 v[j + 4], v[j + 5]);
-    ptx::unpack2(ptx::fma2(k2, ptx::pack2(v[j + 6], v[j + 7]), ptx::pack2(b5.z, b5.w)),
-                 v[j + 6], v[j + 7]);
-    m0 = ptx::max3(m0, v[j + 0], v[j + 1]);
-    m1 = ptx::max3(m1, v[j + 2], v[j + 3]);
-    m2 = ptx::max3(m2, v[j + 4], v[j + 5]);
-    m3 = ptx::max3(m3, v[j + 6], v[j + 7]);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float d0, d1;
-      ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2 * u], v[j + 2 * u + 1]), nm2), d0, d1);
-      s2[u] = ptx::add2(s2[u], ptx::pack2(ex2(d0), ex2(d1)));
-    }
-  }
-  const float mx = fmaxf(ptx::max3(m0, m1, m2), m3);
-  if (mx > M + kLazyRescale) {  // rare: raise the max and take the sums again
-    S *= ex2(M - mx);
-    M = mx;
-    nm2 = ptx::pack2(-M, -M);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) s2[u] = 0ull;
-#pragma unroll
-    for (int j = 0; j < kN; j += 8) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float d0, d1;
-        ptx::unpack2(ptx::add2(ptx::pack2(v[j + 2 * u], v[j + 2 * u + 1]), nm2), d0, d1);
-        s2[u] = ptx::add2(s2[u], ptx::pack2(ex2(d0), ex2(d1)));
-      }
-    }
-  }
-  const uint64_t t2 = ptx::add2(ptx::add2(s2[0], s2[1]), ptx::add2(s2[2], s2[3]));
-  float t0, t1;
-  ptx::unpack2(t2, t0, t1);
-  S += t0 + t1;
 }
 
 // ---------------------------------------------------------------------------------------

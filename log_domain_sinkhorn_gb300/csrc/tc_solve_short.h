@@ -1,0 +1,31 @@
+// tc_solve_short.h -- the persistent solve of short tensor-core contractions
+// (tc_solve_short.cu), used by flashot.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace flashot {
+
+// Bytes of device memory the persistent solve needs for its arrival counters and grid
+// barrier word (zeroed by tc_short_solve itself on `st`).
+size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad);
+
+// Every half-step of the alternating solve (n_stages x iters_per_stage iterations, F then G)
+// in one cooperative launch, for contractions of at most six 128-byte K-chunks. Inputs and
+// outputs are those of the per-pass path: xq / yq the packed clouds (n_pad / m_pad rows of dpt
+// elements), alpha / beta the squared norms, la2 / lb2 the log2 weights, biasF the F pass's
+// column bias on entry (from the initial g), f and g the potentials written. partial holds
+// max_splits x max(n_pad, m_pad) float2. Returns FLASHOT_ERR_NOT_IMPLEMENTED, having enqueued
+// nothing, when the solve does not qualify (a longer contraction, more than 32 eps stages, a
+// grid that cannot be co-resident, or FLASHOT_SHORT_SOLVE=0 in the environment); the caller
+// then runs the per-pass path.
+int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t m,
+                   int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
+                   const float* beta, const float* la2, const float* lb2, float* biasF,
+                   float* biasG, float* f, float* g, const float* eps_sched, int n_stages,
+                   int iters_per_stage, float2* partial, int max_splits, void* sync_words,
+                   size_t sync_bytes, int sms, unsigned* status, cudaStream_t st);
+
+}  // namespace flashot
