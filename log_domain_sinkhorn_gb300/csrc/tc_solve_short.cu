@@ -97,18 +97,27 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+// Release / acquire at GPU scope in the fence form: fence.acq_rel.gpu before a relaxed
+// arrival makes the CTA's earlier writes (ordered before it by the CTA barrier) visible to
+// whoever observes the arrival; a relaxed observation followed by fence.acq_rel.gpu makes
+// them visible to the observer. (With sc fences around acq_rel atomics the end-of-pass
+// counting took about a quarter more cycles.)
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_relaxed_gpu(unsigned* p, unsigned v) {
   unsigned old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+  asm volatile("atom.add.relaxed.gpu.global.u32 %0, [%1], %2;"
                : "=r"(old)
                : "l"(p), "r"(v)
                : "memory");
   return old;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -392,16 +401,15 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       if (etid == 0) {
         int first = 0, last = 0;
         if (tb < te) {
-          __threadfence();  // the epilogue's partials before the arrival (cumulative release)
+          fence_acq_rel_gpu();  // the epilogue's partials before the arrivals
           const int64_t o0 = row_tile_owners(S, rt0);
-          first = o0 == 1 ||
-                  (atom_add_acq_rel_gpu(S.counters + rt0, 1u) + 1u) % (unsigned)o0 == 0u;
-          if (rt1 != rt0) {
-            const int64_t o1 = row_tile_owners(S, rt1);
-            last = o1 == 1 ||
-                   (atom_add_acq_rel_gpu(S.counters + rt1, 1u) + 1u) % (unsigned)o1 == 0u;
-          }
-          __threadfence();
+          const int64_t o1 = rt1 != rt0 ? row_tile_owners(S, rt1) : 1;
+          const unsigned a0 = o0 > 1 ? atom_add_relaxed_gpu(S.counters + rt0, 1u) : 0u;
+          const unsigned a1 = o1 > 1 ? atom_add_relaxed_gpu(S.counters + rt1, 1u) : 0u;
+          first = o0 == 1 || (a0 + 1u) % (unsigned)o0 == 0u;
+          last = rt1 != rt0 && (o1 == 1 || (a1 + 1u) % (unsigned)o1 == 0u);
+          // the last arrival on a shared row tile: the other owners' partials are visible
+          if ((first && o0 > 1) || (last && o1 > 1)) fence_acq_rel_gpu();
         }
         ctl.merge_first = first;
         ctl.merge_last = last;
@@ -434,18 +442,19 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       epi_sync();
       // (4) grid barrier: every CTA's merges are visible before any CTA reads the new biases
       if (etid == 0) {
-        __threadfence();
+        fence_acq_rel_gpu();
         const unsigned target = (unsigned)((p + 1) * (int64_t)gridDim.x);
-        atom_add_acq_rel_gpu(P.grid_bar, 1u);
-        bool arrived = ld_acquire_gpu(P.grid_bar) >= target;
+        atom_add_relaxed_gpu(P.grid_bar, 1u);
+        bool arrived = ld_relaxed_gpu(P.grid_bar) >= target;
         if (!arrived) {
           const uint64_t t0 = ptx::globaltimer();
           while (true) {
 #pragma unroll 1
-            for (int i = 0; i < 32 && !arrived; ++i) arrived = ld_acquire_gpu(P.grid_bar) >= target;
+            for (int i = 0; i < 32 && !arrived; ++i) arrived = ld_relaxed_gpu(P.grid_bar) >= target;
             if (arrived || ptx::globaltimer() - t0 > ptx::kWaitLimitNs) break;
           }
         }
+        fence_acq_rel_gpu();
         if (!arrived) {
           atomicOr(P.status, kErrTimeout);
           ctl.epi_abort[p & 1] = 1;
@@ -501,11 +510,16 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
                    size_t sync_bytes, int sms, unsigned* status, cudaStream_t st) {
   using namespace tc;
   using namespace tc::ssolve;
-  // FLASHOT_SHORT_SOLVE=0 in the environment keeps the per-pass path (for comparisons).
-  static const bool enabled = [] {
+  // FLASHOT_SHORT_SOLVE in the environment: 0 keeps the per-pass path, 1 takes the
+  // persistent solve whenever it applies; unset, it is taken when the CTAs average at least
+  // 1.5 tiles per pass on both sides (with one each, the end-of-pass counting and grid
+  // barrier cost more than the launches they replace: measured 25-30 % slower at 2048^2,
+  // one tile per CTA, and 11-22 % faster at 3072^2 and 4096^2, 1.9 and 3.4, d = 16..128).
+  static const int mode = [] {
     const char* e = std::getenv("FLASHOT_SHORT_SOLVE");
-    return !(e && e[0] == '0');
+    return e && e[0] == '0' ? 0 : (e && e[0] == '1' ? 1 : 2);
   }();
+  const bool enabled = mode != 0;
   const int es = bf16 ? 2 : 4;
   const int kc = (int)(dpt * es / 128);
   if (!enabled || kc < 1 || kc > kMaxKc || n_stages < 1 || n_stages > kMaxEps ||
@@ -519,6 +533,8 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   const int64_t GF = choose_grid(rtX, NTY, sms, max_splits / 2);
   const int64_t GG = choose_grid(rtY, NTX, sms, max_splits / 2);
   const int64_t grid = std::max(GF, GG);
+  if (mode == 2 && (2 * rtX * NTY < 3 * GF || 2 * rtY * NTX < 3 * GG))
+    return FLASHOT_ERR_NOT_IMPLEMENTED;
   const int64_t n_pass = 2LL * n_stages * iters_per_stage;
   if (n_pass * grid >= (1LL << 31)) return FLASHOT_ERR_NOT_IMPLEMENTED;
   auto kern = bf16 ? lse_solve_short_kernel<true> : lse_solve_short_kernel<false>;

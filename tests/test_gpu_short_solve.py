@@ -3,10 +3,11 @@ cooperative launch, stream-K partials merged by the last owner of each row tile,
 barrier between passes) against the per-pass path and the fp64 oracle.
 
 Contractions of at most six 128-byte K-chunks (bf16 d <= 192, tf32 d <= 96, split tf32
-d <= 64) take the persistent solve by default; FLASHOT_SHORT_SOLVE=0 in the environment
-keeps the per-pass launches (read once per process, so that run is a child process). Both
-paths use the same tiles, stream-K ranges, partial slots and merge arithmetic, so their
-potentials and loss must agree bit for bit; both are held to the oracle's full solve at the
+d <= 64) take the persistent solve when the CTAs average at least 1.5 tiles per pass;
+FLASHOT_SHORT_SOLVE=1 in the environment takes it for any size, FLASHOT_SHORT_SOLVE=0 never
+(read once per process, so each forced run is a child process). Both paths use the same
+tiles, stream-K ranges, partial slots and merge arithmetic, so their potentials and loss
+must agree bit for bit; the persistent solve is held to the oracle's full solve at the
 potentials and loss tolerances. The cases cover ragged and rectangular shapes, one point
 against many, one to three K-chunks, every tensor-core precision, an annealed eps schedule
 (the G-update at a stage boundary hands its bias to the next eps), a warm start and zero
@@ -53,7 +54,11 @@ for nm in names:
     eps = [float(e) for e in data[nm + "/eps"]]
     iters, prec = int(data[nm + "/iters"]), str(data[nm + "/prec"])
     g0 = t(data[nm + "/g0"]) if bool(data[nm + "/warm"]) else None
+    timer = lds.KernelTimer().start()
     f, g, loss = lds.sinkhorn_solve(X, Y, a, b, eps, iters, precision=prec, g0=g0)
+    torch.cuda.synchronize()
+    out[nm + "/lse_launches"] = np.int64(timer.read(lds.KernelTimer.LSE)[0])
+    timer.stop()
     out[nm + "/f"] = f.cpu().numpy()
     out[nm + "/g"] = g.cpu().numpy()
     out[nm + "/loss"] = np.float64(loss.cpu())
@@ -75,7 +80,8 @@ def _problem(name):
     return pr.X, pr.Y, a.astype(np.float32), b.astype(np.float32), eps, iters, prec, warm, g0
 
 
-def _per_pass(problems, tmp_path):
+def _child(problems, tmp_path, mode):
+    """The solves in a child process with FLASHOT_SHORT_SOLVE=mode."""
     arrays = {}
     for nm, (X, Y, a, b, eps, iters, prec, warm, g0) in problems.items():
         for k, v in (("X", X), ("Y", Y), ("a", a), ("b", b), ("g0", g0)):
@@ -86,30 +92,26 @@ def _per_pass(problems, tmp_path):
         arrays[f"{nm}/warm"] = np.bool_(warm)
     src = tmp_path / "child.py"
     src.write_text(_CHILD.format(root=ROOT))
-    inp, outp = tmp_path / "in.npz", tmp_path / "out.npz"
+    inp, outp = tmp_path / f"in{mode}.npz", tmp_path / f"out{mode}.npz"
     np.savez(inp, **arrays)
-    env = dict(os.environ, FLASHOT_SHORT_SOLVE="0")
+    env = dict(os.environ, FLASHOT_SHORT_SOLVE=mode)
     r = subprocess.run([sys.executable, str(src), str(inp), str(outp)], env=env,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     out = np.load(outp)
-    return {nm: (out[nm + "/f"], out[nm + "/g"], float(out[nm + "/loss"])) for nm in problems}
+    return {nm: (out[nm + "/f"], out[nm + "/g"], float(out[nm + "/loss"]),
+                 int(out[nm + "/lse_launches"])) for nm in problems}
 
 
 def test_persistent_solve_is_bitwise_the_per_pass_solve_and_matches_oracle(cuda_lib, tmp_path):
-    lds = cuda_lib
     problems = {nm: _problem(nm) for nm in CASES}
-    ref_pass = _per_pass(problems, tmp_path)
+    persistent = _child(problems, tmp_path, "1")
+    per_pass = _child(problems, tmp_path, "0")
     for nm, (X, Y, a, b, eps, iters, prec, warm, g0) in problems.items():
-        timer = lds.KernelTimer().start()
-        f, g, loss = lds.sinkhorn_solve(to_dev(X), to_dev(Y), to_dev(a), to_dev(b), eps, iters,
-                                        precision=prec, g0=to_dev(g0) if warm else None)
-        torch.cuda.synchronize()
-        lse_launches, _ = timer.read(lds.KernelTimer.LSE)
-        timer.stop()
-        assert lse_launches == 1, (nm, lse_launches)  # one persistent launch for the solve
-        f, g, loss = f.cpu().numpy(), g.cpu().numpy(), float(loss.cpu())
-        fp, gp, lp = ref_pass[nm]
+        f, g, loss, launches = persistent[nm]
+        fp, gp, lp, launches_p = per_pass[nm]
+        assert launches == 1, (nm, launches)  # one persistent launch for the whole solve
+        assert launches_p == 2 * len(eps) * iters, (nm, launches_p)
         assert np.array_equal(f, fp) and np.array_equal(g, gp), nm
         assert loss == lp, nm
         fo, go, lo = oracle.solve(X, Y, a, b, eps, iters, g0=g0 if warm else None)
@@ -120,10 +122,29 @@ def test_persistent_solve_is_bitwise_the_per_pass_solve_and_matches_oracle(cuda_
         assert rel_err(loss, lo) <= LOSS_TOL[prec], (nm, loss, lo)
 
 
+@pytest.mark.parametrize("n,expect_persistent", [(2000, False), (3000, True)])
+def test_default_takes_the_persistent_solve_above_one_tile_per_cta(cuda_lib, n,
+                                                                    expect_persistent):
+    """Unforced, the persistent solve runs when the CTAs average at least 1.5 tiles per pass
+    (3000^2: 24 x 12 tiles over 152 CTAs), not with one each (2000^2: 16 x 8 tiles over
+    128 CTAs)."""
+    if os.environ.get("FLASHOT_SHORT_SOLVE"):
+        pytest.skip("FLASHOT_SHORT_SOLVE is set in this environment")
+    lds = cuda_lib
+    pr = make_problem(n, n, 64, x_dist="normal", y_dist="normal_shift05", seed=n)
+    timer = lds.KernelTimer().start()
+    lds.sinkhorn_solve(to_dev(pr.X), to_dev(pr.Y), None, None, 8.0, 3, precision="bf16")
+    torch.cuda.synchronize()
+    launches = timer.read(lds.KernelTimer.LSE)[0]
+    timer.stop()
+    assert launches == (1 if expect_persistent else 6), launches
+
+
 def test_persistent_solve_status_is_clean(cuda_lib):
     """The grid barrier and the row-tile counters never give up a wait on a normal solve."""
     lds = cuda_lib
-    X, Y, a, b, eps, iters, prec, _, _ = _problem("sq2000_d64_bf16")
+    pr = make_problem(3000, 3000, 64, x_dist="normal", y_dist="normal_shift05", seed=5)
+    X, Y, a, b, eps, iters, prec = pr.X, pr.Y, pr.a, pr.b, [8.0], 20, "bf16"
     ws = lds.Workspace(lds.workspace_bytes(X.shape[0], Y.shape[0], X.shape[1], 0, prec))
     for _ in range(3):
         lds.sinkhorn_solve(to_dev(X), to_dev(Y), to_dev(a), to_dev(b), eps, iters,
