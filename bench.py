@@ -1168,7 +1168,7 @@ def run_gpu(args):
                          "frac_clock_matched": clock_matched(achieved / peak, clk.get("sm_mhz"),
                                                              peak_mhz),
                          "peak_clock_mhz": peak_mhz, "traffic": traffic,
-                         "kernel": "lse_tc_kernel (streaming LSE half-step)",
+                         "kernel": "lse_pair_kernel (streaming LSE half-step on 2-SM CTA pairs)",
                          "algorithmic_flops_per_launch": flops_per_launch,
                          "avg_launch_ms": lse_avg_ms, "launches_timed": n_lse,
                          "peak_source": peak_label},
