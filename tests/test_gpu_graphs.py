@@ -43,6 +43,52 @@ def test_captured_solve_replays_bitwise(cuda_lib, precision, idx, n):
         assert float(loss) == float(l_direct)
 
 
+@pytest.mark.parametrize("precision,idx,n", [("bf16", 2, 4000), ("tf32x3", 4, 3000)])
+def test_captured_persistent_solve_replays_bitwise(cuda_lib, precision, idx, n):
+    """Short contractions with enough tiles run as one cooperative launch (after a memset
+    of its counters): both are captured as graph nodes and each replay gives the bits of a
+    direct call."""
+    import os
+    if os.environ.get("FLASHOT_SHORT_SOLVE"):
+        pytest.skip("FLASHOT_SHORT_SOLVE is set in this environment")
+    lds = cuda_lib
+    pr = scaled_workload(idx, n=n, iters=12)
+    X, Y, a, b = problem_tensors(pr)
+    eps = float(pr.eps_schedule[-1])
+    ws = lds.Workspace(lds.workspace_bytes(pr.n, pr.m, pr.d, 0, precision))
+    f = torch.empty(pr.n, device="cuda")
+    g = torch.empty(pr.m, device="cuda")
+    loss = torch.empty((), dtype=torch.float64, device="cuda")
+
+    def step():
+        lds.sinkhorn_solve(X, Y, a, b, eps, 12, precision=precision, f_out=f, g_out=g,
+                           loss_out=loss, workspace=ws)
+
+    timer = lds.KernelTimer().start()
+    step()
+    torch.cuda.synchronize()
+    assert timer.read(lds.KernelTimer.LSE)[0] == 1  # the persistent solve ran
+    timer.stop()
+    f_direct, g_direct, l_direct = f.clone(), g.clone(), loss.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg):
+        step()
+    for _ in range(2):
+        f.zero_()
+        g.zero_()
+        cg.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(f, f_direct) and torch.equal(g, g_direct)
+        assert float(loss) == float(l_direct)
+    assert lds.workspace_status(ws) == 0
+
+
 def test_captured_grad_and_apply_replay_bitwise(cuda_lib):
     lds = cuda_lib
     pr = scaled_workload(5, n=300, iters=10)
