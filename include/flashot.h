@@ -136,6 +136,13 @@ size_t flashot_workspace_bytes(int64_t n, int64_t m, int64_t d, int64_t k, int f
  * in is read first). eps_sched is a HOST array of n_stages floats (annealing schedule).
  * Writes f (n floats), g (m floats) and, if loss != NULL, *loss (ONE device double) =
  * sum_i a_i f_i + sum_j b_j g_j after the final g-update.
+ * Launches: one LSE pass and one merge per half-step; for tensor-core precisions with a
+ * short contraction (bf16 d <= 192, tf32 d <= 96, split tf32 d <= 64), at most 32 eps
+ * stages and at least 1.5 tiles of 128 x 256 scores per SM and pass, every half-step runs
+ * in one cooperative launch instead (all its CTAs, at most one per SM, resident together;
+ * a grid-wide barrier separates the passes). Both give the same bits.
+ * FLASHOT_SHORT_SOLVE=0 in the environment keeps the per-pass launches, =1 takes the
+ * single launch whenever the contraction and stage count allow.
  */
 int flashot_sinkhorn_solve(const float *X, const float *Y, const float *a, const float *b,
                            int64_t n, int64_t m, int64_t d, const float *eps_sched,
