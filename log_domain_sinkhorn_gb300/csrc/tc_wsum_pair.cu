@@ -449,18 +449,26 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
         const uint32_t s_addr = tmem + lane_base + (uint32_t)h * 128u;
         uint64_t sw2 = 0ull, hd2 = 0ull;
         if constexpr (!kAlias) {
-          // bf16 / Hadamard: the 128-column half row in two 64-column loads; S may be
-          // overwritten once both are in registers.
-          uint32_t wp[kHad ? 1 : 64];
+          // bf16 / Hadamard: the 128-column half row in two 64-column loads, both taken
+          // before any arithmetic so that S is released (and the next unit's S MMA can
+          // start) as early as possible; bf16 writes each half's 64 weights (32 bf16 pairs)
+          // to tensor memory as soon as they are formed.
+          float va[64], vb[64];
+          ptx::tmem_ld_x64_sync(s_addr, va);
+          ptx::tmem_ld_x64_sync(s_addr + 64, vb);
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&ctl.s_empty);
+          if constexpr (!kHad) {
+            // W row rloc, K = 128h .. 128h + 127: 64 columns of bf16 pairs at TMEM column
+            // 256 + 64h, once the previous unit's W V has read W.
+            if (!ptx::mbar_wait(&ctl.w_empty, par(w_uses) ^ 1u)) { ok = false; break; }
+            ptx::tc_fence_after();
+          }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
-            float v[64];
-            ptx::tmem_ld_x64_sync(s_addr + 64 * half, v);
-            if (half == 1) {
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(&ctl.s_empty);
-            }
+            float (&v)[64] = half ? vb : va;
+            uint32_t wp[kHad ? 1 : 32];
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
               const float4 b4 = __ldg(cb + 16 * half + j / 4);
@@ -480,18 +488,15 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
               } else {
                 __nv_bfloat162 h01 = __floats2bfloat162_rn(w0, w1);
                 __nv_bfloat162 h23 = __floats2bfloat162_rn(w2, w3);
-                wp[32 * half + j / 2] = *reinterpret_cast<uint32_t*>(&h01);
-                wp[32 * half + j / 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
+                wp[j / 2] = *reinterpret_cast<uint32_t*>(&h01);
+                wp[j / 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
               }
               sw2 = ptx::add2(sw2, ptx::add2(w01, w23));
             }
+            if constexpr (!kHad)
+              ptx::tmem_st_x32_sync(tmem + lane_base + kTmemW + (uint32_t)h * 64u + 32u * half, wp);
           }
           if constexpr (!kHad) {
-            // This warp's 128 weights are W row rloc, K = 128h .. 128h + 127: 64 columns of
-            // bf16 pairs at TMEM column 256 + 64h, once the previous unit's W V has read W.
-            if (!ptx::mbar_wait(&ctl.w_empty, par(w_uses) ^ 1u)) { ok = false; break; }
-            ptx::tc_fence_after();
-            ptx::tmem_st_x64_sync(tmem + lane_base + kTmemW + (uint32_t)h * 64u, wp);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&ctl.w_full);
