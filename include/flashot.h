@@ -115,10 +115,12 @@ int flashot_timer_read(int kernel_class, int64_t *launches, double *total_ms);
 int flashot_timer_stop(void);
 
 /* Self-test of the bounded waits the tensor-core kernels use: one CTA waits on an mbarrier
- * that nothing ever arrives on, gives up after limit_ns (1e6 .. 2e9 ns), records the
- * timeout in the status word of ws (>= 256 bytes, 256-byte aligned, device memory) and
- * returns normally; flashot_workspace_status(ws, stream) then reports
- * FLASHOT_ERR_DEVICE_TIMEOUT and the context stays usable. No fault, no trap. */
+ * that nothing ever arrives on, then one thread waits, as at the grid barrier of the
+ * persistent solve, for a word of ws (byte 128, zeroed first) that nothing writes; each
+ * gives up after limit_ns (1e6 .. 2e9 ns) and records the timeout in the status word of ws
+ * (>= 256 bytes, 256-byte aligned, device memory): bit 0 for any wait, bit 1 also for the
+ * grid-barrier wait. The call returns normally; flashot_workspace_status(ws, stream) then
+ * reports FLASHOT_ERR_DEVICE_TIMEOUT and the context stays usable. No fault, no trap. */
 int flashot_selftest_bounded_wait(void *ws, int64_t limit_ns, flashot_stream_t stream);
 
 /* Bytes of workspace needed for calls with these sizes and flags. k is the column count

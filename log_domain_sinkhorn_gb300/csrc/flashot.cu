@@ -753,8 +753,11 @@ int flashot_selftest_bounded_wait(void* ws, int64_t limit_ns, flashot_stream_t s
   if (rc != FLASHOT_OK) return rc;
   if (!is_device_ptr(ws)) return FLASHOT_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FLASHOT_ERR_ALIGNMENT;
-  rc = tc_selftest_bounded_wait(static_cast<unsigned*>(ws), limit_ns,
-                                reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* status = static_cast<unsigned*>(ws);
+  rc = tc_selftest_bounded_wait(status, limit_ns, st);
+  // then the grid barrier's wait, on the word at byte 128 of ws
+  if (rc == FLASHOT_OK) rc = tc_selftest_grid_wait(status, status + 32, limit_ns, st);
   return rc == FLASHOT_OK ? launch_check() : rc;
 }
 

@@ -121,6 +121,26 @@ __device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* p) {
   return v;
 }
 
+// Status-word bit set, besides kErrTimeout, when a grid-barrier wait gives up.
+constexpr unsigned kErrGridTimeout = 2u;
+
+// The grid barrier's wait: until *bar >= target (relaxed polling, then an acquire fence that
+// pairs with the arrivals' release fences); false once limit_ns have passed.
+__device__ __forceinline__ bool grid_wait(const unsigned* bar, unsigned target,
+                                          uint64_t limit_ns) {
+  bool arrived = ld_relaxed_gpu(bar) >= target;
+  if (!arrived) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+#pragma unroll 1
+      for (int i = 0; i < 32 && !arrived; ++i) arrived = ld_relaxed_gpu(bar) >= target;
+      if (arrived || ptx::globaltimer() - t0 > limit_ns) break;
+    }
+  }
+  fence_acq_rel_gpu();
+  return arrived;
+}
+
 // This CTA's stream-K range of side s (empty when the side uses fewer CTAs).
 __device__ __forceinline__ void cta_range(const Side& S, int64_t cta, int64_t& tb, int64_t& te) {
   if (cta < S.G) {
@@ -445,18 +465,8 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
         fence_acq_rel_gpu();
         const unsigned target = (unsigned)((p + 1) * (int64_t)gridDim.x);
         atom_add_relaxed_gpu(P.grid_bar, 1u);
-        bool arrived = ld_relaxed_gpu(P.grid_bar) >= target;
-        if (!arrived) {
-          const uint64_t t0 = ptx::globaltimer();
-          while (true) {
-#pragma unroll 1
-            for (int i = 0; i < 32 && !arrived; ++i) arrived = ld_relaxed_gpu(P.grid_bar) >= target;
-            if (arrived || ptx::globaltimer() - t0 > ptx::kWaitLimitNs) break;
-          }
-        }
-        fence_acq_rel_gpu();
-        if (!arrived) {
-          atomicOr(P.status, kErrTimeout);
+        if (!grid_wait(P.grid_bar, target, ptx::kWaitLimitNs)) {
+          atomicOr(P.status, kErrTimeout | kErrGridTimeout);
           ctl.epi_abort[p & 1] = 1;
         }
       }
@@ -472,6 +482,14 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Self-test of the grid barrier's bounded wait: one thread waits for a word that nothing
+// writes to reach 1, gives up after limit_ns and records it in the status word.
+__global__ void grid_wait_selftest_kernel(const unsigned* __restrict__ word, uint64_t limit_ns,
+                                          unsigned* __restrict__ status) {
+  if (threadIdx.x == 0 && !ssolve::grid_wait(word, 1u, limit_ns))
+    atomicOr(status, kErrTimeout | ssolve::kErrGridTimeout);
 }
 
 namespace {
@@ -496,6 +514,15 @@ bool smem_plan(int kc, int* dyn, int* stages, int* a_bufs) {
 
 }  // namespace
 }  // namespace tc
+
+int tc_selftest_grid_wait(unsigned* status, unsigned* word, int64_t limit_ns, cudaStream_t st) {
+  if (cudaMemsetAsync(word, 0, sizeof(unsigned), st) != cudaSuccess) return FLASHOT_ERR_CUDA;
+  {
+    TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
+    tc::grid_wait_selftest_kernel<<<1, 32, 0, st>>>(word, (uint64_t)limit_ns, status);
+  }
+  return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
+}
 
 size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad) {
   // grid barrier word (own 128-byte line), then one counter per row tile of each side

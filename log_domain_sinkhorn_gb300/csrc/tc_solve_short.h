@@ -8,6 +8,10 @@
 
 namespace flashot {
 
+// Self-test of the grid barrier's bounded wait: zeroes *word, then one thread waits for it to
+// reach 1 (nothing writes it), gives up after limit_ns and sets bits 1 and 2 of *status.
+int tc_selftest_grid_wait(unsigned* status, unsigned* word, int64_t limit_ns, cudaStream_t st);
+
 // Bytes of device memory the persistent solve needs for its arrival counters and grid
 // barrier word (zeroed by tc_short_solve itself on `st`).
 size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad);

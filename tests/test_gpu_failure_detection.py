@@ -1,7 +1,8 @@
 """Failure detection without a GPU fault: a kernel waits on a barrier that nothing ever
-arrives on; the bounded wait gives up after a short limit, the kernel records the timeout
-in the workspace status word and returns, the host reads the status, and the context keeps
-working. No trap, no illegal address, no endless loop."""
+arrives on, and another polls a grid-barrier word that nothing writes; each bounded wait
+gives up after a short limit, the kernel records the timeout in the workspace status word
+and returns, the host reads the status, and the context keeps working. No trap, no illegal
+address, no endless loop."""
 import numpy as np
 import pytest
 import torch
@@ -21,6 +22,9 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     st = lds.library().flashot_selftest_bounded_wait(ws.ptr, 50_000_000,
                                                      torch.cuda.current_stream().cuda_stream)
     assert st == _binding.OK
+    torch.cuda.synchronize()
+    # both waits gave up: bit 0 (any bounded wait) and bit 1 (the grid-barrier wait)
+    assert int(ws.buf[0:4].view(torch.int32).item()) == 3
     assert lds.workspace_status(ws) == _binding.ERR_DEVICE_TIMEOUT
     # The word is cleared by the read, and the context is still usable afterwards.
     assert lds.workspace_status(ws) == _binding.OK
