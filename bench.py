@@ -506,6 +506,12 @@ def run_other_workload(args):
                                                    clk_rec.get("sm_mhz"), pk_mhz)
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["sfu_frac"] = (per_launch_scores / avg) / (sms * SFU_EX2_PER_SM_CLK * clk)
+    # The governing roofline is the unit whose floor for this work is longest, i.e. the
+    # larger of the two fractions at the run's clock (tensor or FMA pipe, the tensor peak
+    # rescaled to the run clock, against the SFU's one ex2 per score).
+    own = roof.get("frac_clock_matched") or roof["frac"]
+    roof["governing"] = "sfu (ex2)" if roof["sfu_frac"] > own else roof["bound"]
+    roof["governing_frac"] = max(roof["sfu_frac"], own)
     if prec == "fp32" and d <= 32:
         # FMA-pipe work per score of the small-d CUDA-core LSE: the padded dot product
         # (d_pad lanes), kappa * dot + bias, the max shift and the sum (the max itself runs
