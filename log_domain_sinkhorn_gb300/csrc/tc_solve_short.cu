@@ -609,8 +609,14 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mXr, mYc, mYr, mXc, P) != cudaSuccess)
-      return FLASHOT_ERR_CUDA;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mXr, mYc, mYr, mXc, P);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+      // fewer SMs free for co-residency than the occupancy query promised: the per-pass
+      // path runs instead (the counters zeroed above are not read by it)
+      cudaGetLastError();
+      return FLASHOT_ERR_NOT_IMPLEMENTED;
+    }
+    if (e != cudaSuccess) return FLASHOT_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }

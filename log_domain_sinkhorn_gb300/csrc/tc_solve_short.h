@@ -22,10 +22,11 @@ size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad);
 // elements), alpha / beta the squared norms, la2 / lb2 the log2 weights, biasF the F pass's
 // column bias on entry (from the initial g), f and g the potentials written. partial holds
 // max_splits x max(n_pad, m_pad) float2. Returns FLASHOT_ERR_NOT_IMPLEMENTED, having enqueued
-// nothing, when the solve does not qualify (a longer contraction, more than 32 eps stages, a
-// grid that cannot be co-resident, fewer than 1.5 tiles per CTA and pass on either side, or
-// FLASHOT_SHORT_SOLVE=0 in the environment; FLASHOT_SHORT_SOLVE=1 drops the tile-count
-// condition); the caller then runs the per-pass path.
+// nothing the per-pass path reads (at most the zeroing of sync_words), when the solve does
+// not qualify: a longer contraction, more than 32 eps stages, a grid that cannot be
+// co-resident (or a cooperative launch refused for that), fewer than 1.5 tiles per CTA and
+// pass on either side, or FLASHOT_SHORT_SOLVE=0 in the environment (FLASHOT_SHORT_SOLVE=1
+// drops the tile-count condition). The caller then runs the per-pass path.
 int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t m,
                    int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
                    const float* beta, const float* la2, const float* lb2, float* biasF,
