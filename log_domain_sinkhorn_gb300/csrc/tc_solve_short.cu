@@ -84,13 +84,7 @@ struct __align__(128) Ctrl {
   uint32_t tmem_base;
   int merge_first, merge_last;  // end of pass: this CTA merges its first / last row tile
   int epi_abort[2];             // a failed wait in pass p (slot p % 2): the epilogue stops
-  int abort_flag;
 };
-
-__device__ __forceinline__ void flag_error(Ctrl& ctl, unsigned* status) {
-  atomicOr(status, kErrTimeout);
-  ctl.abort_flag = 1;
-}
 
 // The 256 epilogue threads (named barrier 1; barrier 0 is __syncthreads).
 __device__ __forceinline__ void epi_sync() {
@@ -208,7 +202,6 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       ptx::mbar_init(&ctl.a_empty[b], 1);
     }
     ptx::mbar_init(&ctl.mma_done, 1);
-    ctl.abort_flag = 0;
     ctl.epi_abort[0] = ctl.epi_abort[1] = 0;
     ptx::fence_barrier_init();
   }
@@ -265,7 +258,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
           t = seg_end;
         }
       }
-      if (!ok) flag_error(ctl, P.status);
+      if (!ok) atomicOr(P.status, kErrTimeout);
       // Drain: every copy issued must have landed before the CTA may exit.
       for (int s = 0; s < stages; ++s) {
         const int64_t arms = issued / stages + (s < issued % stages ? 1 : 0);
@@ -326,7 +319,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
           t = seg_end;
         }
       }
-      if (!ok) flag_error(ctl, P.status);
+      if (!ok) atomicOr(P.status, kErrTimeout);
       // Every MMA issued must have retired before Tensor Memory is released.
       ptx::umma_commit(&ctl.mma_done);
       ptx::mbar_wait(&ctl.mma_done, 0);
@@ -473,7 +466,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       epi_sync();
       if (ctl.epi_abort[p & 1]) break;
     }
-    if (!ok) flag_error(ctl, P.status);
+    if (!ok) atomicOr(P.status, kErrTimeout);
   }
 
   ptx::tc_fence_before();
