@@ -14,12 +14,10 @@
 //     still finishing the current pass;
 //   - the eight epilogue warps run the online (max, sum) of the per-pass kernel on the same
 //     tiles, the same stream-K ranges and the same partial slots;
-//   - at the end of a pass each CTA counts itself done on the row tiles it shares with other
-//     CTAs (one counter per row tile); the last owner of a row tile merges that tile's
-//     partials in fixed slot order (the merge of lse_combine_kernel) and writes the potential
-//     and the bias the next pass reads;
-//   - a grid-wide barrier (one counter, release / acquire at GPU scope, bounded wait)
-//     separates the passes, since the next pass's biases are the merged values.
+//   - at the end of a pass a grid-wide barrier (one counter, release / acquire at GPU scope,
+//     bounded wait) waits for every CTA's partials; then every CTA merges an equal share of
+//     the rows (the merge of lse_combine_kernel, slots in fixed order), writing the potential
+//     and the bias the next pass reads, and a second barrier publishes the merges.
 // The arithmetic, and so every bit of the result, is that of the per-pass path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -61,13 +59,12 @@ struct Side {
   float* pot;              // the potential the pass writes
   const float* col_bias;   // bias of the column points (read)
   float* next_bias;        // bias of the row points, read by the other side's pass
-  unsigned* counters;      // per row tile: owners done, over all passes of this side
 };
 
 struct Params {
   Side side[2];
   float2* partial;         // stream-K partials of the current pass, slot * rows_pad + row
-  unsigned* grid_bar;      // CTAs arrived, over all passes
+  unsigned* grid_bar;      // arrivals at the grid barriers, over all passes (two per pass)
   unsigned* status;
   int kc, stages, a_bufs, n_stages, iters_per_stage;
   float eps[kMaxEps];
@@ -82,8 +79,11 @@ struct __align__(128) Ctrl {
   uint64_t a_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
-  int merge_first, merge_last;  // end of pass: this CTA merges its first / last row tile
-  int epi_abort[2];             // a failed wait in pass p (slot p % 2): the epilogue stops
+  // A failed wait in pass p: slot [p % 2][0] for the tiles, [p % 2][1] and [p % 2][2] for
+  // the pass's two grid barriers. Each is written in one phase of the pass and read by every
+  // epilogue thread after the named barrier that closes that phase; it is next written two
+  // passes later, after every thread has read it.
+  int epi_abort[2][3];
 };
 
 // The 256 epilogue threads (named barrier 1; barrier 0 is __syncthreads).
@@ -145,11 +145,6 @@ __device__ __forceinline__ void cta_range(const Side& S, int64_t cta, int64_t& t
   }
 }
 
-// Number of CTAs whose ranges touch row tile rt.
-__device__ __forceinline__ int64_t row_tile_owners(const Side& S, int64_t rt) {
-  return sk_owner((rt + 1) * S.NT - 1, S.T, S.G) - sk_owner(rt * S.NT, S.T, S.G) + 1;
-}
-
 // eps of pass p and the ratio eps / eps_next the merge folds into the next bias (the
 // G-update at the end of a stage hands over to the next stage's eps).
 __device__ __forceinline__ void pass_eps(const Params& P, int64_t p, float& eps,
@@ -202,7 +197,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       ptx::mbar_init(&ctl.a_empty[b], 1);
     }
     ptx::mbar_init(&ctl.mma_done, 1);
-    ctl.epi_abort[0] = ctl.epi_abort[1] = 0;
+    for (int i = 0; i < 6; ++i) (&ctl.epi_abort[0][0])[i] = 0;
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -341,6 +336,21 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
     uint32_t acc_ph = 0;
     int bs = 0;
     bool ok = true;
+    // Grid barrier among all CTAs' epilogues (thread 0 of the epilogue arrives and waits;
+    // the named barriers around it order the other epilogue threads' writes before the
+    // arrival and their later reads after the wait). On time-out the pass's abort flag is
+    // set, which every epilogue thread reads after the closing named barrier.
+    auto grid_barrier = [&](unsigned target, int& abort_flag) {
+      if (etid == 0) {
+        fence_acq_rel_gpu();
+        atom_add_relaxed_gpu(P.grid_bar, 1u);
+        if (!grid_wait(P.grid_bar, target, ptx::kWaitLimitNs)) {
+          atomicOr(P.status, kErrTimeout | kErrGridTimeout);
+          abort_flag = 1;
+        }
+      }
+      epi_sync();
+    };
     for (int64_t p = 0; p < n_pass; ++p) {
       const Side& S = P.side[p & 1];
       float eps, ratio;
@@ -405,31 +415,17 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       asm volatile("cp.async.wait_group 0;" ::: "memory");
 
       // ---- end of the pass ----------------------------------------------------------------
-      // (1) every partial of this CTA is written; a failed wait anywhere ends the solve here
-      if (!ok) ctl.epi_abort[p & 1] = 1;
+      // A failed wait anywhere ends the solve at the next check: every epilogue warp reads
+      // the pass's abort flag after the same named barrier.
+      int* abort_flags = ctl.epi_abort[p & 1];
+      if (!ok) abort_flags[0] = 1;
       epi_sync();
-      if (ctl.epi_abort[p & 1]) break;
-      // (2) count this CTA done on the row tiles it shares; the last owner merges
-      const int64_t rt0 = tb < te ? tb / NT : 0, rt1 = tb < te ? (te - 1) / NT : -1;
-      if (etid == 0) {
-        int first = 0, last = 0;
-        if (tb < te) {
-          fence_acq_rel_gpu();  // the epilogue's partials before the arrivals
-          const int64_t o0 = row_tile_owners(S, rt0);
-          const int64_t o1 = rt1 != rt0 ? row_tile_owners(S, rt1) : 1;
-          const unsigned a0 = o0 > 1 ? atom_add_relaxed_gpu(S.counters + rt0, 1u) : 0u;
-          const unsigned a1 = o1 > 1 ? atom_add_relaxed_gpu(S.counters + rt1, 1u) : 0u;
-          first = o0 == 1 || (a0 + 1u) % (unsigned)o0 == 0u;
-          last = rt1 != rt0 && (o1 == 1 || (a1 + 1u) % (unsigned)o1 == 0u);
-          // the last arrival on a shared row tile: the other owners' partials are visible
-          if ((first && o0 > 1) || (last && o1 > 1)) fence_acq_rel_gpu();
-        }
-        ctl.merge_first = first;
-        ctl.merge_last = last;
-      }
-      epi_sync();
-      // (3) merge: new potential and next bias of every row of the row tiles this CTA owns
-      // last, partials read from L2 in fixed slot order
+      if (abort_flags[0]) break;
+      // (1) barrier: every CTA's partials of this pass are written
+      grid_barrier((unsigned)((2 * p + 1) * (int64_t)gridDim.x), abort_flags[1]);
+      if (abort_flags[1]) break;
+      // (2) merge: this CTA's equal share of the rows, partials read from L2 in fixed slot
+      // order; new potential and next bias of each row
       {
         CombineArgs args;
         args.rows = S.n_rows;
@@ -445,26 +441,15 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
         args.err_w = nullptr;
         args.err_rows = nullptr;
         const SplitInfo split{0, 2, S.T, S.G, NT, kBM};
-        const int mf = ctl.merge_first, ml = ctl.merge_last;
-        for (int64_t r = etid; r < (rt1 - rt0 + 1) * kBM; r += kEpiThreads) {
-          const int64_t rt = rt0 + r / kBM;
-          const bool mine = rt == rt0 ? mf != 0 : (rt == rt1 ? ml != 0 : true);
-          if (mine) combine_row<true>(P.partial, S.rows_pad, split, rt * kBM + r % kBM, args);
-        }
+        const int64_t share = (S.rows_pad + gridDim.x - 1) / gridDim.x;
+        const int64_t r_end = min(S.rows_pad, (cta + 1) * share);
+        for (int64_t r = cta * share + etid; r < r_end; r += kEpiThreads)
+          combine_row<true>(P.partial, S.rows_pad, split, r, args);
       }
       epi_sync();
-      // (4) grid barrier: every CTA's merges are visible before any CTA reads the new biases
-      if (etid == 0) {
-        fence_acq_rel_gpu();
-        const unsigned target = (unsigned)((p + 1) * (int64_t)gridDim.x);
-        atom_add_relaxed_gpu(P.grid_bar, 1u);
-        if (!grid_wait(P.grid_bar, target, ptx::kWaitLimitNs)) {
-          atomicOr(P.status, kErrTimeout | kErrGridTimeout);
-          ctl.epi_abort[p & 1] = 1;
-        }
-      }
-      epi_sync();
-      if (ctl.epi_abort[p & 1]) break;
+      // (3) barrier: every merge is visible before any CTA reads the new biases
+      grid_barrier((unsigned)((2 * p + 2) * (int64_t)gridDim.x), abort_flags[2]);
+      if (abort_flags[2]) break;
     }
     if (!ok) atomicOr(P.status, kErrTimeout);
   }
@@ -518,8 +503,10 @@ int tc_selftest_grid_wait(unsigned* status, unsigned* word, int64_t limit_ns, cu
 }
 
 size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad) {
-  // grid barrier word (own 128-byte line), then one counter per row tile of each side
-  return (size_t)(32 + n_pad / tc::ssolve::kBM + m_pad / tc::ssolve::kBM) * sizeof(unsigned);
+  // the grid barrier's word, on a 128-byte line of its own
+  (void)n_pad;
+  (void)m_pad;
+  return 32 * sizeof(unsigned);
 }
 
 int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t m,
@@ -556,7 +543,7 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   if (mode == 2 && (2 * rtX * NTY < 3 * GF || 2 * rtY * NTX < 3 * GG))
     return FLASHOT_ERR_NOT_IMPLEMENTED;
   const int64_t n_pass = 2LL * n_stages * iters_per_stage;
-  if (n_pass * grid >= (1LL << 31)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  if (2 * n_pass * grid >= (1LL << 31)) return FLASHOT_ERR_NOT_IMPLEMENTED;
   auto kern = bf16 ? lse_solve_short_kernel<true> : lse_solve_short_kernel<false>;
   if (set_smem(kern, dyn) != FLASHOT_OK) return FLASHOT_ERR_CUDA;
   // Every CTA must be resident at once (the grid barrier); the cooperative launch checks it
@@ -576,8 +563,8 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   if (rc != FLASHOT_OK) return rc;
   unsigned* words = static_cast<unsigned*>(sync_words);
   Params P = {};
-  P.side[0] = Side{n, n_pad, NTY, rtX * NTY, GF, alpha, la2, f, biasF, biasG, words + 32};
-  P.side[1] = Side{m, m_pad, NTX, rtY * NTX, GG, beta, lb2, g, biasG, biasF, words + 32 + rtX};
+  P.side[0] = Side{n, n_pad, NTY, rtX * NTY, GF, alpha, la2, f, biasF, biasG};
+  P.side[1] = Side{m, m_pad, NTX, rtY * NTX, GG, beta, lb2, g, biasG, biasF};
   P.partial = partial;
   P.grid_bar = words;
   P.status = status;
@@ -605,7 +592,7 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mXr, mYc, mYr, mXc, P);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
       // fewer SMs free for co-residency than the occupancy query promised: the per-pass
-      // path runs instead (the counters zeroed above are not read by it)
+      // path runs instead (the barrier word zeroed above is not read by it)
       cudaGetLastError();
       return FLASHOT_ERR_NOT_IMPLEMENTED;
     }
