@@ -519,9 +519,10 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   using namespace tc::ssolve;
   // FLASHOT_SHORT_SOLVE in the environment: 0 keeps the per-pass path, 1 takes the
   // persistent solve whenever it applies; unset, it is taken when the CTAs average at least
-  // 1.5 tiles per pass on both sides (with one each, the end-of-pass counting and grid
-  // barrier cost more than the launches they replace: measured 25-30 % slower at 2048^2,
-  // one tile per CTA, and 11-22 % faster at 3072^2 and 4096^2, 1.9 and 3.4, d = 16..128).
+  // 1.5 tiles per pass on both sides (with one each, the two grid barriers and the merge
+  // cost more than the launches they replace: measured 21-34 % slower at 512^2 to 2048^2,
+  // one tile per CTA, and 11-28 % faster at 3072^2 and 4096^2, 1.9 and 3.4 tiles per CTA,
+  // 2-10 % from 6144^2, d = 16..128).
   static const int mode = [] {
     const char* e = std::getenv("FLASHOT_SHORT_SOLVE");
     return e && e[0] == '0' ? 0 : (e && e[0] == '1' ? 1 : 2);
