@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 
 #include "flashot.h"
 #include "common.cuh"
@@ -76,6 +77,45 @@ __device__ __forceinline__ void flag_error(PCtrl& ctl, unsigned* status) {
 __device__ __forceinline__ uint32_t par(int64_t n) { return (uint32_t)(n & 1); }
 
 // Shape of the V^T operand of one unit, per CTA: kKV / 2 rows (output columns) x 256 K.
+// The segments a pair walks, each a run of consecutive units of one row group (one output
+// group and pair tile), and the partial slot each writes:
+//   run_len == 0: the pair's stream-K range, in SegOrder's order, slot = the pair's rank
+//                 among the row group's owners;
+//   run_len > 0:  round-robin runs of run_len column tiles: run r = pair + i G covers row
+//                 group r / R and column tiles (r % R) run_len .. + run_len (R runs per row
+//                 group), slot = r % R. At any moment the pairs then work on a few row
+//                 groups, several pairs on each, all at the same column offsets of their
+//                 runs, so the row and column tiles in use fit in L2 even when the pairs'
+//                 row tiles alone would not (split tf32 at large d).
+struct Walk {
+  SegOrder so;
+  int64_t pair, G, NT, L, R, n;
+  __device__ __forceinline__ Walk(int64_t pair_, int64_t G_, int64_t T, int64_t NT_,
+                                  int64_t run_len)
+      : so(sk_begin(pair_, T, G_), sk_begin(pair_ + 1, T, G_), NT_), pair(pair_), G(G_),
+        NT(NT_), L(run_len), R(run_len > 0 ? (NT_ + run_len - 1) / run_len : 1), n(0) {
+    if (L == 0) {
+      n = so.n;
+    } else {
+      const int64_t runs = (T / NT) * R;
+      n = runs > pair ? (runs - pair + G - 1) / G : 0;
+    }
+  }
+  __device__ __forceinline__ void get(int64_t i, int64_t& a, int64_t& b) const {
+    if (L == 0) {
+      so.get(i, a, b);
+      return;
+    }
+    const int64_t r = pair + i * G, vr = r / R, k = r - vr * R;
+    a = vr * NT + k * L;
+    b = vr * NT + min(NT, (k + 1) * L);
+  }
+  // Partial slot of the segment that starts at unit a (row group vr).
+  __device__ __forceinline__ int64_t slot(int64_t a, int64_t vr, int64_t T) const {
+    return L == 0 ? pair - sk_owner(vr * NT, T, G) : (a - vr * NT) / L;
+  }
+};
+
 template <int kPrec, int kKV>
 struct VShape {
   static constexpr int rows = kKV / 2;                       // per CTA
@@ -93,7 +133,8 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
                  const __grid_constant__ CUtensorMap mapVlo,
                  const __grid_constant__ CUtensorMap mapVb, const float* __restrict__ colBias,
                  const float* __restrict__ rowBias, int64_t n_rows, int64_t pair_tiles,
-                 int64_t NT, int64_t T, int kc_count, int kps, int n_st, float kappa,
+                 int64_t NT, int64_t T, int64_t run_len, int kc_count, int kps, int n_st,
+                 float kappa,
                  float* __restrict__ pO, float2* __restrict__ pW, int64_t ldp,
                  unsigned* __restrict__ status) {
   extern __shared__ uint8_t dyn_smem[];
@@ -126,8 +167,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
   const uint32_t stage_bytes = (uint32_t)kps * kChunkBytes;
   const uint32_t v_base = (uint32_t)n_st * stage_bytes;
   const int64_t G = gridDim.x / 2, pair = blockIdx.x / 2;
-  const int64_t t_begin = sk_begin(pair, T, G), t_end = sk_begin(pair + 1, T, G);
-  const SegOrder so(t_begin, t_end, NT);  // every role walks the segments in this order
+  const Walk so(pair, G, T, NT, run_len);  // every role walks the segments in this order
   auto leader = [&](uint64_t* bar) { return ptx::mapa_shared(ptx::smem_u32(bar), 0u); };
   // Barriers that the odd CTA's epilogue arrivals reach through a forwarder: local count 8,
   // plus the forwarder's one arrival in the even CTA.
@@ -572,7 +612,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
         }
       }
       if (!ok) break;
-      const int64_t slot = pair - sk_owner(vr * NT, T, G);
+      const int64_t slot = so.slot(t, vr, T);
       const int64_t prow = vr * 2 * kBM + rank * kBM + rloc;  // row of the partial buffers
       if constexpr (!kHad) {
         if (!ptx::mbar_wait(&ctl.o_full, par(segs))) { ok = false; break; }
@@ -618,7 +658,7 @@ wsum_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant
 template <int kMode>
 __global__ void wsum_pair_reduce_kernel(const float* __restrict__ pO, const float2* __restrict__ pW,
                                         int64_t ldp, int kKV, int64_t pair_tiles, int64_t NT,
-                                        int64_t T, int64_t G, int64_t n_rows,
+                                        int64_t T, int64_t G, int64_t run_len, int64_t n_rows,
                                         const float* __restrict__ rowW, const float* __restrict__ X,
                                         int64_t d, int64_t k, float* __restrict__ out,
                                         int64_t ldo) {
@@ -631,7 +671,8 @@ __global__ void wsum_pair_reduce_kernel(const float* __restrict__ pO, const floa
   const int64_t grp = vr / pair_tiles;
   const int64_t row = (vr - grp * pair_tiles) * 2 * kBM + (prow - vr * 2 * kBM);
   if (row >= n_rows) return;
-  const int slots = (int)(sk_owner((vr + 1) * NT - 1, T, G) - sk_owner(vr * NT, T, G) + 1);
+  const int slots = run_len > 0 ? (int)((NT + run_len - 1) / run_len)
+                                : (int)(sk_owner((vr + 1) * NT - 1, T, G) - sk_owner(vr * NT, T, G) + 1);
   if constexpr (kMode == kWsumHadamard) {
     float hsum = 0.0f;
     for (int s = 0; s < slots; ++s)
@@ -699,8 +740,8 @@ template <int kPrec, int kKV>
 static int launch(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mV,
                   const CUtensorMap& mVlo, const CUtensorMap& mVb, const float* colBias,
                   const float* rowBias, int64_t n_rows, int64_t pair_tiles, int64_t NT, int64_t T,
-                  int64_t pairs, int kc, float kappa, float* pO, float2* pW, int64_t ldp,
-                  unsigned* status, cudaStream_t st) {
+                  int64_t run_len, int64_t pairs, int kc, float kappa, float* pO, float2* pW,
+                  int64_t ldp, unsigned* status, cudaStream_t st) {
   int n_st = 0, kps = 1;
   if (!stage_plan(kc, VShape<kPrec, kKV>::bytes, &n_st, &kps)) return FLASHOT_ERR_INVALID_ARG;
   const int dyn = n_st * kps * 2 * kChunk + (int)VShape<kPrec, kKV>::bytes + 1024;
@@ -722,7 +763,7 @@ static int launch(const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, mA, mB, mV, mVlo, mVb, colBias, rowBias, n_rows,
-                           pair_tiles, NT, T, kc, kps, n_st, kappa, pO, pW, ldp,
+                           pair_tiles, NT, T, run_len, kc, kps, n_st, kappa, pO, pW, ldp,
                            status) != cudaSuccess)
       return FLASHOT_ERR_CUDA;
   }
@@ -799,7 +840,19 @@ int tc_wsum_pair_pass(int prec, int mode, const void* rowQ, const void* colQ,
   const int64_t groups = had ? 1 : (k + kv - 1) / kv;
   const int64_t vrows = groups * pair_tiles;
   const int64_t T = vrows * NT;
-  const int64_t G = tc::choose_grid(vrows, NT, std::min(max_clusters(), sms / 2), kMaxOwners);
+  // Split tf32 rows are three tf32 segments long: when the pairs' row tiles alone would fill
+  // most of L2 (d = 512 and up), the pairs take round-robin runs of a quarter of a row
+  // group's column tiles instead of stream-K ranges. FLASHOT_WSUM_RUNS=0 in the environment
+  // keeps stream-K (for comparisons; read once per process).
+  static const bool runs_enabled = [] {
+    const char* e = std::getenv("FLASHOT_WSUM_RUNS");
+    return !(e && e[0] == '0');
+  }();
+  const int64_t max_pairs = std::min(max_clusters(), sms / 2);
+  const bool runs = runs_enabled && split && NT >= 2 &&
+                    max_pairs * 2 * kBM * dpt * (int64_t)sizeof(float) > (96ll << 20);
+  const int64_t run_len = runs ? (NT + kMaxOwners - 1) / kMaxOwners : 0;
+  const int64_t G = runs ? max_pairs : tc::choose_grid(vrows, NT, max_pairs, kMaxOwners);
   const int64_t ldp = vrows * 2 * kBM;
   float* pO = static_cast<float*>(scratch);
   const size_t po_bytes = (size_t)kMaxOwners * ldp * (had ? 0 : kv) * sizeof(float);
@@ -839,8 +892,8 @@ int tc_wsum_pair_pass(int prec, int mode, const void* rowQ, const void* colQ,
     if (rc != FLASHOT_OK) return rc;
   }
 #define FLASHOT_PAIR_WSUM(P, KV)                                                            \
-  launch<P, KV>(mA, mB, mV, mVlo, mVb, colBias, rowBias, n_rows, pair_tiles, NT, T, G, kc, \
-                kappa, pO, pW, ldp, status, st)
+  launch<P, KV>(mA, mB, mV, mVlo, mVb, colBias, rowBias, n_rows, pair_tiles, NT, T, run_len, G, \
+                kc, kappa, pO, pW, ldp, status, st)
   if (had)
     rc = bf ? FLASHOT_PAIR_WSUM(kPrecBF16, 0) : FLASHOT_PAIR_WSUM(kPrecTF32, 0);
   else if (bf)
@@ -858,13 +911,13 @@ int tc_wsum_pair_pass(int prec, int mode, const void* rowQ, const void* colQ,
     TraceScope ts_(FLASHOT_KERNEL_OTHER, st);
     if (mode == kWsumGrad)
       wsum_pair_reduce_kernel<kWsumGrad><<<blocks, 256, 0, st>>>(
-          pO, pW, ldp, kv, pair_tiles, NT, T, G, n_rows, rowW, X, d, k, out, ldo);
+          pO, pW, ldp, kv, pair_tiles, NT, T, G, run_len, n_rows, rowW, X, d, k, out, ldo);
     else if (mode == kWsumApply)
       wsum_pair_reduce_kernel<kWsumApply><<<blocks, 256, 0, st>>>(
-          pO, pW, ldp, kv, pair_tiles, NT, T, G, n_rows, rowW, X, d, k, out, ldo);
+          pO, pW, ldp, kv, pair_tiles, NT, T, G, run_len, n_rows, rowW, X, d, k, out, ldo);
     else
       wsum_pair_reduce_kernel<kWsumHadamard><<<blocks, 256, 0, st>>>(
-          pO, pW, ldp, 1, pair_tiles, NT, T, G, n_rows, rowW, X, d, k, out, ldo);
+          pO, pW, ldp, 1, pair_tiles, NT, T, G, run_len, n_rows, rowW, X, d, k, out, ldo);
   }
   return cudaGetLastError() == cudaSuccess ? FLASHOT_OK : FLASHOT_ERR_CUDA;
 }
