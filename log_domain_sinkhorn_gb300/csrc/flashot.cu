@@ -160,6 +160,11 @@ struct Layout {
       ftilde, lse2, partial, loss, sync, total;
 };
 
+// The stream-K partials of an LSE pass: up to kMaxSplits (max, sum) pairs per row.
+size_t partial_bytes(const Geometry& g) {
+  return (size_t)kMaxSplits * (size_t)std::max(g.n_pad, g.m_pad) * sizeof(float2);
+}
+
 Layout make_layout(const Geometry& g) {
   Layout L{};
   size_t off = 0;
@@ -187,7 +192,7 @@ Layout make_layout(const Geometry& g) {
   L.biasG = take(np * 4);
   L.ftilde = take(np * 4);
   L.lse2 = take(std::max(np, mp) * 4);
-  L.partial = take((size_t)kMaxSplits * std::max(np, mp) * sizeof(float2));
+  L.partial = take(partial_bytes(g));
   L.loss = take(64);
   // Arrival counters and grid barrier of the persistent short-contraction solve.
   if (g.prec != FLASHOT_PREC_FP32) L.sync = take(tc_short_solve_sync_bytes(g.n_pad, g.m_pad));
@@ -794,7 +799,25 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
     // the f-update's arithmetic on identical inputs. One pass per iteration then suffices,
     // and g is copied from f at the end.
     const bool self = X == Y && a == b && n == m && !(flags & FLASHOT_WARM_START);
-    for (int s = 0; s < n_stages; ++s) {
+    // Short tensor-core contractions: every iteration in one persistent launch (the same
+    // passes, merges and biases as below, so the same bits), from the first iteration's
+    // biases.
+    bool done = false;
+    if (c.g.prec != FLASHOT_PREC_FP32) {
+      if ((rc = launch_bias(c, self ? f : g, false, eps_sched[0])) != FLASHOT_OK) return rc;
+      if (!self && (rc = launch_bias(c, f, true, eps_sched[0])) != FLASHOT_OK) return rc;
+      rc = tc_short_solve(c.g.prec == FLASHOT_PREC_BF16, c.at<void>(c.L.xq),
+                          c.at<void>(c.L.yq), n, m, c.g.n_pad, c.g.m_pad, c.g.dpt,
+                          c.at<float>(c.L.alpha), c.at<float>(c.L.beta), c.at<float>(c.L.la2),
+                          c.at<float>(c.L.lb2), c.at<float>(c.L.biasF), c.at<float>(c.L.biasG),
+                          f, g, eps_sched, n_stages, iters_per_stage, self ? 2 : 1,
+                          c.at<float2>(c.L.partial), partial_bytes(c.g), kMaxSplits,
+                          c.at<void>(c.L.sync), tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad),
+                          c.sms, c.at<unsigned>(c.L.status), c.st);
+      if (rc == FLASHOT_OK) done = true;
+      else if (rc != FLASHOT_ERR_NOT_IMPLEMENTED) return rc;
+    }
+    for (int s = 0; !done && s < n_stages; ++s) {
       const float eps = eps_sched[s];
       for (int it = 0; it < iters_per_stage; ++it) {
         if ((rc = launch_bias(c, self ? f : g, false, eps)) != FLASHOT_OK) return rc;
@@ -824,9 +847,10 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
                         m, c.g.n_pad, c.g.m_pad, c.g.dpt, c.at<float>(c.L.alpha),
                         c.at<float>(c.L.beta), c.at<float>(c.L.la2), c.at<float>(c.L.lb2),
                         c.at<float>(c.L.biasF), c.at<float>(c.L.biasG), f, g, eps_sched,
-                        n_stages, iters_per_stage, c.at<float2>(c.L.partial), kMaxSplits,
-                        c.at<void>(c.L.sync), tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad),
-                        c.sms, c.at<unsigned>(c.L.status), c.st);
+                        n_stages, iters_per_stage, 0, c.at<float2>(c.L.partial),
+                        partial_bytes(c.g), kMaxSplits, c.at<void>(c.L.sync),
+                        tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad), c.sms,
+                        c.at<unsigned>(c.L.status), c.st);
     if (rc == FLASHOT_OK) done = true;
     else if (rc != FLASHOT_ERR_NOT_IMPLEMENTED) return rc;
   }

@@ -61,12 +61,23 @@ struct Side {
   float* next_bias;        // bias of the row points, read by the other side's pass
 };
 
+// The update schedules (of the method's alternating form, and the averaged symmetric one
+// whose two updates both read the previous iterate).
+enum Schedule : int {
+  kAlternating = 0,  // f = F(g), then g = G(f): a merge and two grid barriers per half-step
+  kSymmetric = 1,    // f, g = (old + F(g_old)) / 2, (old + G(f_old)) / 2: both passes, then
+                     // one merge of both sides between two grid barriers per iteration
+  kSymmetricSelf = 2 // the same with X = Y and a = b started from f = g: one pass per
+                     // iteration (g stays equal to f)
+};
+
 struct Params {
   Side side[2];
   float2* partial;         // stream-K partials of the current pass, slot * rows_pad + row
-  unsigned* grid_bar;      // arrivals at the grid barriers, over all passes (two per pass)
+  float2* partial_g;       // symmetric: the G-update's partials (the F-update's in partial)
+  unsigned* grid_bar;      // arrivals at the grid barriers, over all passes
   unsigned* status;
-  int kc, stages, a_bufs, n_stages, iters_per_stage;
+  int kc, stages, a_bufs, n_stages, iters_per_stage, schedule;
   float eps[kMaxEps];
 };
 
@@ -145,16 +156,29 @@ __device__ __forceinline__ void cta_range(const Side& S, int64_t cta, int64_t& t
   }
 }
 
+// Passes of the launch and the side (0: F-update, 1: G-update) of pass p.
+__device__ __forceinline__ int64_t pass_count(const Params& P) {
+  const int64_t iters = (int64_t)P.n_stages * P.iters_per_stage;
+  return P.schedule == kSymmetricSelf ? iters : 2 * iters;
+}
+__device__ __forceinline__ int pass_side(const Params& P, int64_t p) {
+  return P.schedule == kSymmetricSelf ? 0 : (int)(p & 1);
+}
+__device__ __forceinline__ int64_t pass_iteration(const Params& P, int64_t p) {
+  return P.schedule == kSymmetricSelf ? p : p >> 1;
+}
+
 // eps of pass p and the ratio eps / eps_next the merge folds into the next bias (the
-// G-update at the end of a stage hands over to the next stage's eps).
+// alternating G-update at the end of a stage hands over to the next stage's eps).
 __device__ __forceinline__ void pass_eps(const Params& P, int64_t p, float& eps,
                                          float& ratio) {
-  const int64_t it = p >> 1;
+  const int64_t it = pass_iteration(P, p);
   const int st = (int)(it / P.iters_per_stage);
   eps = P.eps[st];
   ratio = 1.0f;
   const bool last_of_stage = (it % P.iters_per_stage) == P.iters_per_stage - 1;
-  if ((p & 1) && last_of_stage && st + 1 < P.n_stages) ratio = eps / P.eps[st + 1];
+  if (P.schedule == kAlternating && (p & 1) && last_of_stage && st + 1 < P.n_stages)
+    ratio = eps / P.eps[st + 1];
 }
 
 }  // namespace ssolve
@@ -183,7 +207,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
   const int kc_count = P.kc, stages = P.stages, a_bufs = P.a_bufs;
   const uint32_t a_bytes = (uint32_t)kc_count * kChunk;
   const int64_t cta = blockIdx.x;
-  const int64_t n_pass = 2LL * P.n_stages * P.iters_per_stage;
+  const int64_t n_pass = pass_count(P);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -222,9 +246,10 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       int64_t issued = 0, segs = 0;
       bool ok = true;
       for (int64_t p = 0; ok && p < n_pass; ++p) {
-        const Side& S = P.side[p & 1];
-        const CUtensorMap* mA = (p & 1) ? &mapYr : &mapXr;
-        const CUtensorMap* mB = (p & 1) ? &mapXc : &mapYc;
+        const int side = pass_side(P, p);
+        const Side& S = P.side[side];
+        const CUtensorMap* mA = side ? &mapYr : &mapXr;
+        const CUtensorMap* mB = side ? &mapXc : &mapYc;
         int64_t tb, te;
         cta_range(S, cta, tb, te);
         for (int64_t t = tb; ok && t < te;) {
@@ -274,7 +299,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       int64_t segs = 0;
       bool ok = true;
       for (int64_t p = 0; ok && p < n_pass; ++p) {
-        const Side& S = P.side[p & 1];
+        const Side& S = P.side[pass_side(P, p)];
         int64_t tb, te;
         cta_range(S, cta, tb, te);
         for (int64_t t = tb; ok && t < te;) {
@@ -340,7 +365,9 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
     // the named barriers around it order the other epilogue threads' writes before the
     // arrival and their later reads after the wait). On time-out the pass's abort flag is
     // set, which every epilogue thread reads after the closing named barrier.
-    auto grid_barrier = [&](unsigned target, int& abort_flag) {
+    unsigned barriers = 0;  // grid barriers passed so far
+    auto grid_barrier = [&](int& abort_flag) {
+      const unsigned target = ++barriers * gridDim.x;
       if (etid == 0) {
         fence_acq_rel_gpu();
         atom_add_relaxed_gpu(P.grid_bar, 1u);
@@ -352,7 +379,11 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       epi_sync();
     };
     for (int64_t p = 0; p < n_pass; ++p) {
-      const Side& S = P.side[p & 1];
+      const int side = pass_side(P, p);
+      const Side& S = P.side[side];
+      // this pass's partials: the symmetric G-update keeps its own, since the F-update's
+      // are merged only after it
+      float2* const partial = (P.schedule == kSymmetric && side == 1) ? P.partial_g : P.partial;
       float eps, ratio;
       pass_eps(P, p, eps, ratio);
       const float kappa = 2.0f * kLog2e / eps;
@@ -409,7 +440,7 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
         if (!ok) break;
         const int64_t row = rt * kBM + q * 32 + lane;
         const int64_t slot = 2 * (cta - sk_owner(rt * NT, S.T, S.G)) + par;
-        if (row < S.n_rows) P.partial[slot * S.rows_pad + row] = make_float2(M, Ssum);
+        if (row < S.n_rows) partial[slot * S.rows_pad + row] = make_float2(M, Ssum);
         t = seg_end;
       }
       asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -421,12 +452,15 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
       if (!ok) abort_flags[0] = 1;
       epi_sync();
       if (abort_flags[0]) break;
-      // (1) barrier: every CTA's partials of this pass are written
-      grid_barrier((unsigned)((2 * p + 1) * (int64_t)gridDim.x), abort_flags[1]);
+      // the symmetric F-update's partials wait for the G-update's: both read the previous
+      // iterate, and both merge after the G-update's pass
+      if (P.schedule == kSymmetric && side == 0) continue;
+      // (1) barrier: every CTA's partials of this pass (symmetric: of both passes) are written
+      grid_barrier(abort_flags[1]);
       if (abort_flags[1]) break;
       // (2) merge: this CTA's equal share of the rows, partials read from L2 in fixed slot
       // order; new potential and next bias of each row
-      {
+      if (P.schedule == kAlternating) {
         CombineArgs args;
         args.rows = S.n_rows;
         args.rows_pad = S.rows_pad;
@@ -445,10 +479,47 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
         const int64_t r_end = min(S.rows_pad, (cta + 1) * share);
         for (int64_t r = cta * share + etid; r < r_end; r += kEpiThreads)
           combine_row<true>(P.partial, S.rows_pad, split, r, args);
+      } else {
+        // Symmetric: each side's potential averaged with its previous value, then the bias
+        // the next iteration reads, from the averaged potentials at that iteration's eps
+        // ((pot - norm) log2e / eps + log2 w; -inf on padding rows). The self-transport
+        // problem's single pass also provides the G-side bias (its g equals f).
+        const int64_t it = pass_iteration(P, p);
+        const int64_t n_iters = (int64_t)P.n_stages * P.iters_per_stage;
+        const bool more = it + 1 < n_iters;
+        const float inv_eps_log2e =
+            more ? kLog2e / P.eps[(int)((it + 1) / P.iters_per_stage)] : 0.0f;
+        for (int t = 0; t < (P.schedule == kSymmetric ? 2 : 1); ++t) {
+          const Side& U = P.side[t];
+          const Side& B = P.schedule == kSymmetric ? U : P.side[1];  // whose bias is written
+          CombineArgs args;
+          args.rows = U.n_rows;
+          args.rows_pad = U.rows_pad;
+          args.norms = U.norms;
+          args.eps = eps;
+          args.lw2 = U.lw2;
+          args.eps_ratio = 1.0f;
+          args.out_pot = U.pot;
+          args.next_bias = nullptr;
+          args.out_lse2 = nullptr;
+          args.average = 1;
+          args.err_w = nullptr;
+          args.err_rows = nullptr;
+          const SplitInfo split{0, 2, U.T, U.G, U.NT, kBM};
+          float2* const part = t == 1 ? P.partial_g : P.partial;
+          const int64_t share = (U.rows_pad + gridDim.x - 1) / gridDim.x;
+          const int64_t r_end = min(U.rows_pad, (cta + 1) * share);
+          for (int64_t r = cta * share + etid; r < r_end; r += kEpiThreads) {
+            combine_row<true>(part, U.rows_pad, split, r, args);
+            if (more)
+              B.next_bias[r] =
+                  r < U.n_rows ? (U.pot[r] - B.norms[r]) * inv_eps_log2e + B.lw2[r] : neg_inf();
+          }
+        }
       }
       epi_sync();
       // (3) barrier: every merge is visible before any CTA reads the new biases
-      grid_barrier((unsigned)((2 * p + 2) * (int64_t)gridDim.x), abort_flags[2]);
+      grid_barrier(abort_flags[2]);
       if (abort_flags[2]) break;
     }
     if (!ok) atomicOr(P.status, kErrTimeout);
@@ -513,8 +584,9 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
                    int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
                    const float* beta, const float* la2, const float* lb2, float* biasF,
                    float* biasG, float* f, float* g, const float* eps_sched, int n_stages,
-                   int iters_per_stage, float2* partial, int max_splits, void* sync_words,
-                   size_t sync_bytes, int sms, unsigned* status, cudaStream_t st) {
+                   int iters_per_stage, int schedule, float2* partial, size_t partial_bytes,
+                   int max_splits, void* sync_words, size_t sync_bytes, int sms,
+                   unsigned* status, cudaStream_t st) {
   using namespace tc;
   using namespace tc::ssolve;
   // FLASHOT_SHORT_SOLVE in the environment: 0 keeps the per-pass path, 1 takes the
@@ -543,8 +615,24 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   const int64_t grid = std::max(GF, GG);
   if (mode == 2 && (2 * rtX * NTY < 3 * GF || 2 * rtY * NTX < 3 * GG))
     return FLASHOT_ERR_NOT_IMPLEMENTED;
-  const int64_t n_pass = 2LL * n_stages * iters_per_stage;
-  if (2 * n_pass * grid >= (1LL << 31)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  if (schedule < kAlternating || schedule > kSymmetricSelf) return FLASHOT_ERR_INVALID_ARG;
+  const int64_t iters = (int64_t)n_stages * iters_per_stage;
+  const int64_t barriers = 2 * (schedule == kAlternating ? 2 * iters : iters);
+  if (barriers * grid >= (1LL << 31)) return FLASHOT_ERR_NOT_IMPLEMENTED;
+  // Partial slots: two per owning CTA and row tile. The symmetric G-update keeps its own
+  // region after the F-update's.
+  auto max_slots = [](int64_t row_tiles, int64_t NT, int64_t G) {
+    const int64_t T = row_tiles * NT;
+    int64_t worst = 1;
+    for (int64_t rt = 0; rt < row_tiles; ++rt)
+      worst = std::max(worst, sk_owner((rt + 1) * NT - 1, T, G) - sk_owner(rt * NT, T, G) + 1);
+    return 2 * worst;
+  };
+  const int64_t f_region = max_slots(rtX, NTY, GF) * n_pad;
+  float2* const partial_g = partial + f_region;
+  if (schedule == kSymmetric &&
+      (size_t)(f_region + max_slots(rtY, NTX, GG) * m_pad) * sizeof(float2) > partial_bytes)
+    return FLASHOT_ERR_NOT_IMPLEMENTED;
   auto kern = bf16 ? lse_solve_short_kernel<true> : lse_solve_short_kernel<false>;
   if (set_smem(kern, dyn) != FLASHOT_OK) return FLASHOT_ERR_CUDA;
   // Every CTA must be resident at once (the grid barrier); the cooperative launch checks it
@@ -567,6 +655,8 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   P.side[0] = Side{n, n_pad, NTY, rtX * NTY, GF, alpha, la2, f, biasF, biasG};
   P.side[1] = Side{m, m_pad, NTX, rtY * NTX, GG, beta, lb2, g, biasG, biasF};
   P.partial = partial;
+  P.partial_g = partial_g;
+  P.schedule = schedule;
   P.grid_bar = words;
   P.status = status;
   P.kc = kc;

@@ -16,22 +16,29 @@ int tc_selftest_grid_wait(unsigned* status, unsigned* word, int64_t limit_ns, cu
 // barrier word (zeroed by tc_short_solve itself on `st`).
 size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad);
 
-// Every half-step of the alternating solve (n_stages x iters_per_stage iterations, F then G)
-// in one cooperative launch, for contractions of at most six 128-byte K-chunks. Inputs and
-// outputs are those of the per-pass path: xq / yq the packed clouds (n_pad / m_pad rows of dpt
-// elements), alpha / beta the squared norms, la2 / lb2 the log2 weights, biasF the F pass's
-// column bias on entry (from the initial g), f and g the potentials written. partial holds
-// max_splits x max(n_pad, m_pad) float2. Returns FLASHOT_ERR_NOT_IMPLEMENTED, having enqueued
+// Every half-step of a solve (n_stages x iters_per_stage iterations) in one cooperative
+// launch, for contractions of at most six 128-byte K-chunks. schedule: 0 alternating (f =
+// F(g), then g = G(f)); 1 symmetric (f and g both averaged with the update from the previous
+// iterate); 2 symmetric for a self-transport problem (X = Y, a = b, started from f = g: one
+// pass per iteration, g left to the caller as a copy of f). Inputs and outputs are those of
+// the per-pass path: xq / yq the packed clouds (n_pad / m_pad rows of dpt elements), alpha /
+// beta the squared norms, la2 / lb2 the log2 weights, biasF (and for the symmetric schedule
+// biasG) the first pass's column biases on entry, f and g the potentials (read too by the
+// symmetric schedule) and written. partial holds partial_bytes of scratch for the stream-K
+// partials (max_splits x max(n_pad, m_pad) float2 serve every schedule but a symmetric one
+// with many owners per row tile). Returns FLASHOT_ERR_NOT_IMPLEMENTED, having enqueued
 // nothing the per-pass path reads (at most the zeroing of sync_words), when the solve does
 // not qualify: a longer contraction, more than 32 eps stages, a grid that cannot be
 // co-resident (or a cooperative launch refused for that), fewer than 1.5 tiles per CTA and
-// pass on either side, or FLASHOT_SHORT_SOLVE=0 in the environment (FLASHOT_SHORT_SOLVE=1
-// drops the tile-count condition). The caller then runs the per-pass path.
+// pass on either side, partials that do not fit, or FLASHOT_SHORT_SOLVE=0 in the
+// environment (FLASHOT_SHORT_SOLVE=1 drops the tile-count condition). The caller then runs
+// the per-pass path.
 int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t m,
                    int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
                    const float* beta, const float* la2, const float* lb2, float* biasF,
                    float* biasG, float* f, float* g, const float* eps_sched, int n_stages,
-                   int iters_per_stage, float2* partial, int max_splits, void* sync_words,
-                   size_t sync_bytes, int sms, unsigned* status, cudaStream_t st);
+                   int iters_per_stage, int schedule, float2* partial, size_t partial_bytes,
+                   int max_splits, void* sync_words, size_t sync_bytes, int sms,
+                   unsigned* status, cudaStream_t st);
 
 }  // namespace flashot

@@ -178,3 +178,100 @@ def test_persistent_solve_random_shapes_bitwise(cuda_lib, tmp_path):
         fp, gp, lp, _ = per_pass[nm]
         assert launches == 1, nm
         assert np.array_equal(f, fp) and np.array_equal(g, gp) and loss == lp, nm
+
+
+_CHILD_SYM = r"""
+import sys
+import numpy as np, torch
+sys.path.insert(0, {root!r})
+import log_domain_sinkhorn_gb300 as lds
+data = np.load(sys.argv[1], allow_pickle=True)
+names = sorted({{k.split("/")[0] for k in data.files}})
+t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()
+out = {{}}
+for nm in names:
+    X, a = t(data[nm + "/X"]), t(data[nm + "/a"])
+    self_ot = bool(data[nm + "/self"])
+    Y, b = (X, a) if self_ot else (t(data[nm + "/Y"]), t(data[nm + "/b"]))
+    eps = [float(e) for e in data[nm + "/eps"]]
+    iters, prec = int(data[nm + "/iters"]), str(data[nm + "/prec"])
+    warm = bool(data[nm + "/warm"])
+    f0 = t(data[nm + "/f0"]) if warm else None
+    g0 = t(data[nm + "/g0"]) if warm else None
+    timer = lds.KernelTimer().start()
+    f, g, loss = lds.sinkhorn_solve(X, Y, a, b, eps, iters, precision=prec, schedule="symmetric",
+                                    f0=f0, g0=g0)
+    torch.cuda.synchronize()
+    out[nm + "/lse_launches"] = np.int64(timer.read(lds.KernelTimer.LSE)[0])
+    timer.stop()
+    out[nm + "/f"] = f.cpu().numpy()
+    out[nm + "/g"] = g.cpu().numpy()
+    out[nm + "/loss"] = np.float64(loss.cpu())
+np.savez(sys.argv[2], **out)
+"""
+
+# name: (n, m, d, precision, eps schedule, iterations per stage, self-transport, warm start)
+SYM_CASES = {
+    "sym3000x2600_d64_bf16": (3000, 2600, 64, "bf16", [8.0], 8, False, False),
+    "sym1500x2000_d64_x3_anneal": (1500, 2000, 64, "tf32x3", [16.0, 8.0, 4.0], 3, False, False),
+    "sym900x1100_d96_tf32_warm": (900, 1100, 96, "tf32", [12.0], 6, False, True),
+    "self2500_d64_bf16": (2500, 2500, 64, "bf16", [64.0], 8, True, False),
+    "self1000_d32_x3_anneal": (1000, 1000, 32, "tf32x3", [4.0, 2.0], 4, True, False),
+}
+
+
+def _sym_child(problems, tmp_path, mode):
+    arrays = {}
+    for nm, (X, Y, a, b, eps, iters, prec, self_ot, warm, f0, g0) in problems.items():
+        for k, v in (("X", X), ("Y", Y), ("a", a), ("b", b), ("f0", f0), ("g0", g0)):
+            arrays[f"{nm}/{k}"] = v
+        arrays[f"{nm}/eps"] = np.asarray(eps, np.float32)
+        arrays[f"{nm}/iters"] = np.int64(iters)
+        arrays[f"{nm}/prec"] = np.array(prec)
+        arrays[f"{nm}/self"] = np.bool_(self_ot)
+        arrays[f"{nm}/warm"] = np.bool_(warm)
+    src = tmp_path / "child_sym.py"
+    src.write_text(_CHILD_SYM.format(root=ROOT))
+    inp, outp = tmp_path / f"sym_in{mode}.npz", tmp_path / f"sym_out{mode}.npz"
+    np.savez(inp, **arrays)
+    env = dict(os.environ, FLASHOT_SHORT_SOLVE=mode)
+    r = subprocess.run([sys.executable, str(src), str(inp), str(outp)], env=env,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    out = np.load(outp)
+    return {nm: (out[nm + "/f"], out[nm + "/g"], float(out[nm + "/loss"]),
+                 int(out[nm + "/lse_launches"])) for nm in problems}
+
+
+def test_persistent_symmetric_solve_is_bitwise_the_per_pass_solve_and_matches_oracle(
+        cuda_lib, tmp_path):
+    """The symmetric (averaged) schedule in one persistent launch: both updates of an
+    iteration read the previous iterate, so their passes run back to back and merge
+    together between two grid barriers; the next iteration's biases are formed in the merge
+    from the averaged potentials. Self-transport problems (the same cloud and weights on
+    both sides) take one pass per iteration. Bits equal to the per-pass symmetric path
+    (which forms the biases in separate launches), values within tolerance of the oracle's
+    symmetric solve."""
+    problems = {}
+    for nm, (n, m, d, prec, eps, iters, self_ot, warm) in SYM_CASES.items():
+        pr = make_problem(n, m, d, x_dist="normal", y_dist="normal_shift05",
+                          weights="dirichlet1", seed=n + m + d)
+        Y, b = (pr.X, pr.a) if self_ot else (pr.Y, pr.b)
+        rng = np.random.default_rng(n)
+        f0 = (0.2 * rng.standard_normal(n)).astype(np.float32)
+        g0 = (0.2 * rng.standard_normal(Y.shape[0])).astype(np.float32)
+        problems[nm] = (pr.X, Y, pr.a, b, eps, iters, prec, self_ot, warm, f0, g0)
+    persistent = _sym_child(problems, tmp_path, "1")
+    per_pass = _sym_child(problems, tmp_path, "0")
+    for nm, (X, Y, a, b, eps, iters, prec, self_ot, warm, f0, g0) in problems.items():
+        f, g, loss, launches = persistent[nm]
+        fp, gp, lp, launches_p = per_pass[nm]
+        assert launches == 1, (nm, launches)
+        assert launches_p == (1 if self_ot else 2) * len(eps) * iters, (nm, launches_p)
+        assert np.array_equal(f, fp) and np.array_equal(g, gp) and loss == lp, nm
+        fo, go, lo = oracle.solve_symmetric(X, Y, a, b, eps, iters, f0=f0 if warm else None,
+                                            g0=g0 if warm else None)
+        assert pot_err(f, g, fo, go) <= POT_TOL[prec], (nm, pot_err(f, g, fo, go))
+        assert rel_err(loss, lo) <= LOSS_TOL[prec], (nm, loss, lo)
+        if self_ot:
+            assert np.array_equal(f, g), nm
