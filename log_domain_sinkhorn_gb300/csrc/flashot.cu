@@ -810,8 +810,8 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
                           c.at<void>(c.L.yq), n, m, c.g.n_pad, c.g.m_pad, c.g.dpt,
                           c.at<float>(c.L.alpha), c.at<float>(c.L.beta), c.at<float>(c.L.la2),
                           c.at<float>(c.L.lb2), c.at<float>(c.L.biasF), c.at<float>(c.L.biasG),
-                          f, g, eps_sched, n_stages, iters_per_stage, self ? 2 : 1,
-                          c.at<float2>(c.L.partial), partial_bytes(c.g), kMaxSplits,
+                          f, g, eps_sched, n_stages, iters_per_stage, self ? 2 : 1, nullptr,
+                          nullptr, -1, c.at<float2>(c.L.partial), partial_bytes(c.g), kMaxSplits,
                           c.at<void>(c.L.sync), tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad),
                           c.sms, c.at<unsigned>(c.L.status), c.st);
       if (rc == FLASHOT_OK) done = true;
@@ -847,7 +847,8 @@ int flashot_sinkhorn_solve(const float* X, const float* Y, const float* a, const
                         m, c.g.n_pad, c.g.m_pad, c.g.dpt, c.at<float>(c.L.alpha),
                         c.at<float>(c.L.beta), c.at<float>(c.L.la2), c.at<float>(c.L.lb2),
                         c.at<float>(c.L.biasF), c.at<float>(c.L.biasG), f, g, eps_sched,
-                        n_stages, iters_per_stage, 0, c.at<float2>(c.L.partial),
+                        n_stages, iters_per_stage, 0, nullptr, nullptr, -1,
+                        c.at<float2>(c.L.partial),
                         partial_bytes(c.g), kMaxSplits, c.at<void>(c.L.sync),
                         tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad), c.sms,
                         c.at<unsigned>(c.L.status), c.st);
@@ -898,37 +899,66 @@ int flashot_sinkhorn_solve_tol(const float* X, const float* Y, const float* a, c
   if ((rc = launch_bias(c, nullptr, false, eps)) != FLASHOT_OK) return rc;
   float* err_rows = c.at<float>(c.L.lse2);
   double* err_dev = c.at<double>(c.L.loss);
+  // The check of iteration kk: sum the error rows its f-update wrote, read the sum and the
+  // status word, and decide.
+  auto check_error = [&](int kk, bool* stop) -> int {
+    {
+      TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
+      sum_rows_kernel<<<1, 1024, 0, c.st>>>(err_rows, n, err_dev);
+    }
+    int r = launch_check();
+    if (r != FLASHOT_OK) return r;
+    double e_host = 0.0;
+    unsigned word = 0;
+    cudaError_t e = cudaMemcpyAsync(&e_host, err_dev, sizeof(double), cudaMemcpyDeviceToHost,
+                                    c.st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(&word, c.at<unsigned>(c.L.status), sizeof(word),
+                          cudaMemcpyDeviceToHost, c.st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // A kernel that gave up a bounded wait left garbage: stop (the word stays set for
+    // flashot_workspace_status).
+    if (word != 0) return FLASHOT_ERR_DEVICE_TIMEOUT;
+    if (err) *err = e_host;
+    if (err_hist) err_hist[kk / check_every - 1] = e_host;
+    *stop = e_host < tol;
+    return FLASHOT_OK;
+  };
   int k = 1;
-  for (; k <= max_iters; ++k) {
+  bool stop = false;
+  // Short tensor-core contractions, checks at least 4 iterations apart: the iterations up to
+  // each check in one persistent launch, whose check iteration's f-update writes the error
+  // rows (the same bits and decisions as the per-pass loop below, which takes over from
+  // iteration k when the launch does not apply).
+  while (c.g.prec != FLASHOT_PREC_FP32 && check_every >= 4 && !stop && k <= max_iters) {
+    const int kc = (std::max(k, 2) + check_every - 1) / check_every * check_every;
+    const int last = std::min(kc, max_iters);
+    const bool check = last == kc;
+    rc = tc_short_solve(c.g.prec == FLASHOT_PREC_BF16, c.at<void>(c.L.xq), c.at<void>(c.L.yq),
+                        n, m, c.g.n_pad, c.g.m_pad, c.g.dpt, c.at<float>(c.L.alpha),
+                        c.at<float>(c.L.beta), c.at<float>(c.L.la2), c.at<float>(c.L.lb2),
+                        c.at<float>(c.L.biasF), c.at<float>(c.L.biasG), f, g, &eps, 1,
+                        last - k + 1, 0, check ? err_rows : nullptr, c.at<float>(c.L.wa),
+                        check ? last - k : -1, c.at<float2>(c.L.partial), partial_bytes(c.g),
+                        kMaxSplits, c.at<void>(c.L.sync),
+                        tc_short_solve_sync_bytes(c.g.n_pad, c.g.m_pad), c.sms,
+                        c.at<unsigned>(c.L.status), c.st);
+    if (rc == FLASHOT_ERR_NOT_IMPLEMENTED) break;
+    if (rc != FLASHOT_OK) return rc;
+    if (check && (rc = check_error(last, &stop)) != FLASHOT_OK) return rc;
+    k = stop ? last : last + 1;
+  }
+  for (; !stop && k <= max_iters; ++k) {
     // Iteration k measures, inside its f-update, the row-marginal error of iterate k-1.
     const bool check = k >= 2 && k % check_every == 0;
     if ((rc = run_lse_pass(c, true, eps, eps, f, true, nullptr, false,
                            check ? err_rows : nullptr)) != FLASHOT_OK)
       return rc;
-    if (check) {
-      {
-        TraceScope ts_(FLASHOT_KERNEL_OTHER, c.st);
-        sum_rows_kernel<<<1, 1024, 0, c.st>>>(err_rows, n, err_dev);
-      }
-      if ((rc = launch_check()) != FLASHOT_OK) return rc;
-    }
     if ((rc = run_lse_pass(c, false, eps, eps, g, true, nullptr)) != FLASHOT_OK) return rc;
     if (check) {
-      double e_host = 0.0;
-      unsigned word = 0;
-      cudaError_t e = cudaMemcpyAsync(&e_host, err_dev, sizeof(double), cudaMemcpyDeviceToHost,
-                                      c.st);
-      if (e == cudaSuccess)
-        e = cudaMemcpyAsync(&word, c.at<unsigned>(c.L.status), sizeof(word),
-                            cudaMemcpyDeviceToHost, c.st);
-      if (e == cudaSuccess) e = cudaStreamSynchronize(c.st);
-      if (e != cudaSuccess) return cuda_fail(e);
-      // A kernel that gave up a bounded wait left garbage: stop (the word stays set for
-      // flashot_workspace_status).
-      if (word != 0) return FLASHOT_ERR_DEVICE_TIMEOUT;
-      if (err) *err = e_host;
-      if (err_hist) err_hist[k / check_every - 1] = e_host;
-      if (e_host < tol) break;
+      if ((rc = check_error(k, &stop)) != FLASHOT_OK) return rc;
+      if (stop) break;
     }
   }
   *iters_done = std::min(k, max_iters);

@@ -77,6 +77,12 @@ struct Params {
   float2* partial_g;       // symmetric: the G-update's partials (the F-update's in partial)
   unsigned* grid_bar;      // arrivals at the grid barriers, over all passes
   unsigned* status;
+  // Convergence check (alternating schedule): the merge of pass err_pass (an F-update; -1:
+  // none) also writes each row's share of the L1 row-marginal error of the previous
+  // iterate into err_rows (weights err_w), as the combine does.
+  float* err_rows;
+  const float* err_w;
+  int64_t err_pass;
   int kc, stages, a_bufs, n_stages, iters_per_stage, schedule;
   float eps[kMaxEps];
 };
@@ -472,8 +478,8 @@ lse_solve_short_kernel(const __grid_constant__ CUtensorMap mapXr,
         args.next_bias = S.next_bias;
         args.out_lse2 = nullptr;
         args.average = 0;
-        args.err_w = nullptr;
-        args.err_rows = nullptr;
+        args.err_w = p == P.err_pass ? P.err_w : nullptr;
+        args.err_rows = p == P.err_pass ? P.err_rows : nullptr;
         const SplitInfo split{0, 2, S.T, S.G, NT, kBM};
         const int64_t share = (S.rows_pad + gridDim.x - 1) / gridDim.x;
         const int64_t r_end = min(S.rows_pad, (cta + 1) * share);
@@ -584,9 +590,10 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
                    int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
                    const float* beta, const float* la2, const float* lb2, float* biasF,
                    float* biasG, float* f, float* g, const float* eps_sched, int n_stages,
-                   int iters_per_stage, int schedule, float2* partial, size_t partial_bytes,
-                   int max_splits, void* sync_words, size_t sync_bytes, int sms,
-                   unsigned* status, cudaStream_t st) {
+                   int iters_per_stage, int schedule, float* err_rows, const float* err_w,
+                   int err_iter, float2* partial, size_t partial_bytes, int max_splits,
+                   void* sync_words, size_t sync_bytes, int sms, unsigned* status,
+                   cudaStream_t st) {
   using namespace tc;
   using namespace tc::ssolve;
   // FLASHOT_SHORT_SOLVE in the environment: 0 keeps the per-pass path, 1 takes the
@@ -657,6 +664,10 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
   P.partial = partial;
   P.partial_g = partial_g;
   P.schedule = schedule;
+  P.err_rows = err_rows;
+  P.err_w = err_w;
+  P.err_pass = (schedule == kAlternating && err_rows != nullptr && err_iter >= 0) ? 2LL * err_iter
+                                                                                 : -1;
   P.grid_bar = words;
   P.status = status;
   P.kc = kc;

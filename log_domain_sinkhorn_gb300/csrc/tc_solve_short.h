@@ -20,7 +20,11 @@ size_t tc_short_solve_sync_bytes(int64_t n_pad, int64_t m_pad);
 // launch, for contractions of at most six 128-byte K-chunks. schedule: 0 alternating (f =
 // F(g), then g = G(f)); 1 symmetric (f and g both averaged with the update from the previous
 // iterate); 2 symmetric for a self-transport problem (X = Y, a = b, started from f = g: one
-// pass per iteration, g left to the caller as a copy of f). Inputs and outputs are those of
+// pass per iteration, g left to the caller as a copy of f). With err_rows != NULL and
+// err_iter >= 0 (alternating only) the f-update of iteration err_iter (counted from 0 in
+// this launch) also writes each row's share of the L1 row-marginal error of the iterate
+// before it, w_i |expm1((f_old - f_new) / eps)| with w = err_w (0 on padding rows), as
+// the per-pass combine does. Inputs and outputs are those of
 // the per-pass path: xq / yq the packed clouds (n_pad / m_pad rows of dpt elements), alpha /
 // beta the squared norms, la2 / lb2 the log2 weights, biasF (and for the symmetric schedule
 // biasG) the first pass's column biases on entry, f and g the potentials (read too by the
@@ -37,8 +41,9 @@ int tc_short_solve(bool bf16, const void* xq, const void* yq, int64_t n, int64_t
                    int64_t n_pad, int64_t m_pad, int64_t dpt, const float* alpha,
                    const float* beta, const float* la2, const float* lb2, float* biasF,
                    float* biasG, float* f, float* g, const float* eps_sched, int n_stages,
-                   int iters_per_stage, int schedule, float2* partial, size_t partial_bytes,
-                   int max_splits, void* sync_words, size_t sync_bytes, int sms,
-                   unsigned* status, cudaStream_t st);
+                   int iters_per_stage, int schedule, float* err_rows, const float* err_w,
+                   int err_iter, float2* partial, size_t partial_bytes, int max_splits,
+                   void* sync_words, size_t sync_bytes, int sms, unsigned* status,
+                   cudaStream_t st);
 
 }  // namespace flashot

@@ -275,3 +275,82 @@ def test_persistent_symmetric_solve_is_bitwise_the_per_pass_solve_and_matches_or
         assert rel_err(loss, lo) <= LOSS_TOL[prec], (nm, loss, lo)
         if self_ot:
             assert np.array_equal(f, g), nm
+
+
+_CHILD_TOL = r"""
+import sys
+import numpy as np, torch
+sys.path.insert(0, {root!r})
+import log_domain_sinkhorn_gb300 as lds
+data = np.load(sys.argv[1], allow_pickle=True)
+names = sorted({{k.split("/")[0] for k in data.files}})
+t = lambda v: torch.from_numpy(np.ascontiguousarray(v)).cuda()
+out = {{}}
+for nm in names:
+    X, Y, a, b = (t(data[nm + "/" + k]) for k in ("X", "Y", "a", "b"))
+    eps, tol = float(data[nm + "/eps"]), float(data[nm + "/tol"])
+    max_iters, every = int(data[nm + "/max_iters"]), int(data[nm + "/every"])
+    prec = str(data[nm + "/prec"])
+    timer = lds.KernelTimer().start()
+    f, g, loss, done, err, hist = lds.sinkhorn_solve_tol(X, Y, a, b, eps, tol, max_iters, every,
+                                                         precision=prec)
+    torch.cuda.synchronize()
+    out[nm + "/lse_launches"] = np.int64(timer.read(lds.KernelTimer.LSE)[0])
+    timer.stop()
+    out[nm + "/f"] = f.cpu().numpy()
+    out[nm + "/g"] = g.cpu().numpy()
+    out[nm + "/loss"] = np.float64(loss.cpu())
+    out[nm + "/done"] = np.int64(done)
+    out[nm + "/err"] = np.float64(err)
+    out[nm + "/hist"] = np.asarray(hist, np.float64)
+np.savez(sys.argv[2], **out)
+"""
+
+# name: (n, m, d, precision, eps, tol, max_iters, check_every)
+TOL_CASES = {
+    "tol3000_d64_bf16": (3000, 3000, 64, "bf16", 8.0, 1e-3, 200, 10),
+    "tol2000x2600_d64_x3": (2000, 2600, 64, "tf32x3", 6.0, 1e-4, 300, 8),
+    "tol_to_max_d96_tf32": (1500, 1700, 96, "tf32", 12.0, 1e-12, 27, 5),
+}
+
+
+def test_persistent_tol_solve_is_bitwise_the_per_pass_solve(cuda_lib, tmp_path):
+    """The convergence-driven solve with checks at least 4 iterations apart runs each check
+    interval in one persistent launch whose check iteration writes the error rows: the
+    iterate, the loss, the iteration count and every measured error equal the per-pass
+    loop's bit for bit; a run that reaches max_iters off a check boundary ends with a launch
+    that checks nothing."""
+    arrays, expect = {}, {}
+    for nm, (n, m, d, prec, eps, tol, max_iters, every) in TOL_CASES.items():
+        pr = make_problem(n, m, d, x_dist="normal", y_dist="normal_shift05",
+                          weights="dirichlet1", seed=n + m)
+        for k, v in (("X", pr.X), ("Y", pr.Y), ("a", pr.a), ("b", pr.b)):
+            arrays[f"{nm}/{k}"] = v
+        for k, v in (("eps", eps), ("tol", tol)):
+            arrays[f"{nm}/{k}"] = np.float64(v)
+        arrays[f"{nm}/max_iters"] = np.int64(max_iters)
+        arrays[f"{nm}/every"] = np.int64(every)
+        arrays[f"{nm}/prec"] = np.array(prec)
+        expect[nm] = (max_iters, every)
+    src = tmp_path / "child_tol.py"
+    src.write_text(_CHILD_TOL.format(root=ROOT))
+    res = {}
+    for mode in ("1", "0"):
+        inp, outp = tmp_path / f"tol_in{mode}.npz", tmp_path / f"tol_out{mode}.npz"
+        np.savez(inp, **arrays)
+        env = dict(os.environ, FLASHOT_SHORT_SOLVE=mode)
+        r = subprocess.run([sys.executable, str(src), str(inp), str(outp)], env=env,
+                           capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0, r.stderr[-3000:]
+        res[mode] = np.load(outp)
+    for nm, (max_iters, every) in expect.items():
+        p1, p0 = res["1"], res["0"]
+        for key in ("f", "g", "loss", "done", "err", "hist"):
+            assert np.array_equal(p1[f"{nm}/{key}"], p0[f"{nm}/{key}"]), (nm, key)
+        done = int(p1[f"{nm}/done"])
+        assert 1 <= done <= max_iters
+        # one launch per check interval (the last one possibly shorter), 2 passes per
+        # iteration on the per-pass path
+        assert int(p1[f"{nm}/lse_launches"]) == -(-done // every), nm
+        assert int(p0[f"{nm}/lse_launches"]) == 2 * done, nm
+    assert int(res["1"]["tol_to_max_d96_tf32/done"]) == 27
