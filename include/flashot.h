@@ -172,6 +172,9 @@ int flashot_sinkhorn_solve(const float *X, const float *Y, const float *a, const
  * returns FLASHOT_ERR_NOT_IMPLEMENTED. The error is formed from fp32 potentials, so it cannot
  * resolve much below ~1e-6 * max|f| / eps (the fp32 spacing of f, relative to eps).
  * Returns FLASHOT_ERR_DEVICE_TIMEOUT (and stops) if a kernel gave up a bounded wait.
+ * Launches: as flashot_sinkhorn_solve; for short tensor-core contractions with
+ * check_every >= 4, the iterations up to each check run as one cooperative launch (the same
+ * bits and decisions).
  */
 int flashot_sinkhorn_solve_tol(const float *X, const float *Y, const float *a,
                                const float *b, int64_t n, int64_t m, int64_t d, float eps,
